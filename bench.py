@@ -1,0 +1,384 @@
+"""Benchmark of the fused ZeRO optimizer step on GB300.
+
+One step = one pass of the whole path over one batch of synthetic gradients: rank-ordered
+reduce-scatter of the M bf16 gradient replicas, global-norm clip, AdamW on every owner's
+fp32 shard, all-gather of the bf16 parameters. Default workload: the 4B dense-transformer
+parameter set (4,092,982,400 params, M = 4, ZeRO-3, clip 1.0).
+
+Prints ONE JSON line (rank 0). Usage:
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 0-4] [--impl ours|reference]
+Multi-GPU: launched by torchrun, one process per GPU; every rank runs its own emulated job
+(weak scaling, no data-path collective); the barrier and the max-over-ranks timing use
+torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) per fused ZeRO step"
+KERNEL_SRC = os.path.join(ROOT, "zero_gradient_reduce_scatter_gb300", "csrc", "zero_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (timing only: barrier + max over ranks)
+# ------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "100"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------
+# byte accounting
+# ------------------------------------------------------------------------------------------
+def alg_bytes_per_param(M: int) -> int:
+    """Algorithmic bytes per parameter of one step: read M bf16 gradients and fp32 master,
+    m, v; write fp32 master, m, v and the bf16 parameter."""
+    return 2 * M + 26
+
+
+def kernel_alg_bytes_per_lane(kernel: str, M: int, write_ghat: bool) -> int:
+    return {"rs_adamw": 2 * M + 26, "adamw": 4 + 26, "rs_norm": 2 * M + (4 if write_ghat else 0),
+            "gather": 4, "norm_final": 0}[kernel]
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, workload_key: str):
+    """dram bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tab = json.load(f)
+        e = tab[kernel_key]
+        if e.get("kernel_src_sha") != kernel_sha() or e.get("workload") != workload_key:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample of the workload
+# ------------------------------------------------------------------------------------------
+def cpu_baseline(w, target_seconds=15.0):
+    import numpy as np
+    import torch
+
+    import oracle as O
+    import workloads as W
+
+    # sample: a contiguous slice of the workload's parameters, same M / stage / clip
+    lanes = 1 << 22
+    sample = W.small_variant(w, (lanes,), steps=1)
+    p = O.plan(sample.numel, sample.M, sample.bucket_bytes)
+    st = O.init_state(p, sample.stage, W.master_init(sample, "cpu").numpy())
+    oh = O.hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 clip=w.clip is not None, max_grad_norm=w.clip or 1.0)
+    sig = np.array([float(W.sigmas(w)[0])])
+    grads = []
+    for r in range(sample.M):
+        g = torch.zeros(p.npad, dtype=torch.bfloat16)
+        W.fill_grads(sample, r, 0, g, [0], sig)
+        grads.append(g.view(torch.int16).numpy().view(np.uint16))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        O.zero_step(p, st, grads, oh)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= target_seconds or done >= 64:
+            break
+    rate = done * p.N / el
+    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} oracle steps of a {p.N}-parameter slice of the workload (M={w.M}, "
+                      f"ZeRO-{w.stage}, clip {'on' if w.clip else 'off'}), single thread, {el:.1f} s"}
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import workloads as W
+    import zero_gradient_reduce_scatter_gb300 as zg
+    from zero_gradient_reduce_scatter_gb300 import _build
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    if not os.path.exists(_build.LIB_PATH):
+        if rank == 0:
+            _build.build()
+        barrier(dist, device)
+
+    w = W.config(args.config)
+    gather = "fused"
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
+                           gather=gather)
+    sig = W.sigmas(w)
+    grads = opt.new_grad_buffers()
+    for r in range(w.M):
+        W.fill_grads(w, r, 0, grads[r], opt.tensor_offsets, sig)
+    h = zg.Hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 clip=w.clip is not None, max_grad_norm=w.clip or 1.0, ghat_mode=args.ghat_mode)
+    clip = w.clip is not None
+    ghat_mode = args.ghat_mode
+    if ghat_mode == "auto":
+        ghat_mode = ("materialize" if (w.M > 4 and opt.ghat is not None) else "recompute") if clip else "none"
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        opt.step(grads, h)
+    torch.cuda.synchronize()
+    if opt.sync_status() != 0:
+        raise SystemExit("warm-up step saw a non-finite gradient norm")
+
+    # ---- timed region: K steps, device events, per-kernel events inside the library ----
+    opt.set_timing(True)
+    opt.kernel_times()  # reset
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        opt.step(grads, h)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist, device)
+    ms_total = e0.elapsed_time(e1)
+    ktimes = opt.kernel_times()
+    opt.set_timing(False)
+    ms_total_max = max_over_ranks(dist, ms_total, device)
+
+    n = w.N
+    ms_per_step = ms_total_max / args.steps
+    value = world * n * args.steps / (ms_total_max / 1e3)
+    alg_b = alg_bytes_per_param(w.M) * n
+    gbs_alg = alg_b / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    launches = int(sum(c for _, c in ktimes.values()))
+
+    # dominant kernel (largest share of the timed region)
+    dom = max((k for k in ktimes if ktimes[k][1] > 0), key=lambda k: ktimes[k][0])
+    dom_ms = ktimes[dom][0] / ktimes[dom][1]
+    lanes = opt.sizes["npad"]
+    dom_bytes = kernel_alg_bytes_per_lane(dom, w.M, ghat_mode == "materialize") * lanes
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    variant = {"rs_adamw": "rs_adamw_scaled" if clip and ghat_mode != "materialize" else "rs_adamw_plain",
+               "adamw": "adamw", "rs_norm": "rs_norm_write" if ghat_mode == "materialize" else "rs_norm_only",
+               "gather": "gather", "norm_final": "norm_final"}[dom]
+    workload_key = f"config{args.config}"
+    traffic = ncu_traffic(variant, workload_key)
+    roofline = {"bound": "hbm", "kernel": variant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
+                "kernel_share": {k: round(v[0] / max(ms_total, 1e-9), 4) for k, v in ktimes.items() if v[1]}}
+
+    # ---- end to end through the C ABI with host buffers (pinned) -----------------------
+    e2e = None
+    if not args.no_e2e:
+        host_grads = [g.cpu().pin_memory() for g in grads]
+        host_params = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+        opt.step_host(host_grads, grads, host_params, h)  # warm-up
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            opt.step_host(host_grads, grads, host_params, h)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(dist, f0.elapsed_time(f1), device)
+        e2e = {"value": world * n * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
+               "ms_per_step": e2e_ms / args.e2e_steps,
+               "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2}
+        del host_grads, host_params
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "params": n, "M": w.M, "stage": w.stage,
+                       "clip": w.clip, "bucket_bytes": w.bucket_bytes, "gather": gather, "ghat_mode": ghat_mode,
+                       "padded_lanes": lanes,
+                       "l2": f"inputs {(opt.sizes['bytes_grad_each'] * w.M + 12 * lanes) / 1e9:.1f} GB > L2 "
+                             f"{L2_BYTES / 1e6:.0f} MB; no flush",
+                       "parallelism": f"{world} independent emulated jobs (one per GPU)"},
+            "gbs_alg": round(gbs_alg, 1), "alg_bytes_per_param": alg_bytes_per_param(w.M),
+            "frac_of_peak_alg": round(gbs_alg / peak, 4),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores, a bounded sample per step
+# ------------------------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    w = W.config(args.config)
+    per_step = []
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, target_seconds=2.0)
+        per_step.append(cb)
+    timed = per_step[args.warmup:]
+    rate = statistics.median(c["value"] for c in timed) if timed else per_step[-1]["value"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.N / rate * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "params": w.N, "M": w.M, "stage": w.stage, "clip": w.clip},
+        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

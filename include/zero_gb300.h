@@ -1,0 +1,240 @@
+/*
+ * zero_gb300.h -- C ABI of the GB300 (sm_103a) ZeRO optimizer step.
+ *
+ * One call performs one data-parallel optimizer step for M emulated ranks whose bf16
+ * gradient replicas sit in one GPU's HBM:
+ *
+ *   (1) reduce-scatter: owner r of every bucket receives the average over ranks of its
+ *       slice, summed in fp32 in rank order 0..M-1 from +0 and multiplied by (float)(1/M)
+ *       ("CS336 2026 Lecture 8" notes, Slide 8: all-reduce = reduce-scatter + all-gather;
+ *       Slide 20 step 2; "并行训练优化、MoE扩展与系统瓶颈" 1.2.2 reduce_scatter_sum);
+ *   (2) optional clipping by the global L2 norm of the averaged gradient;
+ *   (3) AdamW with bias correction and decoupled weight decay on each owner's shard of
+ *       fp32 master / m / v, the 16 bytes/param mixed-precision ledger of Lecture 8
+ *       Slide 17 (Slide 20 step 3; "并行训练优化…" 2.2.1 step 3);
+ *   (4) all-gather of the updated bf16 parameters into the full, unpadded parameter buffer
+ *       (Slide 20 step 4; "并行训练优化…" 1.2.2 all_gather, 2.2.6 for ZeRO-3).
+ * ZeRO stages 1, 2 and 3 (Lecture 8 Slides 19-26; "并行训练优化…" 2.2.1-2.2.6) run the same
+ * arithmetic and differ only in which buffers persist between steps.
+ *
+ * Conventions shared by every entry point:
+ *  - Return value: ZERO_OK (0) or a negative ZERO_ERR_* code; nothing else crosses the ABI.
+ *    zero_strerror() gives the text. No call aborts or throws.
+ *  - Memory: the library allocates no device memory. The caller allocates every device
+ *    buffer in the sizes zero_plan() reports and keeps it alive while a context uses it;
+ *    the context only borrows the pointers. The context owns host tables, CUDA events for
+ *    optional kernel timing, and nothing else.
+ *  - Streams: work is enqueued on the caller's stream (a cudaStream_t passed as void*; NULL
+ *    is the legacy default stream). Calls return once the work is enqueued; only
+ *    zero_last_norm(), zero_sync_status() and zero_kernel_times() wait for the stream.
+ *  - Device: the context binds to the device that holds its buffers; calls make it current
+ *    for their duration and restore the caller's current device.
+ *  - Threads: a context must not be used from two threads at once. Different contexts are
+ *    independent.
+ *
+ * Flat layout (all lane counts are elements, not bytes):
+ *  Tensors are packed in declared order into buckets; a bucket is filled greedily up to
+ *  bucket_bytes of bf16 gradient and never splits a tensor (a larger tensor gets a bucket
+ *  of its own; bucket_bytes = 0 means a single bucket). Bucket b with n_b real lanes is
+ *  padded to M * S_b lanes, S_b = ceil(n_b / (M * ZERO_ALIGN)) * ZERO_ALIGN, and occupies
+ *  padded lanes [off_b, off_b + M * S_b); rank r owns [off_b + r * S_b, off_b + (r+1) * S_b).
+ *  Real lanes of bucket b are [off_b, off_b + n_b). npad = sum of M * S_b.
+ *  The unpadded index of real lane o of bucket b is o - off_b + (sum of n over earlier
+ *  buckets). Padding lanes of gradient buffers are ignored (read as +0); padding lanes of
+ *  master / m / v stay exactly 0; padding never reaches the unpadded parameter buffer.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------- */
+#define ZERO_OK                 0
+#define ZERO_ERR_INVALID_ARG   -1  /* null pointer, out-of-range value, bad enum        */
+#define ZERO_ERR_MISALIGNED    -2  /* a device pointer is not 16-byte aligned           */
+#define ZERO_ERR_SIZE_MISMATCH -3  /* a required buffer is missing for this config       */
+#define ZERO_ERR_STAGE         -4  /* stage not 1/2/3, or not the context's stage        */
+#define ZERO_ERR_NONFINITE     -5  /* the last clipped step saw a non-finite norm and
+                                      left the state untouched                           */
+#define ZERO_ERR_CUDA          -6  /* a CUDA runtime call failed; see zero_last_cuda_error */
+#define ZERO_ERR_BAD_CONTEXT   -7  /* null, destroyed or unknown context                 */
+#define ZERO_ERR_NOT_COMPUTED  -8  /* the requested value was not computed (no clipping)  */
+
+#define ZERO_ALIGN       64  /* shard length granule in lanes: 128 B of bf16, 256 B of fp32 */
+#define ZERO_MAX_RANKS   64  /* largest emulated rank count M                             */
+
+/* gather modes (zero_config.gather) */
+#define ZERO_GATHER_FUSED  0  /* the AdamW epilogue writes each owner's bf16 values straight
+                                 into the full parameter buffer (in-place all-gather)      */
+#define ZERO_GATHER_SHARDS 1  /* stage 3 only: the epilogue writes the persistent padded bf16
+                                 shards; a gather kernel then copies them into the full
+                                 buffer (also available on its own: zero_gather)           */
+
+/* averaged-gradient handling when clipping (zero_hyper.ghat_mode) */
+#define ZERO_GHAT_AUTO        0  /* MATERIALIZE when M > 4 and a ghat buffer exists, else
+                                    RECOMPUTE (fewer bytes in each case)                   */
+#define ZERO_GHAT_MATERIALIZE 1  /* pass 1 writes the fp32 averaged gradient; pass 2 reads it:
+                                    2M + 34 bytes per lane                                 */
+#define ZERO_GHAT_RECOMPUTE   2  /* pass 1 only sums squares; pass 2 re-reads the M bf16
+                                    gradients: 4M + 26 bytes per lane, no ghat buffer      */
+
+/* state arrays for zero_get_state */
+#define ZERO_STATE_MASTER 0
+#define ZERO_STATE_M      1
+#define ZERO_STATE_V      2
+#define ZERO_STATE_GHAT   3
+
+/* kernels reported by zero_kernel_times, in this order */
+#define ZERO_K_RS_NORM      0  /* reduce-scatter + squared-norm partials (+ ghat write)   */
+#define ZERO_K_NORM_FINAL   1  /* one CTA: norm, clip scale, non-finite flag              */
+#define ZERO_K_ADAMW        2  /* AdamW from the materialized averaged gradient           */
+#define ZERO_K_RS_ADAMW     3  /* fused reduce-scatter + AdamW (+ all-gather epilogue)     */
+#define ZERO_K_GATHER       4  /* bf16 shards -> full unpadded buffer                     */
+#define ZERO_K_INIT         5  /* state initialisation                                    */
+#define ZERO_NUM_KERNELS    6
+
+typedef struct zero_ctx zero_ctx; /* opaque, library-owned */
+
+/* Layout and persistence choices, fixed for the life of a context. */
+typedef struct {
+    int32_t M;            /* emulated data-parallel ranks, 1..ZERO_MAX_RANKS            */
+    int32_t stage;        /* ZeRO stage: 1, 2 or 3                                        */
+    int64_t bucket_bytes; /* bf16 gradient bytes per bucket; 0 = one bucket              */
+    int32_t gather;       /* ZERO_GATHER_FUSED or ZERO_GATHER_SHARDS (stage 3 only)       */
+    int32_t reserved;     /* must be 0                                                    */
+} zero_config;
+
+/* Hyper-parameters of one step. */
+typedef struct {
+    double lr;            /* >= 0                                                         */
+    double beta1, beta2;  /* in [0, 1)                                                    */
+    double eps;           /* > 0                                                          */
+    double weight_decay;  /* >= 0, decoupled: p <- p * (1 - lr * weight_decay)           */
+    double max_grad_norm; /* > 0 when clip != 0                                           */
+    int32_t clip;         /* 1: scale the averaged gradient by max_grad_norm / norm when
+                             norm > max_grad_norm; 0: no clipping and no norm             */
+    int32_t ghat_mode;    /* ZERO_GHAT_*; only used when clip != 0                         */
+} zero_hyper;
+
+/* Sizes reported by zero_plan (elements, and bytes for each caller-allocated buffer). */
+typedef struct {
+    int64_t npad;               /* padded flat length (lanes)                              */
+    int64_t n;                  /* real parameters (sum of numel)                          */
+    int64_t n_buckets;
+    int64_t shard_len;          /* lanes owned by one rank (sum of S_b)                     */
+    int64_t bytes_master;       /* fp32 npad                                               */
+    int64_t bytes_m;            /* fp32 npad                                               */
+    int64_t bytes_v;            /* fp32 npad                                               */
+    int64_t bytes_ghat;         /* fp32 npad: averaged-gradient workspace; optional        */
+    int64_t bytes_param_full;   /* bf16 n                                                  */
+    int64_t bytes_param_shards; /* bf16 npad with ZERO_GATHER_SHARDS, else 0               */
+    int64_t bytes_grad_each;    /* bf16 npad: each of the M gradient buffers               */
+    int64_t bytes_scratch;      /* status word, norm partials and the bucket table         */
+} zero_sizes;
+
+/* Device buffers borrowed by a context. All 16-byte aligned (torch allocations are). */
+typedef struct {
+    void* master;       /* fp32 [npad], owner-sharded flat layout; required                */
+    void* m;            /* fp32 [npad]; required                                           */
+    void* v;            /* fp32 [npad]; required                                           */
+    void* ghat;         /* fp32 [npad]; optional (NULL: clipped steps use RECOMPUTE)       */
+    void* param_full;   /* bf16 [n], unpadded tensor-order concatenation; required         */
+    void* param_shards; /* bf16 [npad]; required with ZERO_GATHER_SHARDS, else NULL        */
+    void* scratch;      /* bytes_scratch; required                                         */
+} zero_buffers;
+
+/* Host only, no CUDA call. Computes the layout of n_tensors tensors of numel[i] elements
+ * (numel[i] >= 0, at least one > 0) and the buffer sizes. Errors: INVALID_ARG, STAGE. */
+int zero_plan(const zero_config* cfg, const int64_t* numel, int64_t n_tensors, zero_sizes* out);
+
+/* Host only. Writes the padded start lane of each tensor (tensor_off[n_tensors]) and, if
+ * bucket_table is not NULL, four int64 per bucket: {off_b, n_b, S_b, first tensor}
+ * (bucket_table[4 * n_buckets]). A gradient for tensor i goes to lanes
+ * [tensor_off[i], tensor_off[i] + numel[i]) of each rank's buffer. */
+int zero_plan_layout(const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
+                     int64_t* tensor_off, int64_t* bucket_table);
+
+/* Creates a context over the caller's buffers and initialises the state on `stream`:
+ * master = master_init scattered into the padded layout (padding 0), m = v = 0, t = 0,
+ * param_full = bf16(master_init) (and param_shards = bf16(master) with ZERO_GATHER_SHARDS).
+ * master_init: device fp32 [n], unpadded, read during this call's kernels only.
+ * Errors: INVALID_ARG, STAGE, MISALIGNED, SIZE_MISMATCH, CUDA. On error *out is NULL. */
+int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
+              const zero_buffers* bufs, const void* master_init, void* stream);
+
+/* One optimizer step (steps (1)-(4) above), asynchronous on `stream`.
+ * grads: M device pointers, grads[r] = rank r's bf16 gradient [npad] in the padded layout,
+ * 16-byte aligned, read-only and borrowed until the stream passes this step.
+ * stage must equal the context's stage. Increments the step count t (bias correction uses
+ * the new t) even if the device later skips the update for a non-finite norm.
+ * Errors: BAD_CONTEXT, INVALID_ARG, STAGE, MISALIGNED, SIZE_MISMATCH, CUDA. */
+int zero_step(zero_ctx* ctx, const void* const* grads, int stage, const zero_hyper* hyper,
+              void* stream);
+
+/* zero_step with host-resident data: enqueues the copy of each pinned host gradient
+ * host_grads[r] (bf16 [npad]) into the device buffer dev_grads[r], the step, and the copy
+ * of the full bf16 parameters into the pinned host buffer host_params (bf16 [n]), all on
+ * `stream`. Host buffers must stay valid until the stream passes the step. */
+int zero_step_host(zero_ctx* ctx, const void* const* host_grads, void* const* dev_grads, int stage,
+                   const zero_hyper* hyper, void* host_params, void* stream);
+
+/* Device pointer of the full bf16 parameters [n] (valid until the next step). */
+int zero_params(zero_ctx* ctx, void** full_bf16);
+
+/* Stage 3 with ZERO_GATHER_SHARDS: all-gathers bucket `bucket` (or every bucket when -1)
+ * from the persistent bf16 shards into dst (device bf16 [n], unpadded; NULL = param_full).
+ * Errors: BAD_CONTEXT, INVALID_ARG (bucket out of range or no shards), CUDA. */
+int zero_gather(zero_ctx* ctx, int64_t bucket, void* dst, void* stream);
+
+/* Copies rank `rank`'s shard of state array `which` (ZERO_STATE_*), shard_len fp32 values in
+ * bucket order, into the device buffer dst. GHAT needs a ghat buffer and holds the
+ * averaged gradient of the last step that materialized it. */
+int zero_get_state(zero_ctx* ctx, int which, int rank, void* dst, void* stream);
+
+/* Waits for the last step's stream; returns its global gradient norm and clip scale.
+ * Errors: NOT_COMPUTED when the last step did not clip (or no step yet). */
+int zero_last_norm(zero_ctx* ctx, double* norm, float* scale);
+
+/* Waits for the last step's stream and returns ZERO_OK, ZERO_ERR_NONFINITE (update
+ * skipped), or ZERO_ERR_CUDA. */
+int zero_sync_status(zero_ctx* ctx);
+
+/* Step counter (number of steps taken). zero_set_step restores it from a checkpoint. */
+int zero_get_step(zero_ctx* ctx, int64_t* t);
+int zero_set_step(zero_ctx* ctx, int64_t t);
+
+/* Per-kernel timing with CUDA events on the launching stream (off by default). When on,
+ * every launch is bracketed by two events. zero_kernel_times waits for them and writes the
+ * summed milliseconds and launch counts of each ZERO_K_* kernel since the last call (each
+ * array ZERO_NUM_KERNELS long; either may be NULL), then resets the sums. */
+int zero_set_timing(zero_ctx* ctx, int on);
+int zero_kernel_times(zero_ctx* ctx, double* ms, int64_t* launches);
+
+/* Launch configuration of the streaming kernels: CTAs in the grid and threads per CTA. */
+int zero_launch_shape(zero_ctx* ctx, int* ctas, int* threads);
+
+/* Releases the context (not the caller's buffers). Waits for nothing. */
+int zero_destroy(zero_ctx* ctx);
+
+/* Text of a status code; never NULL. */
+const char* zero_strerror(int status);
+
+/* CUDA error code of the last ZERO_ERR_CUDA on this thread (0 if none). */
+int zero_last_cuda_error(void);
+
+/* Training-state bytes per parameter held by one rank: param + grad + optimizer bytes, of
+ * which ZeRO stage 1 shards the optimizer part over M ranks, stage 2 also the gradient,
+ * stage 3 everything ("CS336 2026 Lecture 8" Slides 17-28; stage 0 = plain data parallel).
+ * Returns a negative value for invalid arguments. Host only. */
+double zero_state_bytes_per_param(int stage, int M, double param_bytes, double grad_bytes,
+                                  double optim_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_GB300_H */

@@ -1,0 +1,282 @@
+"""GPU vs oracle, element by element, at sizes the oracle finishes in seconds that still
+span many CTAs' tiles, several buckets and ragged tails. Every test calls the CUDA path
+through the C ABI (libzero_gb300.so)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import zero_gradient_reduce_scatter_gb300 as zg
+from parity_util import (bf16_ulp_diff, f32, make_hyper, run_elementwise, state_errors, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    yield
+
+
+def gpt_like(d, layers, layernorm=True, vocab=1000):
+    sizes = [vocab * d]
+    for _ in range(layers):
+        if layernorm:
+            sizes += [d, d]
+        sizes += [3 * d * d, d * d]
+        if layernorm:
+            sizes += [d, d]
+        sizes += [4 * d * d, 4 * d * d]
+    if layernorm:
+        sizes += [d, d]
+    return tuple(sizes)
+
+
+def ragged(count, lo, hi, seed):
+    return W.ragged_numel(count, lo, hi, seed)
+
+
+# ------------------------------------------------------------------------------------------
+# The five workloads' recipes at reduced sizes (and the tiny one at full size)
+# ------------------------------------------------------------------------------------------
+def test_tiny_workload_full_size():
+    out = run_elementwise(W.config(0))
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_gpt2_small_recipe_multi_bucket_stage2():
+    w = W.small_variant(W.config(1), gpt_like(100, 3), bucket_bytes=150_000, steps=4)
+    p = O.plan(w.numel, w.M, w.bucket_bytes)
+    assert p.nb >= 5
+    out = run_elementwise(w)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_ragged_multi_bucket_fused_epilogue_all_alignments():
+    """Odd tensor sizes and small buckets: the unpadded start of the buckets falls on every
+    alignment class of the fused all-gather stores (16-, 8-, 4- and 2-byte)."""
+    w = W.small_variant(W.config(1), ragged(60, 50, 4000, 11), bucket_bytes=9000, steps=3, clip=1.0)
+    p = O.plan(w.numel, w.M, w.bucket_bytes)
+    shifts = {int(p.b_off[b] - sum(p.b_n[:b])) % 8 for b in range(p.nb)}
+    assert 0 in shifts and 4 in shifts and (shifts & {2, 6}) and (shifts & {1, 3, 5, 7}), shifts
+    for mode in ("materialize", "recompute"):
+        out = run_elementwise(w, ghat_mode=mode, ghat_buffer=True)
+        assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+@pytest.mark.parametrize("ghat_mode", ["materialize", "recompute"])
+def test_dense_1p3b_recipe_clip_stage1(ghat_mode):
+    w = W.small_variant(W.config(2), gpt_like(128, 2, layernorm=False, vocab=2000), steps=3)
+    out = run_elementwise(w, ghat_mode=ghat_mode, ghat_buffer=True)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+    if ghat_mode == "materialize":
+        # the reduce-scatter result is bit-exact
+        p, st, opt = out["plan"], out["oracle_state"], out["opt"]
+        got = f32(opt.ghat)
+        want = O.flat_state(p, st, "ghat")
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("gather", ["shards", "fused"])
+def test_ragged_recipe_stage3_m16(gather):
+    w = W.small_variant(W.config(3), ragged(150, 2 ** 10, 2 ** 15, 7), steps=3)
+    out = run_elementwise(w, gather=gather)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_dense_4b_recipe_stage3_m4():
+    w = W.small_variant(W.config(4), gpt_like(160, 2, layernorm=False, vocab=1500), steps=3)
+    out = run_elementwise(w)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+# ------------------------------------------------------------------------------------------
+# Edge cases
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 3, 5, 7, 16, 64])
+def test_rank_counts_including_generic_kernel(M):
+    """M outside {1,2,4,8,16} runs the generic rank loop; non-power-of-two M makes
+    (float)(1/M) inexact, which both sides apply the same way."""
+    w = W.small_variant(W.config(3), (3001, 17, 8192, 1, 555), M=M, steps=2)
+    out = run_elementwise(w, gather="shards")
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_fewer_params_than_ranks():
+    """3 real lanes over 16 ranks: 15 owners hold only padding."""
+    w = W.small_variant(W.config(3), (3,), steps=3)
+    out = run_elementwise(w, gather="shards")
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_zero_size_and_unit_tensors():
+    w = W.small_variant(W.config(1), (0, 1, 0, 1, 2, 0, 5000, 1), bucket_bytes=40, steps=2)
+    out = run_elementwise(w)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+def test_padding_garbage_is_ignored():
+    w = W.small_variant(W.config(4), (1001, 77, 3), steps=2)
+    out = run_elementwise(w, garbage_in_padding=True)
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+    # padding lanes of the state stay exactly zero
+    opt, p = out["opt"], out["plan"]
+    pad = ~p.real_mask()
+    for buf in (opt.master, opt.m, opt.v):
+        assert np.all(f32(buf)[pad] == 0.0)
+
+
+def test_large_threshold_equals_no_clip():
+    w_clip = W.small_variant(W.config(2), (20000, 3000), clip=1e9, steps=2)
+    w_off = W.small_variant(W.config(2), (20000, 3000), clip=None, steps=2)
+    a = run_elementwise(w_clip)["opt"]
+    b = run_elementwise(w_off)["opt"]
+    assert a.last_norm()[1] == 1.0
+    assert torch.equal(a.master, b.master) and torch.equal(a.params(), b.params())
+
+
+def test_nonfinite_gradient_skips_step_and_reports():
+    w = W.small_variant(W.config(4), (4096, 100), steps=1)
+    dev = torch.device("cuda")
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    before = opt.master.clone()
+    grads = opt.new_grad_buffers()
+    for r in range(w.M):
+        W.fill_grads(w, r, 0, grads[r], opt.tensor_offsets)
+    grads[2].view(torch.int16)[opt.tensor_offsets[1] + 5] = 0x7F80  # +inf on rank 2
+    h, _ = make_hyper(w)
+    opt.step(grads, h)
+    assert opt.sync_status() == zg.ZERO_ERR_NONFINITE
+    assert not math.isfinite(opt.last_norm()[0])
+    assert torch.equal(opt.master, before)
+    # the next finite step proceeds
+    grads[2].view(torch.int16)[opt.tensor_offsets[1] + 5] = 0
+    opt.step(grads, h)
+    assert opt.sync_status() == 0 and not torch.equal(opt.master, before)
+
+
+def test_deterministic_rerun():
+    w = W.small_variant(W.config(2), gpt_like(64, 2, layernorm=False, vocab=3000), steps=2)
+    a = run_elementwise(w)
+    b = run_elementwise(w)
+    assert a["opt"].last_norm() == b["opt"].last_norm()
+    assert torch.equal(a["opt"].master, b["opt"].master)
+
+
+def test_invalid_step_arguments_rejected_on_host():
+    w = W.small_variant(W.config(0), (4096,), steps=1)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")))
+    grads = opt.new_grad_buffers()
+    h, _ = make_hyper(w)
+    with pytest.raises(zg.ZeroError) as e:
+        opt.step(grads, h, stage=3)
+    assert e.value.code == -4
+    for bad in (zg.Hyper(lr=-1.0), zg.Hyper(beta1=1.0), zg.Hyper(eps=0.0), zg.Hyper(clip=True, max_grad_norm=0.0)):
+        with pytest.raises(zg.ZeroError) as e:
+            opt.step(grads, bad)
+        assert e.value.code == -1
+    # misaligned gradient pointer
+    shifted = torch.zeros(opt.sizes["npad"] + 1, dtype=torch.bfloat16, device="cuda")[1:]
+    with pytest.raises(zg.ZeroError) as e:
+        opt.step([grads[0], shifted], h)
+    assert e.value.code == -2
+    # use after destroy
+    import ctypes
+    raw = ctypes.c_void_p(opt._ctx.value)
+    opt.close()
+    lib = zg._lib()
+    assert lib.zero_step(raw, ctypes.cast(opt._grad_ptrs, ctypes.c_void_p), 1, ctypes.byref(h), None) == -7
+    assert lib.zero_destroy(raw) == -7
+
+
+# ------------------------------------------------------------------------------------------
+# Other entry points: per-rank state, per-bucket gather, host-buffer step, step counter
+# ------------------------------------------------------------------------------------------
+def test_get_state_per_rank_matches_oracle_shards():
+    w = W.small_variant(W.config(2), (5000, 123, 9000), bucket_bytes=12000, steps=2)
+    out = run_elementwise(w, ghat_mode="materialize", ghat_buffer=True)
+    opt, st = out["opt"], out["oracle_state"]
+    for r in range(w.M):
+        for name, arr in (("master", st.master), ("m", st.mom), ("v", st.var), ("ghat", st.ghat)):
+            got = f32(opt.get_state(name, r))
+            assert np.array_equal(got.view(np.uint32), arr[r][:out["plan"].shard_len].view(np.uint32)), (name, r)
+
+
+def test_gather_per_bucket_rebuilds_params():
+    w = W.small_variant(W.config(3), ragged(40, 100, 3000, 3), bucket_bytes=8000, steps=2)
+    out = run_elementwise(w, gather="shards")
+    opt, p = out["opt"], out["plan"]
+    assert p.nb > 3
+    dst = torch.full((p.N,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    for b in range(p.nb):
+        opt.gather_params(b, dst)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(dst), u16(opt.params()))
+
+
+def test_step_from_host_buffers_equals_device_step():
+    w = W.small_variant(W.config(4), (70000, 13), steps=2)
+    dev = torch.device("cuda")
+    a = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    b = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    h, _ = make_hyper(w)
+    dev_grads = a.new_grad_buffers()
+    host_params = torch.empty(a.sizes["n"], dtype=torch.bfloat16).pin_memory()
+    for k in range(w.steps):
+        grads = b.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, grads[r], b.tensor_offsets)
+        host = [g.cpu().pin_memory() for g in grads]
+        b.step(grads, h)
+        a.step_host(host, dev_grads, host_params, h)
+        torch.cuda.synchronize()
+        assert torch.equal(host_params, b.params().cpu())
+        assert torch.equal(a.master, b.master)
+
+
+def test_step_counter_and_resume():
+    """K steps == K1 steps, save (state + t), restore into a fresh context, K2 steps."""
+    w = W.small_variant(W.config(2), (30000, 5000), steps=4)
+    dev = torch.device("cuda")
+    h, _ = make_hyper(w)
+    sig = W.sigmas(w)
+
+    def grads_for(opt, k):
+        gs = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, gs[r], opt.tensor_offsets, sig)
+        return gs
+
+    ref = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    for k in range(4):
+        ref.step(grads_for(ref, k), h)
+    first = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    for k in range(2):
+        first.step(grads_for(first, k), h)
+    saved = (first.master.clone(), first.m.clone(), first.v.clone(), first.t)
+    resumed = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    resumed.master.copy_(saved[0]), resumed.m.copy_(saved[1]), resumed.v.copy_(saved[2])
+    resumed.t = saved[3]
+    assert resumed.t == 2
+    for k in range(2, 4):
+        resumed.step(grads_for(resumed, k), h)
+    torch.cuda.synchronize()
+    assert torch.equal(resumed.master, ref.master) and torch.equal(resumed.params(), ref.params())
+
+
+def test_kernel_timing_counts_launches():
+    w = W.small_variant(W.config(2), (200000,), steps=1)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")), ghat_buffer=True)
+    grads = opt.new_grad_buffers()
+    h, _ = make_hyper(w)
+    opt.set_timing(True)
+    for _ in range(3):
+        opt.step(grads, h)
+    t = opt.kernel_times()
+    assert t["rs_norm"][1] == 3 and t["norm_final"][1] == 3 and t["adamw"][1] == 3 and t["rs_adamw"][1] == 0
+    assert all(v[0] > 0 for k, v in t.items() if v[1])

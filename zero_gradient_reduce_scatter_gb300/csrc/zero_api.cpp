@@ -1,0 +1,642 @@
+// zero_api.cpp -- host side of the C ABI declared in include/zero_gb300.h: the flat-layout
+// planner, argument validation, step orchestration and optional per-kernel event timing.
+// All arithmetic of the step runs in the kernels of zero_kernels.cu; this file only forms
+// the per-step scalars and launches.
+//
+// Built with -ffp-contract=off so the step scalars are plain IEEE double operations.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "zero_gb300.h"
+#include "zero_internal.h"
+
+struct zero_ctx {
+    zero_config cfg;
+    int device;
+    int sm_count;
+    // layout
+    std::vector<int64_t> numel;
+    std::vector<int64_t> tensor_off;
+    std::vector<zg::Bucket> buckets;  // host copy of the device table
+    int64_t npad, n, shard_len;
+    // borrowed device buffers
+    zero_buffers bufs;
+    zg::Status* status;
+    double* partials;
+    zg::Bucket* dev_buckets;
+    // step state
+    int64_t t;
+    int last_clip;
+    cudaStream_t last_stream;
+    int stepped;
+    // launch shapes, per kernel variant (0 = not computed yet)
+    int grid[zg::kNumVariants];
+    // timing
+    int timing;
+    struct TimedLaunch {
+        int kernel;
+        cudaEvent_t start, stop;
+    };
+    std::vector<TimedLaunch> events;  // pool; the first `n_timed` are in use
+    size_t n_timed;
+};
+
+namespace {
+
+std::mutex g_live_mu;
+std::unordered_set<const zero_ctx*> g_live;  // contexts not yet destroyed
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return ZERO_ERR_CUDA;
+}
+
+bool live(const zero_ctx* c) {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    return c && g_live.count(c);
+}
+
+// Makes `dev` current for the lifetime of the guard and restores the caller's device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------------------
+// Planner. Tensors in declared order; a new bucket opens before a non-empty tensor that
+// would push a non-empty bucket past bucket_bytes of bf16 gradient; each bucket is padded
+// to a multiple of M * ZERO_ALIGN lanes.
+// ---------------------------------------------------------------------------------------
+struct Layout {
+    std::vector<int64_t> tensor_off;
+    std::vector<int64_t> first_tensor;
+    std::vector<zg::Bucket> buckets;
+    int64_t npad = 0, n = 0, shard_len = 0;
+};
+
+int check_config(const zero_config* cfg) {
+    if (!cfg) return ZERO_ERR_INVALID_ARG;
+    if (cfg->stage < 1 || cfg->stage > 3) return ZERO_ERR_STAGE;
+    if (cfg->M < 1 || cfg->M > ZERO_MAX_RANKS) return ZERO_ERR_INVALID_ARG;
+    if (cfg->bucket_bytes < 0 || cfg->reserved != 0) return ZERO_ERR_INVALID_ARG;
+    if (cfg->gather != ZERO_GATHER_FUSED && cfg->gather != ZERO_GATHER_SHARDS) return ZERO_ERR_INVALID_ARG;
+    if (cfg->gather == ZERO_GATHER_SHARDS && cfg->stage != 3) return ZERO_ERR_STAGE;
+    return ZERO_OK;
+}
+
+int make_layout(const zero_config* cfg, const int64_t* numel, int64_t n_tensors, Layout* L) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (!numel || n_tensors <= 0) return ZERO_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int64_t i = 0; i < n_tensors; ++i) {
+        if (numel[i] < 0 || numel[i] > (int64_t(1) << 40)) return ZERO_ERR_INVALID_ARG;
+        total += numel[i];
+    }
+    if (total <= 0 || total > (int64_t(1) << 42)) return ZERO_ERR_INVALID_ARG;
+
+    const int64_t M = cfg->M, cap = cfg->bucket_bytes;
+    L->tensor_off.assign((size_t)n_tensors, 0);
+    std::vector<int64_t> bucket_real;  // real lanes per bucket
+    int64_t open_bytes = 0;
+    for (int64_t i = 0; i < n_tensors; ++i) {
+        const int64_t bytes = 2 * numel[i];
+        const bool fresh = bucket_real.empty() ||
+                           (cap > 0 && bytes > 0 && open_bytes > 0 && open_bytes + bytes > cap);
+        if (fresh) {
+            L->first_tensor.push_back(i);
+            bucket_real.push_back(0);
+            open_bytes = 0;
+        }
+        L->tensor_off[(size_t)i] = bucket_real.back();  // relative; made absolute below
+        bucket_real.back() += numel[i];
+        open_bytes += bytes;
+    }
+    const int64_t granule = M * ZERO_ALIGN;
+    int64_t off = 0, uoff = 0, shard = 0;
+    for (size_t b = 0; b < bucket_real.size(); ++b) {
+        const int64_t nb = bucket_real[b];
+        const int64_t S = (nb + granule - 1) / granule * ZERO_ALIGN;
+        L->buckets.push_back(zg::Bucket{off, nb, off + M * S, uoff});
+        off += M * S;
+        uoff += nb;
+        shard += S;
+    }
+    for (size_t b = 0; b < bucket_real.size(); ++b) {
+        const int64_t last = (b + 1 < bucket_real.size()) ? L->first_tensor[b + 1] : n_tensors;
+        for (int64_t i = L->first_tensor[b]; i < last; ++i) L->tensor_off[(size_t)i] += L->buckets[b].off;
+    }
+    L->npad = off;
+    L->n = uoff;
+    L->shard_len = shard;
+    return ZERO_OK;
+}
+
+void fill_sizes(const zero_config* cfg, const Layout& L, zero_sizes* s) {
+    s->npad = L.npad;
+    s->n = L.n;
+    s->n_buckets = (int64_t)L.buckets.size();
+    s->shard_len = L.shard_len;
+    s->bytes_master = s->bytes_m = s->bytes_v = 4 * L.npad;
+    s->bytes_ghat = 4 * L.npad;
+    s->bytes_param_full = 2 * L.n;
+    s->bytes_param_shards = (cfg->gather == ZERO_GATHER_SHARDS) ? 2 * L.npad : 0;
+    s->bytes_grad_each = 2 * L.npad;
+    s->bytes_scratch = zg::scratch_bytes((int64_t)L.buckets.size());
+}
+
+// ---------------------------------------------------------------------------------------
+// Per-step scalars of AdamW (double, rounded once to float).
+// ---------------------------------------------------------------------------------------
+zg::AdamConsts adam_consts(const zero_hyper* h, int64_t t) {
+    const double bc1 = 1.0 - std::pow(h->beta1, (double)t);
+    const double bc2 = 1.0 - std::pow(h->beta2, (double)t);
+    zg::AdamConsts k;
+    k.b1 = (float)h->beta1;
+    k.b2 = (float)h->beta2;
+    k.c1 = (float)(1.0 - h->beta1);
+    k.c2 = (float)(1.0 - h->beta2);
+    k.step = (float)(h->lr / bc1);
+    k.isb = (float)(1.0 / std::sqrt(bc2));
+    k.decay = (float)(1.0 - h->lr * h->weight_decay);
+    k.eps = (float)h->eps;
+    return k;
+}
+
+int check_hyper(const zero_hyper* h) {
+    if (!h) return ZERO_ERR_INVALID_ARG;
+    if (!(std::isfinite(h->lr) && h->lr >= 0.0)) return ZERO_ERR_INVALID_ARG;
+    if (!(h->beta1 >= 0.0 && h->beta1 < 1.0 && h->beta2 >= 0.0 && h->beta2 < 1.0)) return ZERO_ERR_INVALID_ARG;
+    if (!(std::isfinite(h->eps) && h->eps > 0.0)) return ZERO_ERR_INVALID_ARG;
+    if (!(std::isfinite(h->weight_decay) && h->weight_decay >= 0.0)) return ZERO_ERR_INVALID_ARG;
+    if (h->clip != 0 && h->clip != 1) return ZERO_ERR_INVALID_ARG;
+    if (h->clip && !(std::isfinite(h->max_grad_norm) && h->max_grad_norm > 0.0)) return ZERO_ERR_INVALID_ARG;
+    if (h->ghat_mode < ZERO_GHAT_AUTO || h->ghat_mode > ZERO_GHAT_RECOMPUTE) return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
+}
+
+// Grid of a streaming kernel: every SM filled with as many CTAs as fit, no more CTAs than
+// work items, at most kMaxPartials (the norm pass writes one partial per CTA).
+int grid_for(zero_ctx* c, int variant, int64_t work_items) {
+    if (c->grid[variant] == 0) {
+        int per_sm = 0;
+        if (zg::variant_blocks_per_sm(variant, c->cfg.M, &per_sm) != cudaSuccess || per_sm < 1) per_sm = 1;
+        int g = per_sm * c->sm_count;
+        if (g > zg::kMaxPartials) g = zg::kMaxPartials;
+        c->grid[variant] = g;
+    }
+    int64_t need = (work_items + zg::kThreads - 1) / zg::kThreads;
+    if (need < 1) need = 1;
+    return (int)(need < c->grid[variant] ? need : c->grid[variant]);
+}
+
+// Event timing around one launch.
+struct Timed {
+    zero_ctx* c;
+    cudaStream_t s;
+    zero_ctx::TimedLaunch* ev = nullptr;
+    Timed(zero_ctx* ctx, int kernel, cudaStream_t stream) : c(ctx), s(stream) {
+        if (!c->timing) return;
+        if (c->n_timed == c->events.size()) {
+            zero_ctx::TimedLaunch tl{kernel, nullptr, nullptr};
+            if (cudaEventCreate(&tl.start) != cudaSuccess) return;
+            if (cudaEventCreate(&tl.stop) != cudaSuccess) {
+                cudaEventDestroy(tl.start);
+                return;
+            }
+            c->events.push_back(tl);
+        }
+        ev = &c->events[c->n_timed++];
+        ev->kernel = kernel;
+        cudaEventRecord(ev->start, s);
+    }
+    ~Timed() {
+        if (ev) cudaEventRecord(ev->stop, s);
+    }
+};
+
+zg::StepArgs base_args(zero_ctx* c) {
+    zg::StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.master = (float*)c->bufs.master;
+    a.m = (float*)c->bufs.m;
+    a.v = (float*)c->bufs.v;
+    a.ghat = (float*)c->bufs.ghat;
+    const bool shards = c->cfg.gather == ZERO_GATHER_SHARDS;
+    a.out = (uint16_t*)(shards ? c->bufs.param_shards : c->bufs.param_full);
+    a.out_shards = shards ? 1 : 0;
+    a.buckets = c->dev_buckets;
+    a.nb = (int64_t)c->buckets.size();
+    a.nvec = c->npad / 8;
+    a.M = c->cfg.M;
+    a.inv_M = (float)(1.0 / (double)c->cfg.M);
+    a.status = c->status;
+    a.partials = c->partials;
+    return a;
+}
+
+int gather_range(zero_ctx* c, int64_t u_begin, int64_t u_end, uint16_t* dst, cudaStream_t s) {
+    const int grid = grid_for(c, zg::kVarGather, (u_end - u_begin + 7) / 8 + 1);
+    Timed tm(c, ZERO_K_GATHER, s);
+    cudaError_t e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, dst, c->dev_buckets,
+                                      (int64_t)c->buckets.size(), c->npad, u_begin, u_end, grid, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int zero_plan(const zero_config* cfg, const int64_t* numel, int64_t n_tensors, zero_sizes* out) {
+    if (!out) return ZERO_ERR_INVALID_ARG;
+    Layout L;
+    int rc = make_layout(cfg, numel, n_tensors, &L);
+    if (rc) return rc;
+    fill_sizes(cfg, L, out);
+    return ZERO_OK;
+}
+
+int zero_plan_layout(const zero_config* cfg, const int64_t* numel, int64_t n_tensors, int64_t* tensor_off,
+                     int64_t* bucket_table) {
+    if (!tensor_off) return ZERO_ERR_INVALID_ARG;
+    Layout L;
+    int rc = make_layout(cfg, numel, n_tensors, &L);
+    if (rc) return rc;
+    std::memcpy(tensor_off, L.tensor_off.data(), sizeof(int64_t) * (size_t)n_tensors);
+    if (bucket_table) {
+        for (size_t b = 0; b < L.buckets.size(); ++b) {
+            const zg::Bucket& e = L.buckets[b];
+            bucket_table[4 * b + 0] = e.off;
+            bucket_table[4 * b + 1] = e.n;
+            bucket_table[4 * b + 2] = (e.end - e.off) / cfg->M;
+            bucket_table[4 * b + 3] = L.first_tensor[b];
+        }
+    }
+    return ZERO_OK;
+}
+
+int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
+              const zero_buffers* bufs, const void* master_init, void* stream) {
+    if (!out) return ZERO_ERR_INVALID_ARG;
+    *out = nullptr;
+    Layout L;
+    int rc = make_layout(cfg, numel, n_tensors, &L);
+    if (rc) return rc;
+    if (!bufs || !master_init) return ZERO_ERR_INVALID_ARG;
+    if (!bufs->master || !bufs->m || !bufs->v || !bufs->param_full || !bufs->scratch) return ZERO_ERR_SIZE_MISMATCH;
+    if (cfg->gather == ZERO_GATHER_SHARDS && !bufs->param_shards) return ZERO_ERR_SIZE_MISMATCH;
+    const void* must_align[] = {bufs->master, bufs->m, bufs->v, bufs->ghat, bufs->param_full, bufs->param_shards,
+                                bufs->scratch, master_init};
+    for (const void* p : must_align)
+        if (p && !aligned16(p)) return ZERO_ERR_MISALIGNED;
+
+    // The device that holds the buffers.
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, bufs->master);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return ZERO_ERR_INVALID_ARG;
+    const int dev = attr.device;
+    DeviceGuard guard(dev);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    zero_ctx* c = new (std::nothrow) zero_ctx();
+    if (!c) return ZERO_ERR_INVALID_ARG;
+    c->cfg = *cfg;
+    c->device = dev;
+    c->sm_count = sms;
+    c->numel.assign(numel, numel + n_tensors);
+    c->tensor_off = L.tensor_off;
+    c->buckets = L.buckets;
+    c->npad = L.npad;
+    c->n = L.n;
+    c->shard_len = L.shard_len;
+    c->bufs = *bufs;
+    if (cfg->gather != ZERO_GATHER_SHARDS) c->bufs.param_shards = nullptr;
+    char* scratch = (char*)bufs->scratch;
+    c->status = (zg::Status*)(scratch + zg::kScratchStatus);
+    c->partials = (double*)(scratch + zg::kScratchPartials);
+    c->dev_buckets = (zg::Bucket*)(scratch + zg::kScratchBuckets);
+    c->t = 0;
+    c->last_clip = 0;
+    c->last_stream = (cudaStream_t)stream;
+    c->stepped = 0;
+    std::memset(c->grid, 0, sizeof c->grid);
+    c->timing = 0;
+    c->n_timed = 0;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    zg::Status zero_status;
+    std::memset(&zero_status, 0, sizeof zero_status);
+    zero_status.scale = 1.0f;
+    // Pageable-source copies: the runtime stages the host data before returning.
+    e = cudaMemcpyAsync(c->status, &zero_status, sizeof zero_status, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->dev_buckets, c->buckets.data(), sizeof(zg::Bucket) * c->buckets.size(),
+                            cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+        const int grid = grid_for(c, zg::kVarInit, c->npad);
+        Timed tm(c, ZERO_K_INIT, s);
+        e = zg::launch_init((const float*)master_init, (float*)c->bufs.master, (float*)c->bufs.m,
+                            (float*)c->bufs.v, (uint16_t*)c->bufs.param_full, (uint16_t*)c->bufs.param_shards,
+                            c->dev_buckets, (int64_t)c->buckets.size(), c->npad, grid, s);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // host tables above must outlive the copies
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e);
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        g_live.insert(c);
+    }
+    *out = c;
+    return ZERO_OK;
+}
+
+int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper* h, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    if (!grads) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < c->cfg.M; ++r) {
+        if (!grads[r]) return ZERO_ERR_INVALID_ARG;
+        if (!aligned16(grads[r])) return ZERO_ERR_MISALIGNED;
+    }
+    int mode = ZERO_GHAT_RECOMPUTE;
+    if (h->clip) {
+        mode = h->ghat_mode;
+        if (mode == ZERO_GHAT_AUTO) mode = (c->cfg.M > 4 && c->bufs.ghat) ? ZERO_GHAT_MATERIALIZE : ZERO_GHAT_RECOMPUTE;
+        if (mode == ZERO_GHAT_MATERIALIZE && !c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    }
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    c->t += 1;
+    zg::StepArgs a = base_args(c);
+    for (int r = 0; r < c->cfg.M; ++r) a.grads[r] = (const uint16_t*)grads[r];
+    a.k = adam_consts(h, c->t);
+
+    cudaError_t e = cudaSuccess;
+    if (h->clip) {
+        const bool write = mode == ZERO_GHAT_MATERIALIZE;
+        const int g1 = grid_for(c, write ? zg::kVarRsNormWrite : zg::kVarRsNormOnly, a.nvec);
+        {
+            Timed tm(c, ZERO_K_RS_NORM, s);
+            e = zg::launch_rs_norm(a, write, g1, s);
+        }
+        if (e == cudaSuccess) {
+            Timed tm(c, ZERO_K_NORM_FINAL, s);
+            e = zg::launch_norm_final(c->status, c->partials, g1, h->max_grad_norm, 1, s);
+        }
+        if (e == cudaSuccess) {
+            if (write) {
+                const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
+                Timed tm(c, ZERO_K_ADAMW, s);
+                e = zg::launch_adamw(a, g3, s);
+            } else {
+                const int g4 = grid_for(c, zg::kVarRsAdamwScaled, a.nvec);
+                Timed tm(c, ZERO_K_RS_ADAMW, s);
+                e = zg::launch_rs_adamw(a, true, g4, s);
+            }
+        }
+    } else {
+        const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.nvec);
+        Timed tm(c, ZERO_K_RS_ADAMW, s);
+        e = zg::launch_rs_adamw(a, false, g4, s);
+    }
+    if (e == cudaSuccess && c->cfg.gather == ZERO_GATHER_SHARDS) {
+        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);
+        if (rc) return rc;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->last_clip = h->clip;
+    c->last_stream = s;
+    c->stepped = 1;
+    return ZERO_OK;
+}
+
+int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
+                   const zero_hyper* h, void* host_params, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!host_grads || !dev_grads || !host_params) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < c->cfg.M; ++r)
+        if (!host_grads[r] || !dev_grads[r]) return ZERO_ERR_INVALID_ARG;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t gbytes = (size_t)(2 * c->npad);
+    for (int r = 0; r < c->cfg.M; ++r) {
+        cudaError_t e = cudaMemcpyAsync(dev_grads[r], host_grads[r], gbytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    rc = zero_step(c, (const void* const*)dev_grads, stage, h, stream);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(host_params, c->bufs.param_full, (size_t)(2 * c->n), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
+int zero_params(zero_ctx* c, void** full_bf16) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!full_bf16) return ZERO_ERR_INVALID_ARG;
+    *full_bf16 = c->bufs.param_full;
+    return ZERO_OK;
+}
+
+int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.gather != ZERO_GATHER_SHARDS) return ZERO_ERR_INVALID_ARG;
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (bucket < -1 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
+    if (dst && !aligned16(dst)) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    uint16_t* out = (uint16_t*)(dst ? dst : c->bufs.param_full);
+    int64_t u0 = 0, u1 = c->n;
+    if (bucket >= 0) {
+        u0 = c->buckets[(size_t)bucket].uoff;
+        u1 = u0 + c->buckets[(size_t)bucket].n;
+    }
+    return gather_range(c, u0, u1, out, (cudaStream_t)stream);
+}
+
+int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!dst || rank < 0 || rank >= c->cfg.M) return ZERO_ERR_INVALID_ARG;
+    const float* src = nullptr;
+    switch (which) {
+        case ZERO_STATE_MASTER: src = (const float*)c->bufs.master; break;
+        case ZERO_STATE_M: src = (const float*)c->bufs.m; break;
+        case ZERO_STATE_V: src = (const float*)c->bufs.v; break;
+        case ZERO_STATE_GHAT: src = (const float*)c->bufs.ghat; break;
+        default: return ZERO_ERR_INVALID_ARG;
+    }
+    if (!src) return ZERO_ERR_SIZE_MISMATCH;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    float* d = (float*)dst;
+    for (const zg::Bucket& e : c->buckets) {
+        const int64_t S = (e.end - e.off) / c->cfg.M;
+        cudaError_t ce = cudaMemcpyAsync(d, src + e.off + rank * S, sizeof(float) * (size_t)S,
+                                         cudaMemcpyDeviceToDevice, s);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        d += S;
+    }
+    return ZERO_OK;
+}
+
+static int read_status(zero_ctx* c, zg::Status* out) {
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaError_t e = cudaMemcpyAsync(out, c->status, sizeof *out, cudaMemcpyDeviceToHost, c->last_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
+int zero_last_norm(zero_ctx* c, double* norm, float* scale) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!norm || !scale) return ZERO_ERR_INVALID_ARG;
+    if (!c->stepped || !c->last_clip) return ZERO_ERR_NOT_COMPUTED;
+    zg::Status st;
+    int rc = read_status(c, &st);
+    if (rc) return rc;
+    *norm = st.norm;
+    *scale = st.scale;
+    return ZERO_OK;
+}
+
+int zero_sync_status(zero_ctx* c) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    zg::Status st;
+    int rc = read_status(c, &st);
+    if (rc) return rc;
+    if (c->stepped && c->last_clip && (st.flags & zg::kFlagNonfinite)) return ZERO_ERR_NONFINITE;
+    return ZERO_OK;
+}
+
+int zero_get_step(zero_ctx* c, int64_t* t) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!t) return ZERO_ERR_INVALID_ARG;
+    *t = c->t;
+    return ZERO_OK;
+}
+
+int zero_set_step(zero_ctx* c, int64_t t) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (t < 0) return ZERO_ERR_INVALID_ARG;
+    c->t = t;
+    return ZERO_OK;
+}
+
+int zero_set_timing(zero_ctx* c, int on) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    c->timing = on ? 1 : 0;
+    return ZERO_OK;
+}
+
+int zero_kernel_times(zero_ctx* c, double* ms, int64_t* launches) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    double acc[ZERO_NUM_KERNELS] = {0};
+    int64_t cnt[ZERO_NUM_KERNELS] = {0};
+    for (size_t i = 0; i < c->n_timed; ++i) {
+        zero_ctx::TimedLaunch& tl = c->events[i];
+        cudaError_t e = cudaEventSynchronize(tl.stop);
+        float t = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, tl.start, tl.stop);
+        if (e != cudaSuccess) {
+            c->n_timed = 0;
+            return cuda_fail(e);
+        }
+        acc[tl.kernel] += (double)t;
+        cnt[tl.kernel] += 1;
+    }
+    c->n_timed = 0;
+    for (int k = 0; k < ZERO_NUM_KERNELS; ++k) {
+        if (ms) ms[k] = acc[k];
+        if (launches) launches[k] = cnt[k];
+    }
+    return ZERO_OK;
+}
+
+int zero_launch_shape(zero_ctx* c, int* ctas, int* threads) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (ctas) *ctas = grid_for(c, zg::kVarRsAdamwPlain, c->npad / 8);
+    if (threads) *threads = zg::kThreads;
+    return ZERO_OK;
+}
+
+int zero_destroy(zero_ctx* c) {
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        if (!c || !g_live.count(c)) return ZERO_ERR_BAD_CONTEXT;
+        g_live.erase(c);
+    }
+    {
+        DeviceGuard guard(c->device);
+        for (auto& tl : c->events) {
+            cudaEventDestroy(tl.start);
+            cudaEventDestroy(tl.stop);
+        }
+    }
+    delete c;
+    return ZERO_OK;
+}
+
+const char* zero_strerror(int status) {
+    switch (status) {
+        case ZERO_OK: return "ok";
+        case ZERO_ERR_INVALID_ARG: return "invalid argument";
+        case ZERO_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case ZERO_ERR_SIZE_MISMATCH: return "a buffer this configuration needs is missing";
+        case ZERO_ERR_STAGE: return "stage must be 1, 2 or 3 and match the context";
+        case ZERO_ERR_NONFINITE: return "non-finite gradient norm: the update was skipped";
+        case ZERO_ERR_CUDA: return "CUDA runtime error (see zero_last_cuda_error)";
+        case ZERO_ERR_BAD_CONTEXT: return "null, destroyed or unknown context";
+        case ZERO_ERR_NOT_COMPUTED: return "value not computed by the last step";
+        default: return "unknown status";
+    }
+}
+
+int zero_last_cuda_error(void) { return g_last_cuda_error; }
+
+double zero_state_bytes_per_param(int stage, int M, double param_bytes, double grad_bytes, double optim_bytes) {
+    if (M < 1 || param_bytes < 0 || grad_bytes < 0 || optim_bytes < 0) return -1.0;
+    switch (stage) {
+        case 0: return param_bytes + grad_bytes + optim_bytes;
+        case 1: return param_bytes + grad_bytes + optim_bytes / M;
+        case 2: return param_bytes + (grad_bytes + optim_bytes) / M;
+        case 3: return (param_bytes + grad_bytes + optim_bytes) / M;
+        default: return -1.0;
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Internal declarations shared by the host API (zero_api.cpp) and the kernels
+// (zero_kernels.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "zero_gb300.h"
+
+namespace zg {
+
+// One bucket of the flat layout, as the kernels see it (32 bytes).
+//   padded lanes [off, end) with end = off + M * S; real lanes [off, off + n);
+//   the real lane o maps to unpadded index o - off + uoff.
+struct Bucket {
+    int64_t off;
+    int64_t n;
+    int64_t end;
+    int64_t uoff;
+};
+
+// Device status word at the start of the scratch buffer. Written by the norm-finalise
+// kernel; read by the update kernels and, after a stream synchronisation, by the host.
+struct Status {
+    double sumsq;   // sum of squared averaged gradient over real lanes
+    double norm;    // sqrt(sumsq)
+    float scale;    // clip scale applied to the averaged gradient
+    int32_t flags;  // kFlagNonfinite
+    int64_t reserved[13];
+};
+static_assert(sizeof(Status) == 128, "status word is 128 bytes");
+
+constexpr int32_t kFlagNonfinite = 1;
+
+// Step constants of AdamW, formed on the host in double and rounded once to float.
+struct AdamConsts {
+    float b1, b2, c1, c2, step, isb, decay, eps;
+};
+
+// Everything a streaming kernel needs; passed by value (kernel parameter space).
+struct StepArgs {
+    const uint16_t* grads[ZERO_MAX_RANKS];  // M bf16 gradient buffers, padded layout
+    float* master;
+    float* m;
+    float* v;
+    float* ghat;          // fp32 averaged gradient (materialized mode) or nullptr
+    uint16_t* out;        // param_full (unpadded) or param_shards (padded)
+    const Bucket* buckets;
+    int64_t nb;
+    int64_t nvec;         // npad / 8: work items of 8 lanes (16 B of bf16)
+    int32_t M;
+    float inv_M;          // (float)(1.0 / M)
+    int32_t out_shards;   // 1: `out` is the padded shard buffer; 0: the unpadded full buffer
+    int32_t reserved;
+    AdamConsts k;
+    Status* status;
+    double* partials;     // one fp64 partial sum of squares per CTA of the norm pass
+};
+
+// Scratch layout (bytes from the scratch base; every part 256-byte aligned).
+constexpr int kThreads = 256;         // threads per CTA of the streaming kernels
+constexpr int kMaxPartials = 4096;    // largest grid of the norm pass
+constexpr int64_t kScratchStatus = 0;
+constexpr int64_t kScratchPartials = 256;
+constexpr int64_t kScratchBuckets = kScratchPartials + 8 * kMaxPartials;
+inline int64_t scratch_bytes(int64_t n_buckets) {
+    int64_t b = kScratchBuckets + 32 * n_buckets;
+    return (b + 255) / 256 * 256;
+}
+
+// Kernel variants, used as keys of the per-context launch-shape cache.
+enum KernelVariant : int {
+    kVarRsNormWrite = 0,  // reduce-scatter + norm partials + write ghat
+    kVarRsNormOnly,       // reduce-scatter + norm partials
+    kVarAdamw,            // AdamW from ghat
+    kVarRsAdamwScaled,    // fused, applies the device clip scale
+    kVarRsAdamwPlain,     // fused, no clipping
+    kVarGather,
+    kVarInit,
+    kNumVariants
+};
+
+// Largest number of CTAs of `variant` (for rank count M) resident on one SM.
+cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks);
+
+// Launchers. `grid` CTAs of kThreads threads on `stream`.
+cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
+cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm,
+                              int clip, cudaStream_t s);
+cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
+// Copies bf16 shards (padded) into the unpadded full buffer for unpadded indices
+// [u_begin, u_end).
+cudaError_t launch_gather(const uint16_t* shards, uint16_t* full, const Bucket* buckets, int64_t nb,
+                          int64_t npad, int64_t u_begin, int64_t u_end, int grid, cudaStream_t s);
+// Initial state from the unpadded fp32 master vector.
+cudaError_t launch_init(const float* master_init, float* master, float* m, float* v,
+                        uint16_t* full, uint16_t* shards, const Bucket* buckets, int64_t nb,
+                        int64_t npad, int grid, cudaStream_t s);
+
+}  // namespace zg

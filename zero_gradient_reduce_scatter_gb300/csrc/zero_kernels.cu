@@ -1,0 +1,541 @@
+// zero_kernels.cu -- sm_103a kernels of the ZeRO optimizer step.
+//
+// Everything here is HBM-bandwidth bound: per lane the step moves 2M bytes of bf16
+// gradient, 12 bytes of fp32 state in and 12 out, and 2 bytes of bf16 parameter out, for
+// about 10 flops. There is no contraction, so no tensor cores: the kernels are grid-stride
+// streams of 16-byte vector accesses with evict-first cache hints, one "vec" of 8 lanes
+// (16 B of bf16, 32 B of fp32) per thread per iteration, grids of (SMs x resident CTAs).
+//
+// Reduction order is fixed so that results are bit-identical to a plain CPU evaluation:
+// the M rank values of a lane are added in rank order 0..M-1 to a +0.0f accumulator,
+// multiplied once by (float)(1/M), and every AdamW operation is an explicitly rounded
+// IEEE operation (__fadd_rn, __fmul_rn, __fsqrt_rn, __fdiv_rn), so nvcc cannot contract
+// any of them into an FMA.
+//
+// Sources: "CS336 2026 Lecture 8" notes, Slides 8 and 19-26 (reduce-scatter, owner update,
+// all-gather; ZeRO stages); "并行训练优化、MoE扩展与系统瓶颈" 1.2.2 and 2.2.1-2.2.6.
+
+#include <cuda_bf16.h>
+
+#include "zero_internal.h"
+
+namespace zg {
+namespace {
+
+// ---------------------------------------------------------------------------------------
+// bf16 helpers: bf16 is the upper half of a binary32, so widening is a shift.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two bf16 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Streaming (evict-first) vector accesses.
+__device__ __forceinline__ uint4 ld_u4(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ float4 ld_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ void st_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
+__device__ __forceinline__ void st_u4(uint16_t* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
+
+// ---------------------------------------------------------------------------------------
+// Bucket cursor: which bucket a (non-decreasing) lane index falls in.
+// ---------------------------------------------------------------------------------------
+struct Cursor {
+    const Bucket* tab;
+    int64_t nb;
+    int64_t b;
+    Bucket e;
+
+    // Last bucket whose padded start is <= lane (empty buckets share their successor's start).
+    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t lane) {
+        tab = t;
+        nb = n;
+        int64_t lo = 0, hi = n - 1;
+        while (lo < hi) {
+            int64_t mid = (lo + hi + 1) >> 1;
+            if (tab[mid].off <= lane) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+        e = tab[b];
+    }
+    __device__ __forceinline__ void seek(int64_t lane) {
+        while (lane >= e.end && b + 1 < nb) {
+            ++b;
+            e = tab[b];
+        }
+    }
+    // Real lanes of the vec starting at lane o (0..8).
+    __device__ __forceinline__ int nreal(int64_t o) const {
+        int64_t r = e.off + e.n - o;
+        return r <= 0 ? 0 : (r >= 8 ? 8 : (int)r);
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// Reduce-scatter of one vec: acc[i] = sum over ranks (in order) of the bf16 values.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void add8(float acc[8], uint4 q) {
+    acc[0] = __fadd_rn(acc[0], bf_lo(q.x));
+    acc[1] = __fadd_rn(acc[1], bf_hi(q.x));
+    acc[2] = __fadd_rn(acc[2], bf_lo(q.y));
+    acc[3] = __fadd_rn(acc[3], bf_hi(q.y));
+    acc[4] = __fadd_rn(acc[4], bf_lo(q.z));
+    acc[5] = __fadd_rn(acc[5], bf_hi(q.z));
+    acc[6] = __fadd_rn(acc[6], bf_lo(q.w));
+    acc[7] = __fadd_rn(acc[7], bf_hi(q.w));
+}
+
+template <int MT>
+__device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t o, float acc[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
+    if constexpr (MT > 0) {
+        uint4 q[MT];
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_u4(a.grads[r] + o);
+#pragma unroll
+        for (int r = 0; r < MT; ++r) add8(acc, q[r]);
+    } else {
+        int r = 0;
+        for (; r + 4 <= a.M; r += 4) {
+            uint4 q0 = ld_u4(a.grads[r] + o), q1 = ld_u4(a.grads[r + 1] + o);
+            uint4 q2 = ld_u4(a.grads[r + 2] + o), q3 = ld_u4(a.grads[r + 3] + o);
+            add8(acc, q0);
+            add8(acc, q1);
+            add8(acc, q2);
+            add8(acc, q3);
+        }
+        for (; r < a.M; ++r) add8(acc, ld_u4(a.grads[r] + o));
+    }
+}
+
+// Averaged gradient of the vec; padding lanes are +0 whatever the buffers hold.
+__device__ __forceinline__ void average8(const float acc[8], float inv_M, int nreal, float gh[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) gh[i] = (i < nreal) ? __fmul_rn(acc[i], inv_M) : 0.0f;
+}
+
+// ---------------------------------------------------------------------------------------
+// AdamW of one lane (decoupled weight decay, bias correction; eps after the square root).
+// ---------------------------------------------------------------------------------------
+template <bool SCALE>
+__device__ __forceinline__ void adam_lane(float gh, float s, float& p, float& m, float& v,
+                                          const AdamConsts& k) {
+    const float g = SCALE ? __fmul_rn(s, gh) : gh;
+    const float m1 = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.c1, g));
+    const float v1 = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.c2, __fmul_rn(g, g)));
+    const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v1), k.isb), k.eps);
+    p = __fsub_rn(__fmul_rn(p, k.decay), __fmul_rn(k.step, __fdiv_rn(m1, den)));
+    m = m1;
+    v = v1;
+}
+
+template <bool SCALE>
+__device__ __forceinline__ void adam_vec(const float gh[8], float s, float p[8], float m[8], float v[8],
+                                         const AdamConsts& k) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) adam_lane<SCALE>(gh[i], s, p[i], m[i], v[i], k);
+}
+
+__device__ __forceinline__ void unpack(float4 a, float4 b, float x[8]) {
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void load_state(const StepArgs& a, int64_t o, float p[8], float m[8], float v[8]) {
+    float4 p0 = ld_f4(a.master + o), p1 = ld_f4(a.master + o + 4);
+    float4 m0 = ld_f4(a.m + o), m1 = ld_f4(a.m + o + 4);
+    float4 v0 = ld_f4(a.v + o), v1 = ld_f4(a.v + o + 4);
+    unpack(p0, p1, p);
+    unpack(m0, m1, m);
+    unpack(v0, v1, v);
+}
+
+__device__ __forceinline__ void store_state(const StepArgs& a, int64_t o, const float p[8], const float m[8],
+                                            const float v[8]) {
+    st_f4(a.master + o, make_float4(p[0], p[1], p[2], p[3]));
+    st_f4(a.master + o + 4, make_float4(p[4], p[5], p[6], p[7]));
+    st_f4(a.m + o, make_float4(m[0], m[1], m[2], m[3]));
+    st_f4(a.m + o + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_f4(a.v + o, make_float4(v[0], v[1], v[2], v[3]));
+    st_f4(a.v + o + 4, make_float4(v[4], v[5], v[6], v[7]));
+}
+
+// ---------------------------------------------------------------------------------------
+// All-gather epilogue: the owner writes its updated bf16 values either into its padded
+// shard (ZeRO-3 shard mode) or straight to their place in the unpadded full buffer.
+// The unpadded address of a vec is shifted by the padding of earlier buckets, so its
+// alignment is that of (u0 mod 8): the widest aligned stores are used.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void store_params(const StepArgs& a, const Cursor& c, int64_t o, int nreal,
+                                             const float p[8]) {
+    const uint32_t w0 = pack_bf16x2(p[0], p[1]), w1 = pack_bf16x2(p[2], p[3]);
+    const uint32_t w2 = pack_bf16x2(p[4], p[5]), w3 = pack_bf16x2(p[6], p[7]);
+    if (a.out_shards) {
+        st_u4(a.out + o, make_uint4(w0, w1, w2, w3));
+        return;
+    }
+    if (nreal <= 0) return;
+    const int64_t u0 = o - c.e.off + c.e.uoff;
+    uint16_t* dst = a.out + u0;
+    if (nreal == 8) {
+        const int al = (int)(u0 & 7);
+        if (al == 0) {
+            st_u4(dst, make_uint4(w0, w1, w2, w3));
+        } else if (al == 4) {
+            __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w0, w1));
+            __stcs(reinterpret_cast<uint2*>(dst + 4), make_uint2(w2, w3));
+        } else if ((al & 1) == 0) {
+            unsigned int* d = reinterpret_cast<unsigned int*>(dst);
+            __stcs(d, w0);
+            __stcs(d + 1, w1);
+            __stcs(d + 2, w2);
+            __stcs(d + 3, w3);
+        } else {
+            unsigned short* d = reinterpret_cast<unsigned short*>(dst);
+            __stcs(d + 0, (unsigned short)(w0 & 0xFFFF));
+            __stcs(d + 1, (unsigned short)(w0 >> 16));
+            __stcs(d + 2, (unsigned short)(w1 & 0xFFFF));
+            __stcs(d + 3, (unsigned short)(w1 >> 16));
+            __stcs(d + 4, (unsigned short)(w2 & 0xFFFF));
+            __stcs(d + 5, (unsigned short)(w2 >> 16));
+            __stcs(d + 6, (unsigned short)(w3 & 0xFFFF));
+            __stcs(d + 7, (unsigned short)(w3 >> 16));
+        }
+        return;
+    }
+    const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < nreal) dst[i] = (uint16_t)((w[i >> 1] >> (16 * (i & 1))) & 0xFFFF);
+}
+
+// ---------------------------------------------------------------------------------------
+// Squared-norm accumulation. Each square is split exactly as x*x = p + err (p the rounded
+// product, err = fma(x, x, -p), the two-product of Dekker 1971); the p are summed with
+// Kahan's (1965) compensated fp32 summation and the tiny err terms plainly. A thread's
+// total is formed in fp64, and threads and CTAs are combined in fp64 in a fixed order.
+// ---------------------------------------------------------------------------------------
+struct SumSq {
+    float s = 0.0f, c = 0.0f, e = 0.0f;
+    __device__ __forceinline__ void add_square(float x) {
+        const float p = __fmul_rn(x, x);
+        e = __fadd_rn(e, __fmaf_rn(x, x, -p));
+        const float y = __fsub_rn(p, c);
+        const float t = __fadd_rn(s, y);
+        c = __fsub_rn(__fsub_rn(t, s), y);
+        s = t;
+    }
+    __device__ __forceinline__ void add8(const float g[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) add_square(g[i]);
+    }
+    __device__ __forceinline__ double value() const { return ((double)s - (double)c) + (double)e; }
+};
+
+// Sum over the CTA in a fixed order; the result is valid in thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+    __shared__ double warp_sums[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xFFFFFFFFu, x, off);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) warp_sums[warp] = x;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t += warp_sums[w];
+    }
+    return t;
+}
+
+// ---------------------------------------------------------------------------------------
+// K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
+// ---------------------------------------------------------------------------------------
+template <int MT, bool WRITE>
+__global__ void __launch_bounds__(kThreads) k_rs_norm(const StepArgs a) {
+    SumSq acc;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (vi < a.nvec) {
+        Cursor c;
+        c.init(a.buckets, a.nb, vi * 8);
+        for (; vi < a.nvec; vi += stride) {
+            const int64_t o = vi * 8;
+            c.seek(o);
+            float sum[8], gh[8];
+            rank_sum<MT>(a, o, sum);
+            average8(sum, a.inv_M, c.nreal(o), gh);
+            if (WRITE) {
+                st_f4(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
+                st_f4(a.ghat + o + 4, make_float4(gh[4], gh[5], gh[6], gh[7]));
+            }
+            acc.add8(gh);
+        }
+    }
+    const double t = block_sum(acc.value());
+    if (threadIdx.x == 0) a.partials[blockIdx.x] = t;
+}
+
+// ---------------------------------------------------------------------------------------
+// K2: one CTA. Global norm = sqrt(sum of partials); clip scale c / norm when norm > c.
+// A non-finite norm raises the flag that makes the update kernels skip the step.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_norm_final(Status* st, const double* partials, int nparts,
+                                                         double max_norm, int clip) {
+    __shared__ double sm[kThreads];
+    double x = 0.0;
+    for (int i = threadIdx.x; i < nparts; i += kThreads) x += partials[i];
+    sm[threadIdx.x] = x;
+    __syncthreads();
+    for (int h = kThreads / 2; h > 0; h >>= 1) {
+        if (threadIdx.x < h) sm[threadIdx.x] += sm[threadIdx.x + h];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double sumsq = sm[0];
+        const double norm = sqrt(sumsq);
+        const bool finite = isfinite(norm);
+        st->sumsq = sumsq;
+        st->norm = norm;
+        st->flags = finite ? 0 : kFlagNonfinite;
+        st->scale = (clip && finite && norm > max_norm) ? (float)(max_norm / norm) : 1.0f;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K3: AdamW from the materialized fp32 average (clipped, two-pass form).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_adamw(const StepArgs a) {
+    if (a.status->flags & kFlagNonfinite) return;
+    const float s = a.status->scale;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (vi >= a.nvec) return;
+    Cursor c;
+    c.init(a.buckets, a.nb, vi * 8);
+    for (; vi < a.nvec; vi += stride) {
+        const int64_t o = vi * 8;
+        c.seek(o);
+        float gh[8], p[8], m[8], v[8];
+        const float4 g0 = ld_f4(a.ghat + o), g1 = ld_f4(a.ghat + o + 4);
+        load_state(a, o, p, m, v);
+        unpack(g0, g1, gh);
+        adam_vec<true>(gh, s, p, m, v, a.k);
+        store_state(a, o, p, m, v);
+        store_params(a, c, o, c.nreal(o), p);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K4: fused reduce-scatter + AdamW + all-gather epilogue: the averaged gradient never
+// leaves registers. SCALE applies the clip scale computed by K2 (recompute form).
+// ---------------------------------------------------------------------------------------
+template <int MT, bool SCALE>
+__global__ void __launch_bounds__(kThreads) k_rs_adamw(const StepArgs a) {
+    float s = 1.0f;
+    if (SCALE) {
+        if (a.status->flags & kFlagNonfinite) return;
+        s = a.status->scale;
+    }
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (vi >= a.nvec) return;
+    Cursor c;
+    c.init(a.buckets, a.nb, vi * 8);
+    for (; vi < a.nvec; vi += stride) {
+        const int64_t o = vi * 8;
+        c.seek(o);
+        float sum[8], gh[8], p[8], m[8], v[8];
+        rank_sum<MT>(a, o, sum);
+        load_state(a, o, p, m, v);
+        const int nr = c.nreal(o);
+        average8(sum, a.inv_M, nr, gh);
+        adam_vec<SCALE>(gh, s, p, m, v, a.k);
+        store_state(a, o, p, m, v);
+        store_params(a, c, o, nr, p);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K5: all-gather of the padded bf16 shards into the unpadded full buffer, over unpadded
+// indices [u_begin, u_end). Work item: 8 destination elements (one 16-byte store). When
+// its source run is unaligned by k elements, two aligned 16-byte loads are spliced.
+// ---------------------------------------------------------------------------------------
+// Last bucket whose unpadded start is <= u (buckets are never empty for a valid plan).
+__device__ __forceinline__ int64_t bucket_of_unpadded(const Bucket* tab, int64_t nb, int64_t u) {
+    int64_t lo = 0, hi = nb - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (tab[mid].uoff <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint4 splice(uint4 A, uint4 B, int k) {
+    const uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+    switch (k) {
+        case 1: return make_uint4(__byte_perm(w[0], w[1], 0x5432), __byte_perm(w[1], w[2], 0x5432),
+                                  __byte_perm(w[2], w[3], 0x5432), __byte_perm(w[3], w[4], 0x5432));
+        case 2: return make_uint4(w[1], w[2], w[3], w[4]);
+        case 3: return make_uint4(__byte_perm(w[1], w[2], 0x5432), __byte_perm(w[2], w[3], 0x5432),
+                                  __byte_perm(w[3], w[4], 0x5432), __byte_perm(w[4], w[5], 0x5432));
+        case 4: return make_uint4(w[2], w[3], w[4], w[5]);
+        case 5: return make_uint4(__byte_perm(w[2], w[3], 0x5432), __byte_perm(w[3], w[4], 0x5432),
+                                  __byte_perm(w[4], w[5], 0x5432), __byte_perm(w[5], w[6], 0x5432));
+        case 6: return make_uint4(w[3], w[4], w[5], w[6]);
+        case 7: return make_uint4(__byte_perm(w[3], w[4], 0x5432), __byte_perm(w[4], w[5], 0x5432),
+                                  __byte_perm(w[5], w[6], 0x5432), __byte_perm(w[6], w[7], 0x5432));
+        default: return A;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_gather(const uint16_t* __restrict__ shards,
+                                                     uint16_t* __restrict__ full, const Bucket* tab, int64_t nb,
+                                                     int64_t npad, int64_t u_begin, int64_t u_end) {
+    const int64_t w_first = u_begin >> 3, w_last = (u_end + 7) >> 3;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t wi = w_first + (int64_t)blockIdx.x * kThreads + threadIdx.x; wi < w_last; wi += stride) {
+        const int64_t u = wi * 8;
+        const int64_t b = bucket_of_unpadded(tab, nb, u);
+        const Bucket e = tab[b];
+        if (u >= u_begin && u + 8 <= u_end && u >= e.uoff && u + 8 <= e.uoff + e.n) {
+            const int64_t src = u - e.uoff + e.off;
+            const int k = (int)(src & 7);
+            const uint16_t* base = shards + (src - k);
+            if (k == 0) {
+                st_u4(full + u, ld_u4(base));
+                continue;
+            }
+            if (src - k + 8 < npad) {
+                st_u4(full + u, splice(ld_u4(base), ld_u4(base + 8), k));
+                continue;
+            }
+        }
+        for (int i = 0; i < 8; ++i) {
+            const int64_t uu = u + i;
+            if (uu < u_begin || uu >= u_end) continue;
+            const Bucket f = tab[bucket_of_unpadded(tab, nb, uu)];
+            full[uu] = shards[uu - f.uoff + f.off];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Initial state: master = unpadded init scattered into the padded layout (padding 0),
+// m = v = 0, bf16 copies of the parameters. One lane per thread (not a hot kernel).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_init(const float* __restrict__ init, float* master, float* m,
+                                                   float* v, uint16_t* full, uint16_t* shards, const Bucket* tab,
+                                                   int64_t nb, int64_t npad) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t o = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (o >= npad) return;
+    Cursor c;
+    c.init(tab, nb, o);
+    for (; o < npad; o += stride) {
+        c.seek(o);
+        const bool real = o < c.e.off + c.e.n;
+        const int64_t u = o - c.e.off + c.e.uoff;
+        const float x = real ? init[u] : 0.0f;
+        master[o] = x;
+        m[o] = 0.0f;
+        v[o] = 0.0f;
+        const uint16_t h = to_bf16(x);
+        if (shards) shards[o] = h;
+        if (real && full) full[u] = h;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Dispatch on the rank count: fully unrolled variants for M in {1, 2, 4, 8, 16}, a generic
+// loop otherwise.
+// ---------------------------------------------------------------------------------------
+template <template <int> class F>
+struct ByM {
+    static auto get(int M) {
+        switch (M) {
+            case 1: return F<1>::fn();
+            case 2: return F<2>::fn();
+            case 4: return F<4>::fn();
+            case 8: return F<8>::fn();
+            case 16: return F<16>::fn();
+            default: return F<0>::fn();
+        }
+    }
+};
+
+template <int MT> struct RsNormWrite { static auto fn() { return &k_rs_norm<MT, true>; } };
+template <int MT> struct RsNormOnly { static auto fn() { return &k_rs_norm<MT, false>; } };
+template <int MT> struct RsAdamwScaled { static auto fn() { return &k_rs_adamw<MT, true>; } };
+template <int MT> struct RsAdamwPlain { static auto fn() { return &k_rs_adamw<MT, false>; } };
+
+const void* variant_fn(int variant, int M) {
+    switch (variant) {
+        case kVarRsNormWrite: return (const void*)ByM<RsNormWrite>::get(M);
+        case kVarRsNormOnly: return (const void*)ByM<RsNormOnly>::get(M);
+        case kVarAdamw: return (const void*)&k_adamw;
+        case kVarRsAdamwScaled: return (const void*)ByM<RsAdamwScaled>::get(M);
+        case kVarRsAdamwPlain: return (const void*)ByM<RsAdamwPlain>::get(M);
+        case kVarGather: return (const void*)&k_gather;
+        case kVarInit: return (const void*)&k_init;
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks) {
+    const void* fn = variant_fn(variant, M);
+    if (!fn) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads, 0);
+}
+
+cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
+    if (write_ghat) ByM<RsNormWrite>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    else ByM<RsNormOnly>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm, int clip,
+                              cudaStream_t s) {
+    k_norm_final<<<1, kThreads, 0, s>>>(st, partials, nparts, max_norm, clip);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s) {
+    k_adamw<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
+    if (apply_scale) ByM<RsAdamwScaled>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    else ByM<RsAdamwPlain>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* shards, uint16_t* full, const Bucket* buckets, int64_t nb, int64_t npad,
+                          int64_t u_begin, int64_t u_end, int grid, cudaStream_t s) {
+    if (u_end <= u_begin) return cudaSuccess;
+    k_gather<<<grid, kThreads, 0, s>>>(shards, full, buckets, nb, npad, u_begin, u_end);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_init(const float* master_init, float* master, float* m, float* v, uint16_t* full,
+                        uint16_t* shards, const Bucket* buckets, int64_t nb, int64_t npad, int grid,
+                        cudaStream_t s) {
+    if (npad <= 0) return cudaSuccess;
+    k_init<<<grid, kThreads, 0, s>>>(master_init, master, m, v, full, shards, buckets, nb, npad);
+    return cudaGetLastError();
+}
+
+}  // namespace zg
