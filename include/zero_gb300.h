@@ -64,9 +64,12 @@ extern "C" {
 #define ZERO_ERR_CUDA          -6  /* a CUDA runtime call failed; see zero_last_cuda_error */
 #define ZERO_ERR_BAD_CONTEXT   -7  /* null, destroyed or unknown context                 */
 #define ZERO_ERR_NOT_COMPUTED  -8  /* the requested value was not computed (no clipping)  */
+#define ZERO_ERR_TOO_LARGE     -9  /* more buckets than zero_grad_norm_noalloc's fixed
+                                      scratch holds (ZERO_NOALLOC_MAX_BUCKETS)            */
 
 #define ZERO_ALIGN       64  /* shard length granule in lanes: 128 B of bf16, 256 B of fp32 */
 #define ZERO_MAX_RANKS   64  /* largest emulated rank count M                             */
+#define ZERO_NOALLOC_MAX_BUCKETS 2048  /* bucket-table rows zero_grad_norm_noalloc can hold  */
 
 /* gather modes (zero_config.gather) */
 #define ZERO_GATHER_FUSED  0  /* the AdamW epilogue writes each owner's bf16 values straight
@@ -226,6 +229,38 @@ const char* zero_strerror(int status);
 
 /* CUDA error code of the last ZERO_ERR_CUDA on this thread (0 if none). */
 int zero_last_cuda_error(void);
+
+/* Global L2 norm of the averaged gradient and its clip scale, without any allocation.
+ *
+ * This entry point has no counterpart in the pages; it exists for callers that cannot
+ * allocate device memory -- code running where cudaMalloc is not allowed or not possible
+ * (inside an allocator or memory-manager callback, under a host runtime that owns every
+ * device allocation and hands out only fixed buffers, or in tools that must not change the
+ * process's memory footprint). It computes what a clipped zero_step computes first: the
+ * norm over real lanes of the rank-ordered fp32 average of the M bf16 gradients, and
+ * scale = max_grad_norm / norm when norm > max_grad_norm, else 1.
+ *
+ * It takes no context and no scratch buffer: its scratch (status word, per-CTA partial
+ * sums, bucket table: 98,560 bytes) is a fixed array inside the library image, which every
+ * GPU that loads the library holds until the process exits. It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *  grads         M device pointers, bf16 [npad] each in the padded layout, 16-byte aligned
+ *  M             1..ZERO_MAX_RANKS
+ *  bucket_table  host array, 4 int64 per bucket {off_b, n_b, S_b, unused} as written by
+ *                zero_plan_layout; buckets must tile [0, npad) from lane 0
+ *  n_buckets     1..ZERO_NOALLOC_MAX_BUCKETS; more returns ZERO_ERR_TOO_LARGE
+ *  norm_out      device double (8-byte aligned), receives the norm
+ *  scale_out     device float (4-byte aligned), receives the clip scale
+ * Asynchronous on `stream`. The first call on a device also does that device's set-up
+ * (looks up the fixed array's device address and the launch shape); make that first call
+ * before any stream capture. All calls share the one array, which keeps the last call's
+ * contents; nothing in it has to start at zero (every value a call reads is written
+ * earlier in the same call). Calls whose work overlaps on the GPU -- on different streams,
+ * or from different threads -- race on the array and must be serialised by the caller.
+ * Errors: INVALID_ARG, MISALIGNED, TOO_LARGE, CUDA. */
+int zero_grad_norm_noalloc(const void* const* grads, int M, const int64_t* bucket_table,
+                           int64_t n_buckets, double max_grad_norm, double* norm_out,
+                           float* scale_out, void* stream);
 
 /* Training-state bytes per parameter held by one rank: param + grad + optimizer bytes, of
  * which ZeRO stage 1 shards the optimizer part over M ranks, stage 2 also the gradient,

@@ -34,7 +34,7 @@ ZERO_OK = 0
 ERRORS = {
     -1: "ZERO_ERR_INVALID_ARG", -2: "ZERO_ERR_MISALIGNED", -3: "ZERO_ERR_SIZE_MISMATCH",
     -4: "ZERO_ERR_STAGE", -5: "ZERO_ERR_NONFINITE", -6: "ZERO_ERR_CUDA", -7: "ZERO_ERR_BAD_CONTEXT",
-    -8: "ZERO_ERR_NOT_COMPUTED",
+    -8: "ZERO_ERR_NOT_COMPUTED", -9: "ZERO_ERR_TOO_LARGE",
 }
 ZERO_ERR_NONFINITE = -5
 ZERO_ERR_NOT_COMPUTED = -8
@@ -110,6 +110,7 @@ SIGNATURES = {
     "zero_last_cuda_error": (ctypes.c_int, []),
     "zero_state_bytes_per_param": (ctypes.c_double, [ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                      ctypes.c_double, ctypes.c_double]),
+    "zero_grad_norm_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, ctypes.c_double, _P, _P, _P]),
 }
 
 

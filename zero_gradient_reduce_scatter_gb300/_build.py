@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libzero_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["zero_kernels.cu", "zero_api.cpp"]
+SOURCES = ["zero_kernels.cu", "zero_api.cpp", "zero_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -50,15 +50,20 @@ struct zero_ctx {
 };
 
 namespace {
-
-std::mutex g_live_mu;
-std::unordered_set<const zero_ctx*> g_live;  // contexts not yet destroyed
 thread_local int g_last_cuda_error = 0;
+}  // namespace
 
-int cuda_fail(cudaError_t e) {
+int zg::record_cuda_error(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return ZERO_ERR_CUDA;
 }
+
+namespace {
+
+std::mutex g_live_mu;
+std::unordered_set<const zero_ctx*> g_live;  // contexts not yet destroyed
+
+int cuda_fail(cudaError_t e) { return zg::record_cuda_error(e); }
 
 bool live(const zero_ctx* c) {
     std::lock_guard<std::mutex> lk(g_live_mu);
@@ -622,6 +627,7 @@ const char* zero_strerror(int status) {
         case ZERO_ERR_CUDA: return "CUDA runtime error (see zero_last_cuda_error)";
         case ZERO_ERR_BAD_CONTEXT: return "null, destroyed or unknown context";
         case ZERO_ERR_NOT_COMPUTED: return "value not computed by the last step";
+        case ZERO_ERR_TOO_LARGE: return "layout exceeds the fixed scratch of zero_grad_norm_noalloc";
         default: return "unknown status";
     }
 }

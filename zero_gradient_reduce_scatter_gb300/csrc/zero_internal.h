@@ -81,6 +81,9 @@ enum KernelVariant : int {
     kNumVariants
 };
 
+// Records a CUDA error for zero_last_cuda_error() and returns ZERO_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Largest number of CTAs of `variant` (for rank count M) resident on one SM.
 cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks);
 
