@@ -46,7 +46,26 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
+    ap.add_argument("--max-params", type=int, default=0,
+                    help="keep only the workload's leading tensors up to this many parameters (a small "
+                         "case of the same kernels, for profiling); 0 = the whole workload")
     return ap.parse_args()
+
+
+def workload(args):
+    import workloads as W
+    w = W.config(args.config)
+    if args.max_params and args.max_params < w.N:
+        keep, total = [], 0
+        for n in w.numel:
+            if total + n > args.max_params:
+                if not keep:
+                    keep.append(args.max_params)
+                break
+            keep.append(n)
+            total += n
+        w = W.small_variant(w, tuple(keep), name=f"{w.name}; leading {sum(keep):,} parameters only")
+    return w
 
 
 # ------------------------------------------------------------------------------------------
@@ -59,12 +78,17 @@ def dist_env():
     return world, rank, local
 
 
-def dist_init(world, use_cuda):
+def dist_init(world, use_cuda, timeout_s: float | None = None):
+    """Process group for the barrier and the max-over-ranks timing (no data-path collective).
+    A rank that never joins makes the others fail after timeout_s instead of waiting forever."""
     if world <= 1:
         return None
+    import datetime
+
     import torch.distributed as dist
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group("nccl" if use_cuda else "gloo")
+    kw = {"timeout": datetime.timedelta(seconds=timeout_s)} if timeout_s else {}
+    dist.init_process_group("nccl" if use_cuda else "gloo", **kw)
     return dist
 
 
@@ -234,7 +258,7 @@ def run_ours(args):
             _build.build()
         barrier(dist, device)
 
-    w = W.config(args.config)
+    w = workload(args)
     gather = "fused"
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
                            gather=gather)
@@ -293,7 +317,7 @@ def run_ours(args):
     variant = {"rs_adamw": "rs_adamw_scaled" if clip and ghat_mode != "materialize" else "rs_adamw_plain",
                "adamw": "adamw", "rs_norm": "rs_norm_write" if ghat_mode == "materialize" else "rs_norm_only",
                "gather": "gather", "norm_final": "norm_final"}[dom]
-    workload_key = f"config{args.config}"
+    workload_key = f"config{args.config}" + (f"-max{args.max_params}" if args.max_params else "")
     traffic = ncu_traffic(variant, workload_key)
     roofline = {"bound": "hbm", "kernel": variant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -352,8 +376,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    import workloads as W
-    w = W.config(args.config)
+    w = workload(args)
     per_step = []
     cb = None
     for _ in range(args.warmup + args.steps):
