@@ -192,7 +192,7 @@ def ncu_traffic(kernel_key: str, workload_key: str):
     try:
         with open(TRAFFIC_FILE) as f:
             tab = json.load(f)
-        e = tab[kernel_key]
+        e = tab[f"{workload_key}:{kernel_key}"]
         if e.get("kernel_src_sha") != kernel_sha() or e.get("workload") != workload_key:
             return None
         return float(e["dram_bytes_per_launch"])
@@ -228,7 +228,7 @@ def cpu_baseline(w, target_seconds=15.0):
         O.zero_step(p, st, grads, oh)
         done += 1
         el = time.perf_counter() - t0
-        if el >= target_seconds or done >= 64:
+        if el >= target_seconds or done >= 10000:
             break
     rate = done * p.N / el
     return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",

@@ -280,3 +280,58 @@ def test_kernel_timing_counts_launches():
     t = opt.kernel_times()
     assert t["rs_norm"][1] == 3 and t["norm_final"][1] == 3 and t["adamw"][1] == 3 and t["rs_adamw"][1] == 0
     assert all(v[0] > 0 for k, v in t.items() if v[1])
+
+
+# ------------------------------------------------------------------------------------------
+# Guard bands: no kernel writes outside the buffers it was given
+# ------------------------------------------------------------------------------------------
+GUARD = 4096
+
+
+def _guarded(nbytes, dev):
+    raw = torch.full((GUARD + nbytes + GUARD,), 0xA5, dtype=torch.uint8, device=dev)
+    return raw, raw[GUARD:GUARD + nbytes]
+
+
+@pytest.mark.parametrize("gather,mode", [("shards", "materialize"), ("fused", "recompute"), ("fused", "materialize")])
+def test_guard_bands_untouched(gather, mode):
+    import ctypes
+    w = W.small_variant(W.config(3), ragged(30, 100, 5000, 9), M=8, bucket_bytes=20000, steps=2)
+    dev = torch.device("cuda")
+    s = zg.plan(w.numel, w.M, w.stage, w.bucket_bytes, gather)
+    toff, _ = zg.layout(w.numel, w.M, w.stage, w.bucket_bytes, gather)
+    raws, views = {}, {}
+    for name, nbytes in (("master", s["bytes_master"]), ("m", s["bytes_m"]), ("v", s["bytes_v"]),
+                         ("ghat", s["bytes_ghat"]), ("param_full", s["bytes_param_full"]),
+                         ("param_shards", s["bytes_param_shards"]), ("scratch", s["bytes_scratch"])):
+        if nbytes:
+            raws[name], views[name] = _guarded(nbytes, dev)
+    grads = []
+    for r in range(w.M):
+        raws[f"g{r}"], gv = _guarded(s["bytes_grad_each"], dev)
+        gv.zero_()
+        g = gv.view(torch.bfloat16)
+        W.fill_grads(w, r, 0, g, toff)
+        grads.append(g)
+    mi_raw, mi = _guarded(4 * s["n"], dev)
+    mi.view(torch.float32).copy_(W.master_init(w, dev))
+    bufs = zg.Buffers(*[views[k].data_ptr() if k in views else None
+                        for k in ("master", "m", "v", "ghat", "param_full", "param_shards", "scratch")])
+    cfg = zg.Config(w.M, w.stage, w.bucket_bytes, zg.GATHER[gather], 0)
+    arr = (ctypes.c_int64 * len(w.numel))(*w.numel)
+    ctx = ctypes.c_void_p()
+    lib = zg._lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.zero_init(ctypes.byref(ctx), ctypes.byref(cfg), ctypes.cast(arr, ctypes.c_void_p), len(w.numel),
+                         ctypes.byref(bufs), mi.data_ptr(), stream) == 0
+    h, _ = make_hyper(w, mode)
+    ptrs = (ctypes.c_void_p * w.M)(*[g.data_ptr() for g in grads])
+    for _ in range(w.steps):
+        assert lib.zero_step(ctx, ctypes.cast(ptrs, ctypes.c_void_p), w.stage, ctypes.byref(h), stream) == 0
+    if gather == "shards":
+        assert lib.zero_gather(ctx, 1, None, stream) == 0
+    assert lib.zero_sync_status(ctx) == 0
+    torch.cuda.synchronize()
+    for name, raw in list(raws.items()) + [("master_init", mi_raw)]:
+        assert bool((raw[:GUARD] == 0xA5).all()) and bool((raw[-GUARD:] == 0xA5).all()), f"guard band of {name} hit"
+    assert lib.zero_destroy(ctx) == 0

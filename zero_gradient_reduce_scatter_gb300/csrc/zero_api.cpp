@@ -209,7 +209,8 @@ int grid_for(zero_ctx* c, int variant, int64_t work_items) {
         if (g > zg::kMaxPartials) g = zg::kMaxPartials;
         c->grid[variant] = g;
     }
-    int64_t need = (work_items + zg::kThreads - 1) / zg::kThreads;
+    const int threads = zg::variant_threads(variant);
+    int64_t need = (work_items + threads - 1) / threads;
     if (need < 1) need = 1;
     return (int)(need < c->grid[variant] ? need : c->grid[variant]);
 }
@@ -595,7 +596,7 @@ int zero_kernel_times(zero_ctx* c, double* ms, int64_t* launches) {
 int zero_launch_shape(zero_ctx* c, int* ctas, int* threads) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (ctas) *ctas = grid_for(c, zg::kVarRsAdamwPlain, c->npad / 8);
-    if (threads) *threads = zg::kThreads;
+    if (threads) *threads = zg::variant_threads(zg::kVarRsAdamwPlain);
     return ZERO_OK;
 }
 

@@ -58,8 +58,32 @@ struct StepArgs {
     double* partials;     // one fp64 partial sum of squares per CTA of the norm pass
 };
 
+// Launch shapes and load paths of the streaming kernels, chosen by measurement on GB300
+// (threads per CTA; CTAs per SM, 0 = as many as fit; how gradients are loaded). Measured
+// on the full 4B (M = 4) and 1.3B (M = 8) workloads: the fused reduce-scatter + AdamW
+// kernel and the AdamW-from-average kernel run best with 16 warps per SM (one 512-thread
+// CTA; 24 warps per SM lost ~8%), the read-only norm pass with 32 warps per SM, and the
+// norm pass that also writes the average with as many 256-thread CTAs as fit.
+enum LoadPath : int {
+    kLoadEvictFirst = 0,  // ld.global.cs: streaming, evict-first in L1 and L2
+    kLoadNonCoherent = 1, // ld.global.nc.L1::no_allocate: read-only path, no L1 allocation
+    kLoadReadOnly = 2,    // ld.global.nc: read-only (texture) path
+};
+constexpr int kThreadsRsNormOnly = 1024;   // norm pass, averaged gradient kept in registers
+constexpr int kThreadsRsNormWrite = 256;  // norm pass that also writes the averaged gradient
+constexpr int kThreadsRsAdamw = 512;
+constexpr int kThreadsAdamw = 512;
+constexpr int kThreadsGather = 256;
+constexpr int kThreadsInit = 256;
+constexpr int kCtasPerSmRsNormOnly = 0;
+constexpr int kCtasPerSmRsNormWrite = 0;
+constexpr int kCtasPerSmRsAdamw = 0;
+constexpr int kCtasPerSmAdamw = 1;
+constexpr int kGradLoadRsNorm = kLoadReadOnly;
+constexpr int kGradLoadRsAdamw = kLoadReadOnly;
+constexpr int kThreads = 256;         // CTA size of the single-CTA norm finalise
+
 // Scratch layout (bytes from the scratch base; every part 256-byte aligned).
-constexpr int kThreads = 256;         // threads per CTA of the streaming kernels
 constexpr int kMaxPartials = 4096;    // largest grid of the norm pass
 constexpr int64_t kScratchStatus = 0;
 constexpr int64_t kScratchPartials = 256;
@@ -84,10 +108,14 @@ enum KernelVariant : int {
 // Records a CUDA error for zero_last_cuda_error() and returns ZERO_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 
+// Threads per CTA of a kernel variant, and its CTAs-per-SM cap (0 = occupancy limit).
+int variant_threads(int variant);
+int variant_ctas_per_sm_cap(int variant);
+
 // Largest number of CTAs of `variant` (for rank count M) resident on one SM.
 cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks);
 
-// Launchers. `grid` CTAs of kThreads threads on `stream`.
+// Launchers: `grid` CTAs of variant_threads(variant) threads on `stream`.
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
 cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm,
                               int clip, cudaStream_t s);

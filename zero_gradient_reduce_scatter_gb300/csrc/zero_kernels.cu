@@ -40,6 +40,20 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
 
 // Streaming (evict-first) vector accesses.
 __device__ __forceinline__ uint4 ld_u4(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+// Read-only path without L1 allocation, for gradients no kernel writes.
+__device__ __forceinline__ uint4 ld_u4_nc(const uint16_t* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+template <int PATH>
+__device__ __forceinline__ uint4 ld_grad(const uint16_t* p) {
+    if constexpr (PATH == kLoadNonCoherent) return ld_u4_nc(p);
+    else if constexpr (PATH == kLoadReadOnly) return __ldg(reinterpret_cast<const uint4*>(p));
+    else return ld_u4(p);
+}
 __device__ __forceinline__ float4 ld_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
 __device__ __forceinline__ void st_u4(uint16_t* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
@@ -93,27 +107,27 @@ __device__ __forceinline__ void add8(float acc[8], uint4 q) {
     acc[7] = __fadd_rn(acc[7], bf_hi(q.w));
 }
 
-template <int MT>
+template <int MT, int PATH>
 __device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t o, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
     if constexpr (MT > 0) {
         uint4 q[MT];
 #pragma unroll
-        for (int r = 0; r < MT; ++r) q[r] = ld_u4(a.grads[r] + o);
+        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(a.grads[r] + o);
 #pragma unroll
         for (int r = 0; r < MT; ++r) add8(acc, q[r]);
     } else {
         int r = 0;
         for (; r + 4 <= a.M; r += 4) {
-            uint4 q0 = ld_u4(a.grads[r] + o), q1 = ld_u4(a.grads[r + 1] + o);
-            uint4 q2 = ld_u4(a.grads[r + 2] + o), q3 = ld_u4(a.grads[r + 3] + o);
+            uint4 q0 = ld_grad<PATH>(a.grads[r] + o), q1 = ld_grad<PATH>(a.grads[r + 1] + o);
+            uint4 q2 = ld_grad<PATH>(a.grads[r + 2] + o), q3 = ld_grad<PATH>(a.grads[r + 3] + o);
             add8(acc, q0);
             add8(acc, q1);
             add8(acc, q2);
             add8(acc, q3);
         }
-        for (; r < a.M; ++r) add8(acc, ld_u4(a.grads[r] + o));
+        for (; r < a.M; ++r) add8(acc, ld_grad<PATH>(a.grads[r] + o));
     }
 }
 
@@ -242,8 +256,9 @@ struct SumSq {
 };
 
 // Sum over the CTA in a fixed order; the result is valid in thread 0.
+template <int THREADS>
 __device__ __forceinline__ double block_sum(double x) {
-    __shared__ double warp_sums[kThreads / 32];
+    __shared__ double warp_sums[THREADS / 32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xFFFFFFFFu, x, off);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -252,7 +267,7 @@ __device__ __forceinline__ double block_sum(double x) {
     double t = 0.0;
     if (threadIdx.x == 0) {
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) t += warp_sums[w];
+        for (int w = 0; w < THREADS / 32; ++w) t += warp_sums[w];
     }
     return t;
 }
@@ -260,11 +275,11 @@ __device__ __forceinline__ double block_sum(double x) {
 // ---------------------------------------------------------------------------------------
 // K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool WRITE>
-__global__ void __launch_bounds__(kThreads) k_rs_norm(const StepArgs a) {
+template <int MT, bool WRITE, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly>
+__global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     SumSq acc;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * THREADS;
+    int64_t vi = (int64_t)blockIdx.x * THREADS + threadIdx.x;
     if (vi < a.nvec) {
         Cursor c;
         c.init(a.buckets, a.nb, vi * 8);
@@ -272,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) k_rs_norm(const StepArgs a) {
             const int64_t o = vi * 8;
             c.seek(o);
             float sum[8], gh[8];
-            rank_sum<MT>(a, o, sum);
+            rank_sum<MT, kGradLoadRsNorm>(a, o, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
             if (WRITE) {
                 st_f4(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
@@ -281,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) k_rs_norm(const StepArgs a) {
             acc.add8(gh);
         }
     }
-    const double t = block_sum(acc.value());
+    const double t = block_sum<THREADS>(acc.value());
     if (threadIdx.x == 0) a.partials[blockIdx.x] = t;
 }
 
@@ -314,11 +329,11 @@ __global__ void __launch_bounds__(kThreads) k_norm_final(Status* st, const doubl
 // ---------------------------------------------------------------------------------------
 // K3: AdamW from the materialized fp32 average (clipped, two-pass form).
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_adamw(const StepArgs a) {
+__global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
     if (a.status->flags & kFlagNonfinite) return;
     const float s = a.status->scale;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreadsAdamw;
+    int64_t vi = (int64_t)blockIdx.x * kThreadsAdamw + threadIdx.x;
     if (vi >= a.nvec) return;
     Cursor c;
     c.init(a.buckets, a.nb, vi * 8);
@@ -340,14 +355,14 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const StepArgs a) {
 // leaves registers. SCALE applies the clip scale computed by K2 (recompute form).
 // ---------------------------------------------------------------------------------------
 template <int MT, bool SCALE>
-__global__ void __launch_bounds__(kThreads) k_rs_adamw(const StepArgs a) {
+__global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
     float s = 1.0f;
     if (SCALE) {
         if (a.status->flags & kFlagNonfinite) return;
         s = a.status->scale;
     }
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreadsRsAdamw;
+    int64_t vi = (int64_t)blockIdx.x * kThreadsRsAdamw + threadIdx.x;
     if (vi >= a.nvec) return;
     Cursor c;
     c.init(a.buckets, a.nb, vi * 8);
@@ -355,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) k_rs_adamw(const StepArgs a) {
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
-        rank_sum<MT>(a, o, sum);
+        rank_sum<MT, kGradLoadRsAdamw>(a, o, sum);
         load_state(a, o, p, m, v);
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
@@ -399,12 +414,12 @@ __device__ __forceinline__ uint4 splice(uint4 A, uint4 B, int k) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads) k_gather(const uint16_t* __restrict__ shards,
+__global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
                                                      uint16_t* __restrict__ full, const Bucket* tab, int64_t nb,
                                                      int64_t npad, int64_t u_begin, int64_t u_end) {
     const int64_t w_first = u_begin >> 3, w_last = (u_end + 7) >> 3;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t wi = w_first + (int64_t)blockIdx.x * kThreads + threadIdx.x; wi < w_last; wi += stride) {
+    const int64_t stride = (int64_t)gridDim.x * kThreadsGather;
+    for (int64_t wi = w_first + (int64_t)blockIdx.x * kThreadsGather + threadIdx.x; wi < w_last; wi += stride) {
         const int64_t u = wi * 8;
         const int64_t b = bucket_of_unpadded(tab, nb, u);
         const Bucket e = tab[b];
@@ -434,11 +449,11 @@ __global__ void __launch_bounds__(kThreads) k_gather(const uint16_t* __restrict_
 // Initial state: master = unpadded init scattered into the padded layout (padding 0),
 // m = v = 0, bf16 copies of the parameters. One lane per thread (not a hot kernel).
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_init(const float* __restrict__ init, float* master, float* m,
+__global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__ init, float* master, float* m,
                                                    float* v, uint16_t* full, uint16_t* shards, const Bucket* tab,
                                                    int64_t nb, int64_t npad) {
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    int64_t o = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreadsInit;
+    int64_t o = (int64_t)blockIdx.x * kThreadsInit + threadIdx.x;
     if (o >= npad) return;
     Cursor c;
     c.init(tab, nb, o);
@@ -494,15 +509,42 @@ const void* variant_fn(int variant, int M) {
 
 }  // namespace
 
+int variant_threads(int variant) {
+    switch (variant) {
+        case kVarRsNormWrite: return kThreadsRsNormWrite;
+        case kVarRsNormOnly: return kThreadsRsNormOnly;
+        case kVarAdamw: return kThreadsAdamw;
+        case kVarRsAdamwScaled:
+        case kVarRsAdamwPlain: return kThreadsRsAdamw;
+        case kVarGather: return kThreadsGather;
+        case kVarInit: return kThreadsInit;
+        default: return kThreads;
+    }
+}
+
+int variant_ctas_per_sm_cap(int variant) {
+    switch (variant) {
+        case kVarRsNormWrite: return kCtasPerSmRsNormWrite;
+        case kVarRsNormOnly: return kCtasPerSmRsNormOnly;
+        case kVarAdamw: return kCtasPerSmAdamw;
+        case kVarRsAdamwScaled:
+        case kVarRsAdamwPlain: return kCtasPerSmRsAdamw;
+        default: return 0;
+    }
+}
+
 cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks) {
     const void* fn = variant_fn(variant, M);
     if (!fn) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, variant_threads(variant), 0);
+    const int cap = variant_ctas_per_sm_cap(variant);
+    if (e == cudaSuccess && cap > 0 && *blocks > cap) *blocks = cap;
+    return e;
 }
 
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
-    if (write_ghat) ByM<RsNormWrite>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
-    else ByM<RsNormOnly>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    if (write_ghat) ByM<RsNormWrite>::get(a.M)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
+    else ByM<RsNormOnly>::get(a.M)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -513,20 +555,20 @@ cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, do
 }
 
 cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s) {
-    k_adamw<<<grid, kThreads, 0, s>>>(a);
+    k_adamw<<<grid, kThreadsAdamw, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
-    if (apply_scale) ByM<RsAdamwScaled>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
-    else ByM<RsAdamwPlain>::get(a.M)<<<grid, kThreads, 0, s>>>(a);
+    if (apply_scale) ByM<RsAdamwScaled>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    else ByM<RsAdamwPlain>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* full, const Bucket* buckets, int64_t nb, int64_t npad,
                           int64_t u_begin, int64_t u_end, int grid, cudaStream_t s) {
     if (u_end <= u_begin) return cudaSuccess;
-    k_gather<<<grid, kThreads, 0, s>>>(shards, full, buckets, nb, npad, u_begin, u_end);
+    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, full, buckets, nb, npad, u_begin, u_end);
     return cudaGetLastError();
 }
 
@@ -534,7 +576,7 @@ cudaError_t launch_init(const float* master_init, float* master, float* m, float
                         uint16_t* shards, const Bucket* buckets, int64_t nb, int64_t npad, int grid,
                         cudaStream_t s) {
     if (npad <= 0) return cudaSuccess;
-    k_init<<<grid, kThreads, 0, s>>>(master_init, master, m, v, full, shards, buckets, nb, npad);
+    k_init<<<grid, kThreadsInit, 0, s>>>(master_init, master, m, v, full, shards, buckets, nb, npad);
     return cudaGetLastError();
 }
 

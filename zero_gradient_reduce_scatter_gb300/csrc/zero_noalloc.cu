@@ -153,7 +153,7 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     a.inv_M = (float)(1.0 / (double)M);
     a.status = status;
     a.partials = partials;
-    int64_t need = (a.nvec + zg::kThreads - 1) / zg::kThreads;
+    int64_t need = (a.nvec + zg::kThreadsRsNormOnly - 1) / zg::kThreadsRsNormOnly;
     if (need < 1) need = 1;
     const int grid = (int)(need < grid_cap ? need : grid_cap);
     // Every partial the finalise kernel reads is written by this call's norm pass, and the
