@@ -179,6 +179,22 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
 int zero_step(zero_ctx* ctx, const void* const* grads, int stage, const zero_hyper* hyper,
               void* stream);
 
+/* ZeRO-2 per-bucket streaming ("CS336 2026 Lecture 8" Slide 23; "并行训练优化、MoE扩展与系统瓶颈"
+ * 2.2.4: each layer's gradient is reduce-scattered as soon as it is produced and the full
+ * gradient is then freed). zero_reduce_bucket reduce-scatters bucket `bucket` into the
+ * persistent fp32 averaged-gradient shard (the ghat buffer, required) and keeps the
+ * bucket's sum of squares; grads_b[r] points at rank r's slice of that bucket (M * S_b bf16
+ * lanes in the padded layout, 16-byte aligned), which the caller may free or reuse once the
+ * stream has passed the call. When every bucket has been reduced, zero_apply performs the
+ * rest of the step: the global norm from the per-bucket sums (and the clip scale if
+ * hyper->clip), AdamW on all owner shards from the averaged gradient, the all-gather; it
+ * increments t. All calls of one step must be ordered on one stream (they share the norm
+ * partials). Bytes per lane: 2M + 4 in the reductions, 30 in the update.
+ * Errors: BAD_CONTEXT, INVALID_ARG (bad bucket, or zero_apply before every bucket was
+ * reduced), MISALIGNED, SIZE_MISMATCH (no ghat buffer), STAGE, CUDA. */
+int zero_reduce_bucket(zero_ctx* ctx, int64_t bucket, const void* const* grads_b, void* stream);
+int zero_apply(zero_ctx* ctx, int stage, const zero_hyper* hyper, void* stream);
+
 /* zero_step with host-resident data: enqueues the copy of each pinned host gradient
  * host_grads[r] (bf16 [npad]) into the device buffer dev_grads[r], the step, and the copy
  * of the full bf16 parameters into the pinned host buffer host_params (bf16 [n]), all on
@@ -194,6 +210,18 @@ int zero_params(zero_ctx* ctx, void** full_bf16);
  * Errors: BAD_CONTEXT, INVALID_ARG (bucket out of range or no shards), CUDA. */
 int zero_gather(zero_ctx* ctx, int64_t bucket, void* dst, void* stream);
 
+/* ZeRO-3 per-module gather ("CS336 2026 Lecture 8" Slides 24-26: parameters are gathered
+ * just before a module's forward / backward and freed after; "CS231n Lecture 11" 4.3: the
+ * next block's weights are prefetched while the current one computes). With
+ * ZERO_GATHER_SHARDS, writes bucket `bucket`'s n_b bf16 parameters, in tensor order, to the
+ * transient device buffer dst[0 .. n_b) (2-byte aligned), on `stream`; running it on a side
+ * stream one bucket ahead is the prefetch. Errors: BAD_CONTEXT, INVALID_ARG, MISALIGNED,
+ * CUDA. */
+int zero_gather_bucket(zero_ctx* ctx, int64_t bucket, void* dst, void* stream);
+
+/* Bucket `bucket`'s first unpadded parameter index and its parameter count (host only). */
+int zero_bucket_info(zero_ctx* ctx, int64_t bucket, int64_t* uoff, int64_t* n);
+
 /* Copies rank `rank`'s shard of state array `which` (ZERO_STATE_*), shard_len fp32 values in
  * bucket order, into the device buffer dst. GHAT needs a ghat buffer and holds the
  * averaged gradient of the last step that materialized it. */
@@ -206,6 +234,20 @@ int zero_last_norm(zero_ctx* ctx, double* norm, float* scale);
 /* Waits for the last step's stream and returns ZERO_OK, ZERO_ERR_NONFINITE (update
  * skipped), or ZERO_ERR_CUDA. */
 int zero_sync_status(zero_ctx* ctx);
+
+/* Checkpoint form of the optimizer state: the real lanes of fp32 master, m and v as unpadded
+ * vectors of n values in tensor order. This form does not depend on the rank count, bucket
+ * size or stage, so a state saved by one context loads into another with a different M
+ * (resharding, elastic restart; "CS336 2026 Lecture 8" Slide 67 lists checkpointing and
+ * elastic restart among the needs at scale).
+ * zero_save_state: device fp32 [n] outputs; any of the three may be NULL (not written).
+ * zero_load_state: device fp32 [n] inputs, read during this call's kernel; m and v may be
+ * NULL (zeros); also rebuilds the bf16 parameters (and shards) from the master and sets the
+ * step counter to t. Both are asynchronous on `stream`. Errors: BAD_CONTEXT, INVALID_ARG,
+ * CUDA. */
+int zero_save_state(zero_ctx* ctx, void* master, void* m, void* v, void* stream);
+int zero_load_state(zero_ctx* ctx, const void* master, const void* m, const void* v, int64_t t,
+                    void* stream);
 
 /* Step counter (number of steps taken). zero_set_step restores it from a checkpoint. */
 int zero_get_step(zero_ctx* ctx, int64_t* t);

@@ -93,7 +93,7 @@ def _load():
             lib.orc_adamw.restype = None
             lib.orc_adamw.argtypes = [_I64, _P, ctypes.c_float, _P, _P, _P, ctypes.POINTER(Hyper), _I64]
             lib.orc_init.restype = None
-            lib.orc_init.argtypes = [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P]
+            lib.orc_init.argtypes = [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
             lib.orc_zero_step.restype = ctypes.c_int
             lib.orc_zero_step.argtypes = [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           ctypes.POINTER(Hyper), _I64,
@@ -268,10 +268,14 @@ class RankState:
     t: int = 0   # steps taken
 
 
-def init_state(p: Plan, stage: int, master_init: np.ndarray) -> RankState:
+def init_state(p: Plan, stage: int, master_init: np.ndarray, m_init=None, v_init=None, t: int = 0) -> RankState:
+    """Rank structures from unpadded state (m, v default to zeros; t = steps already taken)."""
     assert stage in (1, 2, 3)
     mi = np.ascontiguousarray(master_init, dtype=np.float32)
     assert mi.size == p.N
+    mm = None if m_init is None else np.ascontiguousarray(m_init, dtype=np.float32)
+    vv = None if v_init is None else np.ascontiguousarray(v_init, dtype=np.float32)
+    assert (mm is None or mm.size == p.N) and (vv is None or vv.size == p.N)
     L = max(p.shard_len, 1)
     master = [np.empty(L, dtype=np.float32) for _ in range(p.M)]
     mom = [np.empty(L, dtype=np.float32) for _ in range(p.M)]
@@ -279,9 +283,10 @@ def init_state(p: Plan, stage: int, master_init: np.ndarray) -> RankState:
     ghat = [np.zeros(L, dtype=np.float32) for _ in range(p.M)]
     plen = L if stage == 3 else max(p.N, 1)
     param = [np.empty(plen, dtype=np.uint16) for _ in range(p.M)]
-    _load().orc_init(p.M, stage, p.nb, _ptr(p.b_n), _ptr(p.b_S), _ptr(mi), _ptr_array(master),
-                     _ptr_array(mom), _ptr_array(var), _ptr_array(param))
-    return RankState(stage, master, mom, var, ghat, param)
+    _load().orc_init(p.M, stage, p.nb, _ptr(p.b_n), _ptr(p.b_S), _ptr(mi), _ptr(mm) if mm is not None else None,
+                     _ptr(vv) if vv is not None else None, _ptr_array(master), _ptr_array(mom), _ptr_array(var),
+                     _ptr_array(param))
+    return RankState(stage, master, mom, var, ghat, param, t)
 
 
 def zero_step(p: Plan, st: RankState, grads, h: Hyper):

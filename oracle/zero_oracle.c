@@ -277,14 +277,15 @@ void orc_adamw(int64_t n, const float* ghat, float s, float* p, float* m, float*
 }
 
 /* ------------------------------------------------------------------------------------ */
-/* Initial state. master_init is the unpadded fp32 parameter vector (N values).           */
-/* Every rank's optimizer state is its shard of the padded layout; m = v = 0.            */
+/* Initial state. master_init is the unpadded fp32 parameter vector (N values); m_init and */
+/* v_init are the unpadded Adam moments, or NULL for zeros (a fresh start). Every rank's   */
+/* optimizer state is its shard of the padded layout; padding lanes are 0.               */
 /* Stages 1 and 2 keep a full bf16 replica per rank (N values); stage 3 keeps a bf16      */
 /* shard per rank ([L8] Slides 19, 22, 24; [EQ] 2.2.1, 2.2.3, 2.2.5).                     */
 /* ------------------------------------------------------------------------------------ */
 void orc_init(int32_t M, int32_t stage, int64_t nb, const int64_t* b_n, const int64_t* b_S,
-              const float* master_init, float* const* master, float* const* mom,
-              float* const* var, uint16_t* const* param)
+              const float* master_init, const float* m_init, const float* v_init,
+              float* const* master, float* const* mom, float* const* var, uint16_t* const* param)
 {
     int64_t slen = orc_shard_len(nb, b_S);
     for (int32_t r = 0; r < M; ++r) {
@@ -292,14 +293,14 @@ void orc_init(int32_t M, int32_t stage, int64_t nb, const int64_t* b_n, const in
         for (int64_t b = 0; b < nb; ++b) {
             for (int64_t j = 0; j < b_S[b]; ++j) {
                 int64_t in_bucket = (int64_t)r * b_S[b] + j;
-                master[r][base + j] = (in_bucket < b_n[b]) ? master_init[ubase + in_bucket] : 0.0f;
+                int real = in_bucket < b_n[b];
+                int64_t u = ubase + in_bucket;
+                master[r][base + j] = real ? master_init[u] : 0.0f;
+                mom[r][base + j] = (real && m_init) ? m_init[u] : 0.0f;
+                var[r][base + j] = (real && v_init) ? v_init[u] : 0.0f;
             }
             base += b_S[b];
             ubase += b_n[b];
-        }
-        for (int64_t i = 0; i < slen; ++i) {
-            mom[r][i] = 0.0f;
-            var[r][i] = 0.0f;
         }
         if (stage == 3) {
             for (int64_t i = 0; i < slen; ++i) param[r][i] = orc_f32_to_bf16(master[r][i]);

@@ -135,6 +135,24 @@ def test_plan_single_tensor_bruteforce():
                 assert np.all(seen == 1)
 
 
+def test_init_with_moments_places_them_like_master():
+    """Initial m / v given unpadded land at the same owner lanes as the master (brute force),
+    padding stays 0, and omitting them is the same as passing zeros."""
+    for M in (1, 3, 4, 7):
+        numel = [5, 130, 1, 64]
+        p = O.plan(numel, M, 300, 8)
+        x = np.arange(1, p.N + 1, dtype=np.float32)
+        st = O.init_state(p, 2, x, -x, 2 * x)
+        u = p.unpadded_index()
+        for name, want in (("master", x), ("mom", -x), ("var", 2 * x)):
+            flat = O.flat_state(p, st, name)
+            assert np.array_equal(flat[u >= 0], want) and np.all(flat[u < 0] == 0)
+        z = O.init_state(p, 3, x, np.zeros(p.N, np.float32), np.zeros(p.N, np.float32))
+        z0 = O.init_state(p, 3, x)
+        for a, b in zip(z.mom + z.var + z.param, z0.mom + z0.var + z0.param):
+            assert np.array_equal(a, b)
+
+
 def test_plan_multi_tensor_bruteforce():
     rng = np.random.default_rng(5)
     for trial in range(400):

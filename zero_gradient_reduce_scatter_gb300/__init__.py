@@ -95,8 +95,14 @@ SIGNATURES = {
                                  _P, _P]),
     "zero_step": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_step_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P, _P]),
+    "zero_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
+    "zero_apply": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_params": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
+    "zero_save_state": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "zero_load_state": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P]),
     "zero_gather": (ctypes.c_int, [_P, _I64, _P, _P]),
+    "zero_gather_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
+    "zero_bucket_info": (ctypes.c_int, [_P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "zero_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P, _P]),
     "zero_last_norm": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]),
     "zero_sync_status": (ctypes.c_int, [_P]),
@@ -264,9 +270,90 @@ class ZeroOptimizer:
                                      ctypes.byref(hyper), host_params.data_ptr(), _stream_handle(stream)),
                "zero_step_host")
 
+    # -- ZeRO-2 per-bucket streaming ----------------------------------------------------------
+    def bucket_lanes(self, bucket: int) -> int:
+        off, n, S, _ = self.buckets[bucket]
+        return self.M * S
+
+    def new_bucket_grad_buffers(self, bucket: int):
+        """M zeroed bf16 buffers for one bucket (M * S_b lanes each)."""
+        return [torch.zeros(self.bucket_lanes(bucket), dtype=torch.bfloat16, device=self.device)
+                for _ in range(self.M)]
+
+    def bucket_tensor_view(self, bucket_buf: torch.Tensor, bucket: int, i: int) -> torch.Tensor:
+        """View of tensor i (which must live in `bucket`) inside a bucket gradient buffer."""
+        off = self.buckets[bucket][0]
+        o = self.tensor_offsets[i] - off
+        if not (0 <= o and o + self.numel[i] <= self.bucket_lanes(bucket)):
+            raise ValueError(f"tensor {i} is not in bucket {bucket}")
+        return bucket_buf[o:o + self.numel[i]]
+
+    def reduce_bucket(self, bucket: int, grads_b, stream=None):
+        if len(grads_b) != self.M:
+            raise ValueError(f"expected {self.M} bucket gradient buffers")
+        lanes = self.bucket_lanes(bucket)
+        for g in grads_b:
+            if not (g.is_cuda and g.dtype == torch.bfloat16 and g.is_contiguous() and g.numel() >= lanes):
+                raise ValueError("bucket gradients must be contiguous CUDA bf16 tensors of M * S_b lanes")
+        ptrs = (ctypes.c_void_p * self.M)(*[g.data_ptr() for g in grads_b])
+        _check(_lib().zero_reduce_bucket(self._ctx, bucket, ctypes.cast(ptrs, _P), _stream_handle(stream)),
+               "zero_reduce_bucket")
+
+    def apply(self, hyper: Hyper, stream=None):
+        _check(_lib().zero_apply(self._ctx, self.stage, ctypes.byref(hyper), _stream_handle(stream)), "zero_apply")
+
     def gather_params(self, bucket: int = -1, dst: torch.Tensor | None = None, stream=None):
         _check(_lib().zero_gather(self._ctx, bucket, dst.data_ptr() if dst is not None else None,
                                   _stream_handle(stream)), "zero_gather")
+
+    def gather_bucket(self, bucket: int, dst: torch.Tensor, stream=None):
+        """ZeRO-3: bucket `bucket`'s bf16 parameters into the transient buffer dst[:n_b]."""
+        if not (dst.is_cuda and dst.dtype == torch.bfloat16 and dst.numel() >= self.buckets[bucket][1]):
+            raise ValueError("dst must be a CUDA bf16 tensor with room for the bucket")
+        _check(_lib().zero_gather_bucket(self._ctx, bucket, dst.data_ptr(), _stream_handle(stream)),
+               "zero_gather_bucket")
+
+    def bucket_range(self, bucket: int):
+        """(first unpadded index, parameter count) of a bucket."""
+        u, n = _I64(), _I64()
+        _check(_lib().zero_bucket_info(self._ctx, bucket, ctypes.byref(u), ctypes.byref(n)), "zero_bucket_info")
+        return u.value, n.value
+
+    def prefetched_buckets(self, order, stream=None, side_stream=None):
+        """ZeRO-3 just-in-time parameters with one-bucket-ahead prefetch.
+
+        Yields (bucket, params) in `order`; `params` (bf16, the bucket's n_b values) is ready
+        for work queued on `stream` when yielded. The gather of the next bucket runs on
+        `side_stream` meanwhile, into the other of two transient buffers; a buffer is reused
+        only after the work the consumer queued on `stream` before asking for the next
+        bucket has finished with it.
+        """
+        order = list(order)
+        if not order:
+            return
+        stream = stream or torch.cuda.current_stream()
+        side = side_stream or torch.cuda.Stream(device=self.device)
+        cap = max(self.buckets[b][1] for b in order)
+        bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(2)]
+        ready = [torch.cuda.Event() for _ in range(2)]
+        free = [torch.cuda.Event() for _ in range(2)]
+        for i in range(2):
+            free[i].record(stream)
+
+        def issue(i):
+            slot = i % 2
+            side.wait_event(free[slot])
+            self.gather_bucket(order[i], bufs[slot], stream=side)
+            ready[slot].record(side)
+
+        issue(0)
+        for i, b in enumerate(order):
+            if i + 1 < len(order):
+                issue(i + 1)
+            slot = i % 2
+            stream.wait_event(ready[slot])
+            yield b, bufs[slot][:self.buckets[b][1]]
+            free[slot].record(stream)
 
     # -- results ------------------------------------------------------------------------------
     def params(self) -> torch.Tensor:
@@ -280,6 +367,46 @@ class ZeroOptimizer:
         _check(_lib().zero_get_state(self._ctx, STATE[which], rank, out.data_ptr(), _stream_handle(stream)),
                "zero_get_state")
         return out
+
+    # -- checkpoint / resume / reshard ---------------------------------------------------------
+    def save_state(self, stream=None) -> dict:
+        """Layout-independent state: unpadded fp32 master / m / v (device tensors) and t."""
+        n = self.sizes["n"]
+        out = {k: torch.empty(n, dtype=torch.float32, device=self.device) for k in ("master", "m", "v")}
+        _check(_lib().zero_save_state(self._ctx, out["master"].data_ptr(), out["m"].data_ptr(), out["v"].data_ptr(),
+                                      _stream_handle(stream)), "zero_save_state")
+        out["t"] = self.t
+        return out
+
+    def load_state(self, state: dict, stream=None):
+        """Loads a state saved by any context over the same tensors (any M, bucket size, stage)."""
+        n = self.sizes["n"]
+        ts = {}
+        for k in ("master", "m", "v"):
+            x = state.get(k)
+            if x is not None:
+                x = x.to(device=self.device, dtype=torch.float32).contiguous()
+                if x.numel() != n:
+                    raise ValueError(f"{k} has {x.numel()} values, expected {n}")
+            ts[k] = x
+        if ts["master"] is None:
+            raise ValueError("state needs the master weights")
+        _check(_lib().zero_load_state(self._ctx, ts["master"].data_ptr(),
+                                      ts["m"].data_ptr() if ts["m"] is not None else None,
+                                      ts["v"].data_ptr() if ts["v"] is not None else None, int(state.get("t", 0)),
+                                      _stream_handle(stream)), "zero_load_state")
+        (stream or torch.cuda.current_stream()).synchronize()  # the inputs may be temporaries
+
+    def state_dict(self) -> dict:
+        """Host copy for a checkpoint file (torch.save-able), with the tensor sizes."""
+        st = self.save_state()
+        torch.cuda.current_stream().synchronize()
+        return {"numel": list(self.numel), "t": st["t"], **{k: st[k].cpu() for k in ("master", "m", "v")}}
+
+    def load_state_dict(self, sd: dict):
+        if list(sd["numel"]) != list(self.numel):
+            raise ValueError("checkpoint was written for different tensors")
+        self.load_state(sd)
 
     def last_norm(self):
         """(norm, scale) of the last clipped step, or None if it did not clip."""

@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -37,6 +38,9 @@ struct zero_ctx {
     int last_clip;
     cudaStream_t last_stream;
     int stepped;
+    // per-bucket streaming (zero_reduce_bucket / zero_apply)
+    double* bucket_sums;          // device: one fp64 sum of squares per bucket
+    std::vector<char> reduced;    // host: buckets reduced since the last zero_apply
     // launch shapes, per kernel variant (0 = not computed yet)
     int grid[zg::kNumVariants];
     // timing
@@ -253,6 +257,9 @@ zg::StepArgs base_args(zero_ctx* c) {
     a.buckets = c->dev_buckets;
     a.nb = (int64_t)c->buckets.size();
     a.nvec = c->npad / 8;
+    a.vbeg = 0;
+    a.vend = a.nvec;
+    a.gbase = 0;
     a.M = c->cfg.M;
     a.inv_M = (float)(1.0 / (double)c->cfg.M);
     a.status = c->status;
@@ -260,11 +267,12 @@ zg::StepArgs base_args(zero_ctx* c) {
     return a;
 }
 
-int gather_range(zero_ctx* c, int64_t u_begin, int64_t u_end, uint16_t* dst, cudaStream_t s) {
-    const int grid = grid_for(c, zg::kVarGather, (u_end - u_begin + 7) / 8 + 1);
+// out[0 .. count) = parameters of unpadded indices [u0, u0 + count).
+int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStream_t s) {
+    const int grid = grid_for(c, zg::kVarGather, count / 8 + 2);
     Timed tm(c, ZERO_K_GATHER, s);
-    cudaError_t e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, dst, c->dev_buckets,
-                                      (int64_t)c->buckets.size(), c->npad, u_begin, u_end, grid, s);
+    cudaError_t e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, out, c->dev_buckets,
+                                      (int64_t)c->buckets.size(), c->npad, u0, count, grid, s);
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
@@ -344,6 +352,8 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->status = (zg::Status*)(scratch + zg::kScratchStatus);
     c->partials = (double*)(scratch + zg::kScratchPartials);
     c->dev_buckets = (zg::Bucket*)(scratch + zg::kScratchBuckets);
+    c->bucket_sums = (double*)(scratch + zg::scratch_bucket_sums((int64_t)L.buckets.size()));
+    c->reduced.assign(L.buckets.size(), 0);
     c->t = 0;
     c->last_clip = 0;
     c->last_stream = (cudaStream_t)stream;
@@ -364,7 +374,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     if (e == cudaSuccess) {
         const int grid = grid_for(c, zg::kVarInit, c->npad);
         Timed tm(c, ZERO_K_INIT, s);
-        e = zg::launch_init((const float*)master_init, (float*)c->bufs.master, (float*)c->bufs.m,
+        e = zg::launch_init((const float*)master_init, nullptr, nullptr, (float*)c->bufs.master, (float*)c->bufs.m,
                             (float*)c->bufs.v, (uint16_t*)c->bufs.param_full, (uint16_t*)c->bufs.param_shards,
                             c->dev_buckets, (int64_t)c->buckets.size(), c->npad, grid, s);
     }
@@ -435,10 +445,79 @@ int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper
         e = zg::launch_rs_adamw(a, false, g4, s);
     }
     if (e == cudaSuccess && c->cfg.gather == ZERO_GATHER_SHARDS) {
-        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);
+        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);  // the all-gather
         if (rc) return rc;
     }
     if (e != cudaSuccess) return cuda_fail(e);
+    c->last_clip = h->clip;
+    c->last_stream = s;
+    c->stepped = 1;
+    return ZERO_OK;
+}
+
+int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (bucket < 0 || bucket >= nb || !grads_b) return ZERO_ERR_INVALID_ARG;
+    if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    for (int r = 0; r < c->cfg.M; ++r) {
+        if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
+        if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
+    }
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const zg::Bucket& e = c->buckets[(size_t)bucket];
+    zg::StepArgs a = base_args(c);
+    for (int r = 0; r < c->cfg.M; ++r) a.grads[r] = (const uint16_t*)grads_b[r];
+    a.vbeg = e.off / 8;
+    a.vend = e.end / 8;
+    a.gbase = e.off;
+    const int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
+    cudaError_t err;
+    {
+        Timed tm(c, ZERO_K_RS_NORM, s);
+        err = zg::launch_rs_norm(a, true, g1, s);
+    }
+    if (err == cudaSuccess) {
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        err = zg::launch_sum_partials(c->partials, g1, c->bucket_sums + bucket, s);
+    }
+    if (err != cudaSuccess) return cuda_fail(err);
+    c->reduced[(size_t)bucket] = 1;
+    return ZERO_OK;
+}
+
+int zero_apply(zero_ctx* c, int stage, const zero_hyper* h, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    for (char r : c->reduced)
+        if (!r) return ZERO_ERR_INVALID_ARG;  // every bucket must be reduced first
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    c->t += 1;
+    zg::StepArgs a = base_args(c);
+    a.k = adam_consts(h, c->t);
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        e = zg::launch_norm_final(c->status, c->bucket_sums, (int)c->buckets.size(), h->max_grad_norm, h->clip, s);
+    }
+    if (e == cudaSuccess) {
+        const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
+        Timed tm(c, ZERO_K_ADAMW, s);
+        e = zg::launch_adamw(a, g3, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (c->cfg.gather == ZERO_GATHER_SHARDS) {
+        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);
+        if (rc) return rc;
+    }
+    std::fill(c->reduced.begin(), c->reduced.end(), 0);
     c->last_clip = h->clip;
     c->last_stream = s;
     c->stepped = 1;
@@ -468,6 +547,36 @@ int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
+int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!master && !m && !v) return ZERO_ERR_INVALID_ARG;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int grid = grid_for(c, zg::kVarInit, c->npad);
+    cudaError_t e = zg::launch_save((const float*)c->bufs.master, (const float*)c->bufs.m, (const float*)c->bufs.v,
+                                    (float*)master, (float*)m, (float*)v, c->dev_buckets,
+                                    (int64_t)c->buckets.size(), c->npad, grid, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
+int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* v, int64_t t, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!master || t < 0) return ZERO_ERR_INVALID_ARG;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int grid = grid_for(c, zg::kVarInit, c->npad);
+    Timed tm(c, ZERO_K_INIT, s);
+    cudaError_t e = zg::launch_init((const float*)master, (const float*)m, (const float*)v, (float*)c->bufs.master,
+                                    (float*)c->bufs.m, (float*)c->bufs.v, (uint16_t*)c->bufs.param_full,
+                                    (uint16_t*)c->bufs.param_shards, c->dev_buckets, (int64_t)c->buckets.size(),
+                                    c->npad, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->t = t;
+    return ZERO_OK;
+}
+
 int zero_params(zero_ctx* c, void** full_bf16) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!full_bf16) return ZERO_ERR_INVALID_ARG;
@@ -484,12 +593,31 @@ int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     uint16_t* out = (uint16_t*)(dst ? dst : c->bufs.param_full);
-    int64_t u0 = 0, u1 = c->n;
+    int64_t u0 = 0, count = c->n;
     if (bucket >= 0) {
         u0 = c->buckets[(size_t)bucket].uoff;
-        u1 = u0 + c->buckets[(size_t)bucket].n;
+        count = c->buckets[(size_t)bucket].n;
     }
-    return gather_range(c, u0, u1, out, (cudaStream_t)stream);
+    return gather_range(c, u0, count, out + u0, (cudaStream_t)stream);
+}
+
+int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.gather != ZERO_GATHER_SHARDS || !dst) return ZERO_ERR_INVALID_ARG;
+    if (bucket < 0 || bucket >= (int64_t)c->buckets.size()) return ZERO_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dst) & 1u) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    const zg::Bucket& e = c->buckets[(size_t)bucket];
+    return gather_range(c, e.uoff, e.n, (uint16_t*)dst, (cudaStream_t)stream);
+}
+
+int zero_bucket_info(zero_ctx* c, int64_t bucket, int64_t* uoff, int64_t* n) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (bucket < 0 || bucket >= (int64_t)c->buckets.size() || !uoff || !n) return ZERO_ERR_INVALID_ARG;
+    *uoff = c->buckets[(size_t)bucket].uoff;
+    *n = c->buckets[(size_t)bucket].n;
+    return ZERO_OK;
 }
 
 int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {

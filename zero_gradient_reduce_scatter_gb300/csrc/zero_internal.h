@@ -49,6 +49,8 @@ struct StepArgs {
     const Bucket* buckets;
     int64_t nb;
     int64_t nvec;         // npad / 8: work items of 8 lanes (16 B of bf16)
+    int64_t vbeg, vend;   // vec range of the norm pass (the whole layout, or one bucket)
+    int64_t gbase;        // lane at which grads[r] starts (0, or the bucket's first lane)
     int32_t M;
     float inv_M;          // (float)(1.0 / M)
     int32_t out_shards;   // 1: `out` is the padded shard buffer; 0: the unpadded full buffer
@@ -88,9 +90,10 @@ constexpr int kMaxPartials = 4096;    // largest grid of the norm pass
 constexpr int64_t kScratchStatus = 0;
 constexpr int64_t kScratchPartials = 256;
 constexpr int64_t kScratchBuckets = kScratchPartials + 8 * kMaxPartials;
+// One fp64 sum of squares per bucket (per-bucket streaming) follows the bucket table.
+inline int64_t scratch_bucket_sums(int64_t n_buckets) { return (kScratchBuckets + 32 * n_buckets + 255) / 256 * 256; }
 inline int64_t scratch_bytes(int64_t n_buckets) {
-    int64_t b = kScratchBuckets + 32 * n_buckets;
-    return (b + 255) / 256 * 256;
+    return (scratch_bucket_sums(n_buckets) + 8 * n_buckets + 255) / 256 * 256;
 }
 
 // Kernel variants, used as keys of the per-context launch-shape cache.
@@ -119,15 +122,21 @@ cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks);
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
 cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm,
                               int clip, cudaStream_t s);
+// One CTA: *out = sum of partials[0 .. nparts) in a fixed order.
+cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s);
 cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
-// Copies bf16 shards (padded) into the unpadded full buffer for unpadded indices
-// [u_begin, u_end).
-cudaError_t launch_gather(const uint16_t* shards, uint16_t* full, const Bucket* buckets, int64_t nb,
-                          int64_t npad, int64_t u_begin, int64_t u_end, int grid, cudaStream_t s);
-// Initial state from the unpadded fp32 master vector.
-cudaError_t launch_init(const float* master_init, float* master, float* m, float* v,
-                        uint16_t* full, uint16_t* shards, const Bucket* buckets, int64_t nb,
-                        int64_t npad, int grid, cudaStream_t s);
+// out[d] = bf16 parameter of unpadded index u0 + d, d < count, from the padded shards
+// (out needs only 2-byte alignment).
+cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb,
+                          int64_t npad, int64_t u0, int64_t count, int grid, cudaStream_t s);
+// State from unpadded fp32 vectors (m_init / v_init may be null: zeros), plus bf16 copies.
+cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init,
+                        float* master, float* m, float* v, uint16_t* full, uint16_t* shards,
+                        const Bucket* buckets, int64_t nb, int64_t npad, int grid, cudaStream_t s);
+// Real lanes of master / m / v into unpadded vectors (any output may be null).
+cudaError_t launch_save(const float* master, const float* m, const float* v, float* out_master,
+                        float* out_m, float* out_v, const Bucket* buckets, int64_t nb, int64_t npad,
+                        int grid, cudaStream_t s);
 
 }  // namespace zg

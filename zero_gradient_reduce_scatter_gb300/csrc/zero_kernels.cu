@@ -114,20 +114,21 @@ __device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t o, float acc
     if constexpr (MT > 0) {
         uint4 q[MT];
 #pragma unroll
-        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(a.grads[r] + o);
+        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(a.grads[r] + (o - a.gbase));
 #pragma unroll
         for (int r = 0; r < MT; ++r) add8(acc, q[r]);
     } else {
         int r = 0;
+        const int64_t g = o - a.gbase;
         for (; r + 4 <= a.M; r += 4) {
-            uint4 q0 = ld_grad<PATH>(a.grads[r] + o), q1 = ld_grad<PATH>(a.grads[r + 1] + o);
-            uint4 q2 = ld_grad<PATH>(a.grads[r + 2] + o), q3 = ld_grad<PATH>(a.grads[r + 3] + o);
+            uint4 q0 = ld_grad<PATH>(a.grads[r] + g), q1 = ld_grad<PATH>(a.grads[r + 1] + g);
+            uint4 q2 = ld_grad<PATH>(a.grads[r + 2] + g), q3 = ld_grad<PATH>(a.grads[r + 3] + g);
             add8(acc, q0);
             add8(acc, q1);
             add8(acc, q2);
             add8(acc, q3);
         }
-        for (; r < a.M; ++r) add8(acc, ld_grad<PATH>(a.grads[r] + o));
+        for (; r < a.M; ++r) add8(acc, ld_grad<PATH>(a.grads[r] + g));
     }
 }
 
@@ -279,11 +280,11 @@ template <int MT, bool WRITE, int THREADS = WRITE ? kThreadsRsNormWrite : kThrea
 __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     SumSq acc;
     const int64_t stride = (int64_t)gridDim.x * THREADS;
-    int64_t vi = (int64_t)blockIdx.x * THREADS + threadIdx.x;
-    if (vi < a.nvec) {
+    int64_t vi = a.vbeg + (int64_t)blockIdx.x * THREADS + threadIdx.x;
+    if (vi < a.vend) {
         Cursor c;
         c.init(a.buckets, a.nb, vi * 8);
-        for (; vi < a.nvec; vi += stride) {
+        for (; vi < a.vend; vi += stride) {
             const int64_t o = vi * 8;
             c.seek(o);
             float sum[8], gh[8];
@@ -304,26 +305,37 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
 // K2: one CTA. Global norm = sqrt(sum of partials); clip scale c / norm when norm > c.
 // A non-finite norm raises the flag that makes the update kernels skip the step.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_norm_final(Status* st, const double* partials, int nparts,
-                                                         double max_norm, int clip) {
+// Fixed-order fp64 sum of n partials by one CTA; the result is valid in thread 0.
+__device__ __forceinline__ double cta_sum_partials(const double* partials, int n) {
     __shared__ double sm[kThreads];
     double x = 0.0;
-    for (int i = threadIdx.x; i < nparts; i += kThreads) x += partials[i];
+    for (int i = threadIdx.x; i < n; i += kThreads) x += partials[i];
     sm[threadIdx.x] = x;
     __syncthreads();
     for (int h = kThreads / 2; h > 0; h >>= 1) {
         if (threadIdx.x < h) sm[threadIdx.x] += sm[threadIdx.x + h];
         __syncthreads();
     }
+    return sm[0];
+}
+
+__global__ void __launch_bounds__(kThreads) k_norm_final(Status* st, const double* partials, int nparts,
+                                                         double max_norm, int clip) {
+    const double sumsq = cta_sum_partials(partials, nparts);
     if (threadIdx.x == 0) {
-        const double sumsq = sm[0];
         const double norm = sqrt(sumsq);
         const bool finite = isfinite(norm);
         st->sumsq = sumsq;
         st->norm = norm;
-        st->flags = finite ? 0 : kFlagNonfinite;
+        st->flags = (clip && !finite) ? kFlagNonfinite : 0;
         st->scale = (clip && finite && norm > max_norm) ? (float)(max_norm / norm) : 1.0f;
     }
+}
+
+// Per-bucket streaming: the sum of one bucket's CTA partials into the bucket's slot.
+__global__ void __launch_bounds__(kThreads) k_sum_partials(const double* partials, int nparts, double* out) {
+    const double t = cta_sum_partials(partials, nparts);
+    if (threadIdx.x == 0) *out = t;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -414,42 +426,53 @@ __device__ __forceinline__ uint4 splice(uint4 A, uint4 B, int k) {
     }
 }
 
+// out[d] = shards[lane of unpadded index u0 + d] for d in [0, count). Work item: one
+// 16-byte-aligned slot of 8 output elements (a0 = the output's misalignment in elements);
+// slots wholly inside the range whose source run lies in one bucket take one aligned
+// 16-byte store (the source run spliced from two aligned loads when it is unaligned);
+// edge slots go element by element.
 __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
-                                                     uint16_t* __restrict__ full, const Bucket* tab, int64_t nb,
-                                                     int64_t npad, int64_t u_begin, int64_t u_end) {
-    const int64_t w_first = u_begin >> 3, w_last = (u_end + 7) >> 3;
+                                                     uint16_t* __restrict__ out, const Bucket* tab, int64_t nb,
+                                                     int64_t npad, int64_t u0, int64_t count) {
+    const int64_t a0 = (int64_t)((reinterpret_cast<uintptr_t>(out) >> 1) & 7);
+    const int64_t nslots = (count + a0 + 7) >> 3;
     const int64_t stride = (int64_t)gridDim.x * kThreadsGather;
-    for (int64_t wi = w_first + (int64_t)blockIdx.x * kThreadsGather + threadIdx.x; wi < w_last; wi += stride) {
-        const int64_t u = wi * 8;
-        const int64_t b = bucket_of_unpadded(tab, nb, u);
-        const Bucket e = tab[b];
-        if (u >= u_begin && u + 8 <= u_end && u >= e.uoff && u + 8 <= e.uoff + e.n) {
-            const int64_t src = u - e.uoff + e.off;
-            const int k = (int)(src & 7);
-            const uint16_t* base = shards + (src - k);
-            if (k == 0) {
-                st_u4(full + u, ld_u4(base));
-                continue;
-            }
-            if (src - k + 8 < npad) {
-                st_u4(full + u, splice(ld_u4(base), ld_u4(base + 8), k));
-                continue;
+    for (int64_t w = (int64_t)blockIdx.x * kThreadsGather + threadIdx.x; w < nslots; w += stride) {
+        const int64_t d0 = w * 8 - a0;  // first output element of the slot (may be < 0)
+        if (d0 >= 0 && d0 + 8 <= count) {
+            const int64_t u = u0 + d0;
+            const Bucket e = tab[bucket_of_unpadded(tab, nb, u)];
+            if (u + 8 <= e.uoff + e.n) {
+                const int64_t src = u - e.uoff + e.off;
+                const int k = (int)(src & 7);
+                const uint16_t* base = shards + (src - k);
+                if (k == 0) {
+                    st_u4(out + d0, ld_u4(base));
+                    continue;
+                }
+                if (src - k + 8 < npad) {
+                    st_u4(out + d0, splice(ld_u4(base), ld_u4(base + 8), k));
+                    continue;
+                }
             }
         }
         for (int i = 0; i < 8; ++i) {
-            const int64_t uu = u + i;
-            if (uu < u_begin || uu >= u_end) continue;
+            const int64_t d = d0 + i;
+            if (d < 0 || d >= count) continue;
+            const int64_t uu = u0 + d;
             const Bucket f = tab[bucket_of_unpadded(tab, nb, uu)];
-            full[uu] = shards[uu - f.uoff + f.off];
+            out[d] = shards[uu - f.uoff + f.off];
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------
-// Initial state: master = unpadded init scattered into the padded layout (padding 0),
-// m = v = 0, bf16 copies of the parameters. One lane per thread (not a hot kernel).
+// State in: master (and optionally m, v; zeros when null) from unpadded vectors scattered
+// into the padded layout (padding 0), plus the bf16 copies of the parameters. One lane per
+// thread (not a hot kernel). Serves initialisation and checkpoint loading.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__ init, float* master, float* m,
+__global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__ init, const float* __restrict__ m_init,
+                                                   const float* __restrict__ v_init, float* master, float* m,
                                                    float* v, uint16_t* full, uint16_t* shards, const Bucket* tab,
                                                    int64_t nb, int64_t npad) {
     const int64_t stride = (int64_t)gridDim.x * kThreadsInit;
@@ -463,11 +486,31 @@ __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__
         const int64_t u = o - c.e.off + c.e.uoff;
         const float x = real ? init[u] : 0.0f;
         master[o] = x;
-        m[o] = 0.0f;
-        v[o] = 0.0f;
+        m[o] = (real && m_init) ? m_init[u] : 0.0f;
+        v[o] = (real && v_init) ? v_init[u] : 0.0f;
         const uint16_t h = to_bf16(x);
         if (shards) shards[o] = h;
         if (real && full) full[u] = h;
+    }
+}
+
+// State out: the real lanes of master, m and v gathered into unpadded vectors (the layout-
+// independent form a checkpoint keeps, loadable under any rank count or bucket size).
+__global__ void __launch_bounds__(kThreadsInit) k_save(const float* __restrict__ master, const float* __restrict__ m,
+                                                   const float* __restrict__ v, float* out_master, float* out_m,
+                                                   float* out_v, const Bucket* tab, int64_t nb, int64_t npad) {
+    const int64_t stride = (int64_t)gridDim.x * kThreadsInit;
+    int64_t o = (int64_t)blockIdx.x * kThreadsInit + threadIdx.x;
+    if (o >= npad) return;
+    Cursor c;
+    c.init(tab, nb, o);
+    for (; o < npad; o += stride) {
+        c.seek(o);
+        if (o >= c.e.off + c.e.n) continue;
+        const int64_t u = o - c.e.off + c.e.uoff;
+        if (out_master) out_master[u] = master[o];
+        if (out_m) out_m[u] = m[o];
+        if (out_v) out_v[u] = v[o];
     }
 }
 
@@ -554,6 +597,11 @@ cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, do
     return cudaGetLastError();
 }
 
+cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s) {
+    k_sum_partials<<<1, kThreads, 0, s>>>(partials, nparts, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s) {
     k_adamw<<<grid, kThreadsAdamw, 0, s>>>(a);
     return cudaGetLastError();
@@ -565,18 +613,25 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaS
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t* shards, uint16_t* full, const Bucket* buckets, int64_t nb, int64_t npad,
-                          int64_t u_begin, int64_t u_end, int grid, cudaStream_t s) {
-    if (u_end <= u_begin) return cudaSuccess;
-    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, full, buckets, nb, npad, u_begin, u_end);
+cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb, int64_t npad,
+                          int64_t u0, int64_t count, int grid, cudaStream_t s) {
+    if (count <= 0) return cudaSuccess;
+    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count);
     return cudaGetLastError();
 }
 
-cudaError_t launch_init(const float* master_init, float* master, float* m, float* v, uint16_t* full,
-                        uint16_t* shards, const Bucket* buckets, int64_t nb, int64_t npad, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init, float* master, float* m,
+                        float* v, uint16_t* full, uint16_t* shards, const Bucket* buckets, int64_t nb, int64_t npad,
+                        int grid, cudaStream_t s) {
     if (npad <= 0) return cudaSuccess;
-    k_init<<<grid, kThreadsInit, 0, s>>>(master_init, master, m, v, full, shards, buckets, nb, npad);
+    k_init<<<grid, kThreadsInit, 0, s>>>(master_init, m_init, v_init, master, m, v, full, shards, buckets, nb, npad);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_save(const float* master, const float* m, const float* v, float* out_master, float* out_m,
+                        float* out_v, const Bucket* buckets, int64_t nb, int64_t npad, int grid, cudaStream_t s) {
+    if (npad <= 0) return cudaSuccess;
+    k_save<<<grid, kThreadsInit, 0, s>>>(master, m, v, out_master, out_m, out_v, buckets, nb, npad);
     return cudaGetLastError();
 }
 

@@ -149,6 +149,9 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     a.buckets = table;
     a.nb = n_buckets;
     a.nvec = npad / 8;
+    a.vbeg = 0;
+    a.vend = a.nvec;
+    a.gbase = 0;
     a.M = M;
     a.inv_M = (float)(1.0 / (double)M);
     a.status = status;
