@@ -98,6 +98,14 @@ def _load():
             lib.orc_zero_step.argtypes = [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           ctypes.POINTER(Hyper), _I64,
                                           ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]
+            lib.orc_hsdp_step.restype = ctypes.c_int
+            lib.orc_hsdp_step.argtypes = [_I32, _I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          ctypes.POINTER(Hyper), _I64,
+                                          ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]
+            lib.orc_naive_dp_step_groups.restype = ctypes.c_int
+            lib.orc_naive_dp_step_groups.argtypes = [_I32, _I32, _I64, _P, _P, _P, _P, _P, ctypes.POINTER(Hyper),
+                                                     _I64, ctypes.POINTER(ctypes.c_double),
+                                                     ctypes.POINTER(ctypes.c_float)]
             lib.orc_naive_dp_step.restype = ctypes.c_int
             lib.orc_naive_dp_step.argtypes = [_I32, _I64, _P, _P, _P, _P, _P, ctypes.POINTER(Hyper), _I64,
                                               ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]
@@ -266,11 +274,23 @@ class RankState:
     ghat: list
     param: list  # stage 1/2: full bf16 replicas (N); stage 3: bf16 shards (shard_len)
     t: int = 0   # steps taken
+    groups: int = 1  # hybrid sharding: G groups of p.M owners each (structures grp * p.M + k)
 
 
-def init_state(p: Plan, stage: int, master_init: np.ndarray, m_init=None, v_init=None, t: int = 0) -> RankState:
-    """Rank structures from unpadded state (m, v default to zeros; t = steps already taken)."""
+def init_state(p: Plan, stage: int, master_init: np.ndarray, m_init=None, v_init=None, t: int = 0,
+               groups: int = 1) -> RankState:
+    """Rank structures from unpadded state (m, v default to zeros; t = steps already taken).
+    With groups > 1 (hybrid sharding) p is planned for the K owners of one group and every
+    group gets its own copy of the K structures."""
     assert stage in (1, 2, 3)
+    if groups > 1:
+        one = init_state(p, stage, master_init, m_init, v_init, t)
+        copies = [init_state(p, stage, master_init, m_init, v_init, t) for _ in range(groups - 1)]
+        for c in copies:
+            for f in ("master", "mom", "var", "ghat", "param"):
+                getattr(one, f).extend(getattr(c, f))
+        one.groups = groups
+        return one
     mi = np.ascontiguousarray(master_init, dtype=np.float32)
     assert mi.size == p.N
     mm = None if m_init is None else np.ascontiguousarray(m_init, dtype=np.float32)
@@ -290,16 +310,20 @@ def init_state(p: Plan, stage: int, master_init: np.ndarray, m_init=None, v_init
 
 
 def zero_step(p: Plan, st: RankState, grads, h: Hyper):
-    """One ZeRO step; returns (full bf16 params [N] as uint16, norm, scale, rc)."""
+    """One ZeRO step (hybrid-sharded when st.groups > 1, with groups * p.M rank gradients);
+    returns (full bf16 params [N] as uint16, norm, scale, rc)."""
     g = [np.ascontiguousarray(x, dtype=np.uint16) for x in grads]
-    assert len(g) == p.M and all(x.size == p.npad for x in g)
+    assert len(g) == p.M * st.groups and all(x.size == p.npad for x in g)
     full = np.empty(max(p.N, 1), dtype=np.uint16)
     norm, scale = ctypes.c_double(0.0), ctypes.c_float(0.0)
     st.t += 1
-    rc = _load().orc_zero_step(p.M, st.stage, p.nb, _ptr(p.b_off), _ptr(p.b_n), _ptr(p.b_S), _ptr_array(g),
-                               _ptr_array(st.master), _ptr_array(st.mom), _ptr_array(st.var),
-                               _ptr_array(st.ghat), _ptr_array(st.param), _ptr(full), ctypes.byref(h), st.t,
-                               ctypes.byref(norm), ctypes.byref(scale))
+    args = (p.nb, _ptr(p.b_off), _ptr(p.b_n), _ptr(p.b_S), _ptr_array(g), _ptr_array(st.master),
+            _ptr_array(st.mom), _ptr_array(st.var), _ptr_array(st.ghat), _ptr_array(st.param), _ptr(full),
+            ctypes.byref(h), st.t, ctypes.byref(norm), ctypes.byref(scale))
+    if st.groups > 1:
+        rc = _load().orc_hsdp_step(st.groups, p.M, st.stage, *args)
+    else:
+        rc = _load().orc_zero_step(p.M, st.stage, *args)
     if rc < 0:
         raise AssertionError("oracle: gathered replicas disagree")
     return full[:p.N], norm.value, scale.value, rc
@@ -333,16 +357,17 @@ def naive_dp_init(M: int, master_init: np.ndarray) -> DPState:
     return DPState(master, mom, var, param)
 
 
-def naive_dp_step(st: DPState, grads_unpadded, h: Hyper):
-    """One naive-DP step on full replicas; returns (bf16 params, norm, scale, rc)."""
+def naive_dp_step(st: DPState, grads_unpadded, h: Hyper, groups: int = 1):
+    """One naive-DP step on full replicas (all-reduce summed group by group when groups > 1);
+    returns (bf16 params, norm, scale, rc)."""
     g = [np.ascontiguousarray(x, dtype=np.uint16) for x in grads_unpadded]
     M = len(g)
     N = int(g[0].size)
     norm, scale = ctypes.c_double(0.0), ctypes.c_float(0.0)
     st.t += 1
-    rc = _load().orc_naive_dp_step(M, N, _ptr_array(g), _ptr_array(st.master), _ptr_array(st.mom),
-                                   _ptr_array(st.var), _ptr_array(st.param), ctypes.byref(h), st.t,
-                                   ctypes.byref(norm), ctypes.byref(scale))
+    rc = _load().orc_naive_dp_step_groups(M, groups, N, _ptr_array(g), _ptr_array(st.master), _ptr_array(st.mom),
+                                          _ptr_array(st.var), _ptr_array(st.param), ctypes.byref(h), st.t,
+                                          ctypes.byref(norm), ctypes.byref(scale))
     if rc < 0:
         raise AssertionError("oracle: naive-DP replicas disagree")
     return st.param[0][:N].copy(), norm.value, scale.value, rc

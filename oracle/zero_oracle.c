@@ -147,34 +147,60 @@ static int64_t orc_shard_len(int64_t nb, const int64_t* b_S)
 /* ------------------------------------------------------------------------------------ */
 /* Gradient average of one lane over the M emulated ranks ([L8] Slide 15; [EQ] 2.1       */
 /* all_reduce with ReduceOp.AVG; [JZ] DP identity grad = (1/N) sum_i g_i; [231] 4.1).    */
+/* With G > 1 (hybrid sharding, [231] 4.4: M = G x K ranks, sharded inside each group of  */
+/* K, replicated across the G groups), rank q = grp*K + k: each group's K values are      */
+/* summed in order (the reduce-scatter inside the group), then the G group sums in order  */
+/* (the all-reduce across groups), then the one multiplication by 1/M.                    */
 /* ------------------------------------------------------------------------------------ */
+static float orc_rank_average_grouped(int32_t M, int32_t G, const uint16_t* const* g, int64_t o)
+{
+    float inv_M = (float)(1.0 / (double)M);
+    if (G <= 1) {
+        float acc = 0.0f; /* +0: a sum of -0 replicas is +0 */
+        for (int32_t r = 0; r < M; ++r) acc = acc + orc_bf16_to_f32(g[r][o]);
+        return acc * inv_M;
+    }
+    int32_t K = M / G;
+    float acc = 0.0f;
+    for (int32_t grp = 0; grp < G; ++grp) {
+        float part = 0.0f;
+        for (int32_t k = 0; k < K; ++k) part = part + orc_bf16_to_f32(g[grp * K + k][o]);
+        acc = acc + part;
+    }
+    return acc * inv_M;
+}
+
 static float orc_rank_average(int32_t M, const uint16_t* const* g, int64_t o)
 {
-    float acc = 0.0f; /* +0: a sum of -0 replicas is +0 */
-    for (int32_t r = 0; r < M; ++r) acc = acc + orc_bf16_to_f32(g[r][o]);
-    float inv_M = (float)(1.0 / (double)M);
-    return acc * inv_M;
+    return orc_rank_average_grouped(M, 1, g, o);
 }
 
 /* ------------------------------------------------------------------------------------ */
 /* Reduce-scatter ([L8] Slide 20 step 2; [EQ] 2.2.1 step 2, reduce_scatter_sum): owner r  */
 /* receives, for each lane of its shard, the average over ranks. Padding lanes get +0.    */
-/* grads[q] is rank q's full padded gradient; ghat[r] is owner r's shard.                 */
+/* grads[q] is rank q's full padded gradient; ghat[r] is owner r's shard. K owners, M     */
+/* ranks in G groups (K = M, G = 1 without hybrid sharding).                              */
 /* ------------------------------------------------------------------------------------ */
-void orc_reduce_scatter(int32_t M, int64_t nb, const int64_t* b_off, const int64_t* b_n,
-                        const int64_t* b_S, const uint16_t* const* grads, float* const* ghat)
+static void orc_rs(int32_t K, int32_t M, int32_t G, int64_t nb, const int64_t* b_off, const int64_t* b_n,
+                   const int64_t* b_S, const uint16_t* const* grads, float* const* ghat)
 {
-    for (int32_t r = 0; r < M; ++r) {
+    for (int32_t r = 0; r < K; ++r) {
         int64_t base = 0; /* start of bucket b's slice inside rank r's shard */
         for (int64_t b = 0; b < nb; ++b) {
             for (int64_t j = 0; j < b_S[b]; ++j) {
                 int64_t in_bucket = (int64_t)r * b_S[b] + j;
                 int64_t o = b_off[b] + in_bucket;
-                ghat[r][base + j] = (in_bucket < b_n[b]) ? orc_rank_average(M, grads, o) : 0.0f;
+                ghat[r][base + j] = (in_bucket < b_n[b]) ? orc_rank_average_grouped(M, G, grads, o) : 0.0f;
             }
             base += b_S[b];
         }
     }
+}
+
+void orc_reduce_scatter(int32_t M, int64_t nb, const int64_t* b_off, const int64_t* b_n,
+                        const int64_t* b_S, const uint16_t* const* grads, float* const* ghat)
+{
+    orc_rs(M, M, 1, nb, b_off, b_n, b_S, grads, ghat);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -341,18 +367,21 @@ static void orc_all_gather(int32_t M, int64_t nb, const int64_t* b_n, const int6
 /* Returns 0, or 1 when clipping is on and the norm is not finite (state left untouched), */
 /* or -1 when the M gathered replicas disagree.                                           */
 /* ------------------------------------------------------------------------------------ */
-int orc_zero_step(int32_t M, int32_t stage, int64_t nb, const int64_t* b_off,
-                  const int64_t* b_n, const int64_t* b_S, const uint16_t* const* grads,
-                  float* const* master, float* const* mom, float* const* var,
-                  float* const* ghat, uint16_t* const* param, uint16_t* full_out,
-                  const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
+/* The step of one sharding group: K owners (and K receivers of the all-gather); the    */
+/* average runs over M ranks in G groups.                                                 */
+static int orc_step_core(int32_t K, int32_t Mtot, int32_t G, int32_t stage, int64_t nb, const int64_t* b_off,
+                         const int64_t* b_n, const int64_t* b_S, const uint16_t* const* grads,
+                         float* const* master, float* const* mom, float* const* var,
+                         float* const* ghat, uint16_t* const* param, uint16_t* full_out,
+                         const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
 {
+    const int32_t M = K; /* owners and receivers of this group */
     int64_t slen = orc_shard_len(nb, b_S);
     int64_t N = 0;
     for (int64_t b = 0; b < nb; ++b) N += b_n[b];
 
     /* (2) reduce-scatter: every owner receives the averaged gradient of its shard. */
-    orc_reduce_scatter(M, nb, b_off, b_n, b_S, grads, ghat);
+    orc_rs(K, Mtot, G, nb, b_off, b_n, b_S, grads, ghat);
 
     /* norm and clip scale */
     double norm = sqrt(orc_global_sumsq(M, nb, b_n, b_S, (const float* const*)ghat));
@@ -395,6 +424,53 @@ int orc_zero_step(int32_t M, int32_t stage, int64_t nb, const int64_t* b_off,
     return rc;
 }
 
+int orc_zero_step(int32_t M, int32_t stage, int64_t nb, const int64_t* b_off,
+                  const int64_t* b_n, const int64_t* b_S, const uint16_t* const* grads,
+                  float* const* master, float* const* mom, float* const* var,
+                  float* const* ghat, uint16_t* const* param, uint16_t* full_out,
+                  const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
+{
+    return orc_step_core(M, M, 1, stage, nb, b_off, b_n, b_S, grads, master, mom, var, ghat, param, full_out,
+                         h, t, norm_out, scale_out);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Hybrid sharded data parallelism ([231] 4.4): M = G x K ranks; the state is sharded over */
+/* the K ranks of each group (the layout b_off / b_S is planned for K owners) and every   */
+/* group holds a replica of it. The rank structures are G x K: structure grp*K + k is     */
+/* owner k of group grp. Each group runs the ZeRO step on the average over all M ranks    */
+/* (reduce-scatter inside the group, all-reduce of the shard across groups); the G        */
+/* replicas must agree. Returns 0, 1 (skipped, non-finite norm) or -1 (replicas differ).  */
+/* ------------------------------------------------------------------------------------ */
+int orc_hsdp_step(int32_t G, int32_t K, int32_t stage, int64_t nb, const int64_t* b_off,
+                  const int64_t* b_n, const int64_t* b_S, const uint16_t* const* grads,
+                  float* const* master, float* const* mom, float* const* var,
+                  float* const* ghat, uint16_t* const* param, uint16_t* full_out,
+                  const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
+{
+    int64_t N = 0;
+    for (int64_t b = 0; b < nb; ++b) N += b_n[b];
+    uint16_t* other = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(N > 0 ? N : 1));
+    int rc = 0;
+    for (int32_t grp = 0; grp < G; ++grp) {
+        double norm;
+        float s;
+        uint16_t* dst = grp == 0 ? full_out : other;
+        int r = orc_step_core(K, G * K, G, stage, nb, b_off, b_n, b_S, grads, master + grp * K, mom + grp * K,
+                              var + grp * K, ghat + grp * K, param + grp * K, dst, h, t, &norm, &s);
+        if (grp == 0) {
+            *norm_out = norm;
+            *scale_out = s;
+            rc = r;
+        } else if (r != rc || memcmp(dst, full_out, sizeof(uint16_t) * (size_t)N) != 0 ||
+                   !(norm == *norm_out || (norm != norm && *norm_out != *norm_out)) || s != *scale_out) {
+            rc = -1;
+        }
+    }
+    free(other);
+    return rc;
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Naive data parallelism ([L8] Slides 15-16; [EQ] 2.1 pseudocode): every rank holds the  */
 /* full unpadded state, all-reduces (averages) the full gradient and runs the same AdamW  */
@@ -403,14 +479,15 @@ int orc_zero_step(int32_t M, int32_t stage, int64_t nb, const int64_t* b_off,
 /* parallel"; [JZ]: the computation does not change, only where W and g are stored).      */
 /* Returns 0, 1 (non-finite norm, skipped) or -1 (replicas disagree).                      */
 /* ------------------------------------------------------------------------------------ */
-int orc_naive_dp_step(int32_t M, int64_t N, const uint16_t* const* grads, float* const* master,
-                      float* const* mom, float* const* var, uint16_t* const* param,
-                      const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
+int orc_naive_dp_step_groups(int32_t M, int32_t G, int64_t N, const uint16_t* const* grads,
+                             float* const* master, float* const* mom, float* const* var,
+                             uint16_t* const* param, const orc_hyper* h, int64_t t, double* norm_out,
+                             float* scale_out)
 {
     float* gbar = (float*)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
     int rc = 0;
     for (int32_t q = 0; q < M; ++q) {
-        for (int64_t u = 0; u < N; ++u) gbar[u] = orc_rank_average(M, grads, u); /* all-reduce */
+        for (int64_t u = 0; u < N; ++u) gbar[u] = orc_rank_average_grouped(M, G, grads, u); /* all-reduce */
         double acc = 0.0;
         for (int64_t u = 0; u < N; ++u) acc += (double)gbar[u] * (double)gbar[u];
         double norm = sqrt(acc);
@@ -435,6 +512,13 @@ int orc_naive_dp_step(int32_t M, int64_t N, const uint16_t* const* grads, float*
     }
     free(gbar);
     return rc;
+}
+
+int orc_naive_dp_step(int32_t M, int64_t N, const uint16_t* const* grads, float* const* master,
+                      float* const* mom, float* const* var, uint16_t* const* param,
+                      const orc_hyper* h, int64_t t, double* norm_out, float* scale_out)
+{
+    return orc_naive_dp_step_groups(M, 1, N, grads, master, mom, var, param, h, t, norm_out, scale_out);
 }
 
 /* ------------------------------------------------------------------------------------ */

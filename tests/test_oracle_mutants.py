@@ -38,6 +38,8 @@ MUTANTS = [
     ("bucket cap ignored", "cur_bytes + bytes > bucket_bytes);", "cur_bytes + bytes > 2 * bucket_bytes);"),
     ("gather to padded place", "if (in_bucket < b_n[b]) dst[ubase + in_bucket] = shard_bf16[r][base + j];",
      "if (in_bucket < b_n[b]) dst[base * 0 + in_bucket + b * 1] = shard_bf16[r][base + j];"),
+    ("groups summed flat", "        for (int32_t k = 0; k < K; ++k) part = part + orc_bf16_to_f32(g[grp * K + k][o]);\n        acc = acc + part;",
+     "        for (int32_t k = 0; k < K; ++k) acc = acc + orc_bf16_to_f32(g[grp * K + k][o]);\n        part = part + acc;"),
     ("nonfinite not skipped", "if (!isfinite(norm)) skipped = 1;\n        else s = orc_clip_scale(norm, h->max_grad_norm);\n    }\n    *scale_out = s;",
      "s = orc_clip_scale(norm, h->max_grad_norm);\n    }\n    *scale_out = s;"),
 ]

@@ -557,3 +557,79 @@ def test_lane_steps_equal_full_step():
     assert np.array_equal(mm, O.flat_state(p, st, "mom")[lanes])
     assert np.array_equal(vv, O.flat_state(p, st, "var")[lanes])
     assert np.array_equal(bfv, O.bf16_rne(pp))
+
+
+# ------------------------------------------------------------------------------------------
+# Hybrid sharding ("CS231n Lecture 11" 4.4): M = G x K, sharded in groups of K, replicated
+# across the G groups; the average is summed inside each group, then across groups.
+# ------------------------------------------------------------------------------------------
+def test_hsdp_group_order_pin():
+    """G = 2, K = 2, one lane with values 1, 2^-24, 2^-24, 2^-24: flat order gives
+    ((1 + 2^-24) + 2^-24) + 2^-24 = 1 (three ties to even); by groups
+    (1 + 2^-24) + (2^-24 + 2^-24) = 1 + 2^-23 exactly."""
+    vals = [1.0, 2.0 ** -24, 2.0 ** -24, 2.0 ** -24]
+    p2 = O.plan([1], 2, 0, 1)
+    st = O.init_state(p2, 1, np.zeros(1, np.float32), groups=2)
+    h = O.hyper(lr=0.0, beta1=0.0, weight_decay=0.0)  # m = g exactly exposes the average
+    O.zero_step(p2, st, [p2.pad(bf([v])) for v in vals], h)
+    assert st.mom[0][0] == np.float32((1.0 + 2.0 ** -23) / 4)
+    p4 = O.plan([1], 4, 0, 1)
+    st4 = O.init_state(p4, 1, np.zeros(1, np.float32))
+    O.zero_step(p4, st4, [p4.pad(bf([v])) for v in vals], h)
+    assert st4.mom[0][0] == np.float32(0.25)
+
+
+def test_hsdp_exact_integer_sums():
+    rng = np.random.default_rng(31)
+    for G, K in ((2, 2), (4, 2), (2, 8), (3, 3)):
+        M = G * K
+        p = O.plan([300, 17], K, 0, 8)
+        vals = rng.integers(-100, 101, size=(M, p.N))
+        st = O.init_state(p, 2, np.zeros(p.N, np.float32), groups=G)
+        h = O.hyper(lr=0.0, beta1=0.0, weight_decay=0.0)
+        O.zero_step(p, st, [p.pad(bf(vals[r].astype(np.float32))) for r in range(M)], h)
+        got = O.flat_state(p, st, "mom")[p.unpadded_index() >= 0].astype(np.float64)
+        exact = vals.sum(axis=0).astype(np.float64)
+        want = (exact.astype(np.float32) * np.float32(1.0 / M)).astype(np.float64)  # sums are exact in fp32
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("G,K,stage,bucket_bytes,clip", [
+    (1, 4, 1, 0, True), (2, 2, 2, 300, True), (2, 4, 3, 0, False), (4, 2, 3, 800, True), (3, 2, 1, 0, True)])
+def test_hsdp_equals_naive_dp_with_grouped_allreduce(G, K, stage, bucket_bytes, clip):
+    rng = np.random.default_rng(200 + 10 * G + K)
+    numel = [257, 1, 1000, 63]
+    N = sum(numel)
+    M = G * K
+    w0 = rng.normal(0, 0.02, N).astype(np.float32)
+    steps = [[O.bf16_rne(rng.normal(0, 1e-2, N).astype(np.float32)) for _ in range(M)] for _ in range(3)]
+    h = O.hyper(clip=clip, max_grad_norm=0.05)
+    p = O.plan(numel, K, bucket_bytes, 64)
+    st = O.init_state(p, stage, w0, groups=G)
+    dp = O.naive_dp_init(M, w0)
+    for gs in steps:
+        full, norm, s, rc = O.zero_step(p, st, [p.pad(g) for g in gs], h)
+        full_dp, norm_dp, s_dp, rc_dp = O.naive_dp_step(dp, gs, h, groups=G)
+        assert rc == rc_dp == 0 and norm == norm_dp and s == s_dp
+        assert np.array_equal(full, full_dp)
+    u = p.unpadded_index()
+    assert np.array_equal(O.flat_state(p, st, "master")[u >= 0].view(np.uint32), dp.master[0].view(np.uint32))
+    # every group's replica of the shards is the same
+    for grp in range(1, G):
+        for k in range(K):
+            assert np.array_equal(st.master[grp * K + k], st.master[k])
+
+
+def test_hsdp_one_rank_per_group_is_plain_dp():
+    """K = 1: each inner sum has one term (exact), so the grouped average is the flat one."""
+    rng = np.random.default_rng(41)
+    M, N = 5, 700
+    w0 = rng.normal(0, 0.02, N).astype(np.float32)
+    gs = [O.bf16_rne(rng.normal(0, 1e-2, N).astype(np.float32)) for _ in range(M)]
+    h = O.hyper(clip=True, max_grad_norm=0.05)
+    p = O.plan([N], 1, 0, 64)
+    st = O.init_state(p, 1, w0, groups=M)
+    dp = O.naive_dp_init(M, w0)
+    full, norm, s, _ = O.zero_step(p, st, [p.pad(g) for g in gs], h)
+    full_dp, norm_dp, s_dp, _ = O.naive_dp_step(dp, gs, h)
+    assert norm == norm_dp and np.array_equal(full, full_dp)
