@@ -38,6 +38,7 @@
  *  of its own; bucket_bytes = 0 means a single bucket). Bucket b with n_b real lanes is
  *  padded to M * S_b lanes, S_b = ceil(n_b / (M * ZERO_ALIGN)) * ZERO_ALIGN, and occupies
  *  padded lanes [off_b, off_b + M * S_b); rank r owns [off_b + r * S_b, off_b + (r+1) * S_b).
+ *  (With hybrid sharding, M here and below is the group size K = M / groups.)
  *  Real lanes of bucket b are [off_b, off_b + n_b). npad = sum of M * S_b.
  *  The unpadded index of real lane o of bucket b is o - off_b + (sum of n over earlier
  *  buckets). Padding lanes of gradient buffers are ignored (read as +0); padding lanes of
@@ -109,7 +110,13 @@ typedef struct {
     int32_t stage;        /* ZeRO stage: 1, 2 or 3                                        */
     int64_t bucket_bytes; /* bf16 gradient bytes per bucket; 0 = one bucket              */
     int32_t gather;       /* ZERO_GATHER_FUSED or ZERO_GATHER_SHARDS (stage 3 only)       */
-    int32_t reserved;     /* must be 0                                                    */
+    int32_t groups;       /* hybrid sharding ("CS231n Lecture 11" 4.4): 0 or 1 = none; G > 1
+                             splits the M ranks into G groups of K = M / G. The state is
+                             sharded over the K ranks of a group (the layout is planned for K
+                             owners) and each group holds a replica of it, of which the
+                             device keeps one copy; rank q = grp * K + k. The average sums
+                             each group's K gradients in order, then the G group sums in
+                             order, then multiplies by (float)(1/M). M % G must be 0.        */
 } zero_config;
 
 /* Hyper-parameters of one step. */

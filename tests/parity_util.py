@@ -68,17 +68,17 @@ def make_hyper(w: W.Workload, ghat_mode="auto"):
 
 
 def run_elementwise(w: W.Workload, gather="fused", ghat_mode="auto", steps=None, ghat_buffer=None,
-                    garbage_in_padding=False, check_every_step=True):
+                    garbage_in_padding=False, check_every_step=True, groups=1):
     """Runs the GPU path and the oracle side by side on w and compares everything.
     Returns a dict of the largest deviations seen."""
     dev = torch.device("cuda")
     steps = w.steps if steps is None else steps
     mi = W.master_init(w, dev)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, gather=gather,
-                           ghat_buffer=ghat_buffer)
-    p = O.plan(w.numel, w.M, w.bucket_bytes)
+                           ghat_buffer=ghat_buffer, groups=groups)
+    p = O.plan(w.numel, w.M // groups, w.bucket_bytes)  # hybrid sharding: planned for the group size
     assert p.npad == opt.sizes["npad"] and [int(x) for x in p.t_off] == opt.tensor_offsets
-    st = O.init_state(p, w.stage, f32(mi))
+    st = O.init_state(p, w.stage, f32(mi), groups=groups)
     h, oh = make_hyper(w, ghat_mode)
     sig = W.sigmas(w)
     real = p.real_mask()
@@ -116,7 +116,7 @@ def run_elementwise(w: W.Workload, gather="fused", ghat_mode="auto", steps=None,
             if gather == "shards":
                 sh = u16(opt.param_shards)
                 want_sh = np.zeros(p.npad, dtype=np.uint16)
-                for rr in range(w.M):
+                for rr in range(p.M):
                     want_sh[p.shard_lanes(rr)] = st.param[rr][:p.shard_len]
                 assert bf16_ulp_diff(sh, want_sh) <= 1
     out = dict(worst, opt=opt, plan=p, oracle_state=st)

@@ -60,6 +60,13 @@ def _cmp_with_oracle(zg, numel, M, stage, bucket_bytes):
     assert sizes["bytes_grad_each"] == 2 * p.npad and sizes["bytes_param_full"] == 2 * p.N
 
 
+def test_hybrid_sharding_plans_for_the_group_size(zg):
+    # M = 8 ranks in 2 groups: the layout is the one of 4 owners
+    for numel, bb in (([1000, 33, 4097], 0), ([300] * 9, 1500)):
+        assert zg.plan(numel, 8, 2, bb, groups=2) == zg.plan(numel, 4, 2, bb)
+        assert zg.layout(numel, 8, 3, bb, "shards", groups=2) == zg.layout(numel, 4, 3, bb, "shards")
+
+
 def test_planner_matches_oracle_random(zg):
     rng = np.random.default_rng(21)
     for _ in range(300):
@@ -89,11 +96,12 @@ def test_workload_sizes(zg):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(M=0), -1), (dict(M=65), -1), (dict(stage=0), -4), (dict(stage=4), -4),
-    (dict(bucket_bytes=-1), -1), (dict(gather=1, stage=1), -4), (dict(gather=2), -1), (dict(reserved=1), -1)])
+    (dict(bucket_bytes=-1), -1), (dict(gather=1, stage=1), -4), (dict(gather=2), -1), (dict(groups=-1), -1),
+    (dict(groups=3), -1)])
 def test_invalid_config_rejected(zg, kw, code):
-    cfg = dict(M=2, stage=3, bucket_bytes=0, gather=0, reserved=0)
+    cfg = dict(M=2, stage=3, bucket_bytes=0, gather=0, groups=0)
     cfg.update(kw)
-    c = zg.Config(cfg["M"], cfg["stage"], cfg["bucket_bytes"], cfg["gather"], cfg["reserved"])
+    c = zg.Config(cfg["M"], cfg["stage"], cfg["bucket_bytes"], cfg["gather"], cfg["groups"])
     arr = (ctypes.c_int64 * 1)(100)
     out = zg.Sizes()
     assert zg._lib().zero_plan(ctypes.byref(c), ctypes.cast(arr, ctypes.c_void_p), 1, ctypes.byref(out)) == code

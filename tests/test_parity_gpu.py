@@ -335,3 +335,17 @@ def test_guard_bands_untouched(gather, mode):
     for name, raw in list(raws.items()) + [("master_init", mi_raw)]:
         assert bool((raw[:GUARD] == 0xA5).all()) and bool((raw[-GUARD:] == 0xA5).all()), f"guard band of {name} hit"
     assert lib.zero_destroy(ctx) == 0
+
+
+# ------------------------------------------------------------------------------------------
+# Hybrid sharding ("CS231n Lecture 11" 4.4): M = G x K, state sharded over K, replicated over G
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("G,K,stage,gather,bucket_bytes,clip", [
+    (2, 4, 3, "shards", 0, 1.0), (4, 2, 1, "fused", 40000, 1.0), (3, 2, 2, "fused", 0, None),
+    (2, 8, 3, "fused", 0, 1.0), (8, 1, 1, "fused", 0, 1.0)])
+def test_hybrid_sharding_matches_oracle(G, K, stage, gather, bucket_bytes, clip):
+    w = W.small_variant(W.config(3), ragged(40, 200, 6000, 23), M=G * K, stage=stage,
+                        bucket_bytes=bucket_bytes, clip=clip, steps=3)
+    for mode in (("materialize", "recompute") if clip else ("auto",)):
+        out = run_elementwise(w, gather=gather, groups=G, ghat_mode=mode, ghat_buffer=True)
+        assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0

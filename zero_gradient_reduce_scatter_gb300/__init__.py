@@ -57,7 +57,7 @@ class ZeroError(RuntimeError):
 # ---- ctypes mirrors of the ABI structs --------------------------------------------------
 class Config(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int32), ("stage", ctypes.c_int32), ("bucket_bytes", ctypes.c_int64),
-                ("gather", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("gather", ctypes.c_int32), ("groups", ctypes.c_int32)]
 
 
 class Hyper(ctypes.Structure):
@@ -158,20 +158,20 @@ def _stream_handle(stream) -> int:
 
 
 # ---- host-only planning -----------------------------------------------------------------
-def plan(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused") -> dict:
+def plan(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused", groups: int = 1) -> dict:
     """Layout sizes of the ZeRO step (host only, no CUDA)."""
-    cfg = Config(M, stage, bucket_bytes, GATHER[gather], 0)
+    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups)
     arr = _i64_array(numel)
     out = Sizes()
     _check(_lib().zero_plan(ctypes.byref(cfg), ctypes.cast(arr, _P), len(numel), ctypes.byref(out)), "zero_plan")
     return {k: getattr(out, k) for k, _ in Sizes._fields_}
 
 
-def layout(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused"):
+def layout(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused", groups: int = 1):
     """(tensor_offsets, buckets): padded start lane of each tensor and, per bucket,
     (off, n, S, first_tensor)."""
-    sizes = plan(numel, M, stage, bucket_bytes, gather)
-    cfg = Config(M, stage, bucket_bytes, GATHER[gather], 0)
+    sizes = plan(numel, M, stage, bucket_bytes, gather, groups)
+    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups)
     arr = _i64_array(numel)
     toff = (ctypes.c_int64 * max(len(numel), 1))()
     btab = (ctypes.c_int64 * max(4 * sizes["n_buckets"], 1))()
@@ -195,13 +195,15 @@ class ZeroOptimizer:
     """
 
     def __init__(self, numel, M: int, stage: int, master_init: torch.Tensor, bucket_bytes: int = 0,
-                 gather: str = "fused", ghat_buffer: bool | None = None, stream=None):
+                 gather: str = "fused", ghat_buffer: bool | None = None, stream=None, groups: int = 1):
         if not (isinstance(master_init, torch.Tensor) and master_init.is_cuda and master_init.dtype == torch.float32):
             raise TypeError("master_init must be a CUDA float32 tensor of the unpadded parameters")
         self.numel = [int(x) for x in numel]
         self.M, self.stage, self.bucket_bytes, self.gather = int(M), int(stage), int(bucket_bytes), gather
-        self.sizes = plan(self.numel, M, stage, bucket_bytes, gather)
-        self.tensor_offsets, self.buckets = layout(self.numel, M, stage, bucket_bytes, gather)
+        self.groups = max(1, int(groups))
+        self.K = self.M // self.groups  # owners sharing one copy of the state
+        self.sizes = plan(self.numel, M, stage, bucket_bytes, gather, self.groups)
+        self.tensor_offsets, self.buckets = layout(self.numel, M, stage, bucket_bytes, gather, self.groups)
         s = self.sizes
         if master_init.numel() != s["n"]:
             raise ValueError(f"master_init has {master_init.numel()} values, the tensors {s['n']}")
@@ -223,7 +225,7 @@ class ZeroOptimizer:
                        self.ghat.data_ptr() if self.ghat is not None else None, self.param_full.data_ptr(),
                        self.param_shards.data_ptr() if self.param_shards is not None else None,
                        self.scratch.data_ptr())
-        cfg = Config(M, stage, bucket_bytes, GATHER[gather], 0)
+        cfg = Config(M, stage, bucket_bytes, GATHER[gather], self.groups)
         arr = _i64_array(self.numel)
         ctx = _P()
         mi = master_init.contiguous()
@@ -273,7 +275,7 @@ class ZeroOptimizer:
     # -- ZeRO-2 per-bucket streaming ----------------------------------------------------------
     def bucket_lanes(self, bucket: int) -> int:
         off, n, S, _ = self.buckets[bucket]
-        return self.M * S
+        return self.K * S
 
     def new_bucket_grad_buffers(self, bucket: int):
         """M zeroed bf16 buffers for one bucket (M * S_b lanes each)."""

@@ -102,11 +102,15 @@ struct Layout {
     int64_t npad = 0, n = 0, shard_len = 0;
 };
 
+// Ranks that share one copy of the sharded state: K = M without hybrid sharding, M / groups with.
+int shard_count(const zero_config* cfg) { return cfg->groups > 1 ? cfg->M / cfg->groups : cfg->M; }
+
 int check_config(const zero_config* cfg) {
     if (!cfg) return ZERO_ERR_INVALID_ARG;
     if (cfg->stage < 1 || cfg->stage > 3) return ZERO_ERR_STAGE;
     if (cfg->M < 1 || cfg->M > ZERO_MAX_RANKS) return ZERO_ERR_INVALID_ARG;
-    if (cfg->bucket_bytes < 0 || cfg->reserved != 0) return ZERO_ERR_INVALID_ARG;
+    if (cfg->bucket_bytes < 0 || cfg->groups < 0) return ZERO_ERR_INVALID_ARG;
+    if (cfg->groups > 1 && cfg->M % cfg->groups != 0) return ZERO_ERR_INVALID_ARG;
     if (cfg->gather != ZERO_GATHER_FUSED && cfg->gather != ZERO_GATHER_SHARDS) return ZERO_ERR_INVALID_ARG;
     if (cfg->gather == ZERO_GATHER_SHARDS && cfg->stage != 3) return ZERO_ERR_STAGE;
     return ZERO_OK;
@@ -123,7 +127,7 @@ int make_layout(const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
     }
     if (total <= 0 || total > (int64_t(1) << 42)) return ZERO_ERR_INVALID_ARG;
 
-    const int64_t M = cfg->M, cap = cfg->bucket_bytes;
+    const int64_t M = shard_count(cfg), cap = cfg->bucket_bytes;  // owners per copy of the state
     L->tensor_off.assign((size_t)n_tensors, 0);
     std::vector<int64_t> bucket_real;  // real lanes per bucket
     int64_t open_bytes = 0;
@@ -262,6 +266,7 @@ zg::StepArgs base_args(zero_ctx* c) {
     a.gbase = 0;
     a.M = c->cfg.M;
     a.inv_M = (float)(1.0 / (double)c->cfg.M);
+    a.groups = c->cfg.groups > 1 ? c->cfg.groups : 1;
     a.status = c->status;
     a.partials = c->partials;
     return a;
@@ -301,7 +306,7 @@ int zero_plan_layout(const zero_config* cfg, const int64_t* numel, int64_t n_ten
             const zg::Bucket& e = L.buckets[b];
             bucket_table[4 * b + 0] = e.off;
             bucket_table[4 * b + 1] = e.n;
-            bucket_table[4 * b + 2] = (e.end - e.off) / cfg->M;
+            bucket_table[4 * b + 2] = (e.end - e.off) / shard_count(cfg);
             bucket_table[4 * b + 3] = L.first_tensor[b];
         }
     }
@@ -622,7 +627,7 @@ int zero_bucket_info(zero_ctx* c, int64_t bucket, int64_t* uoff, int64_t* n) {
 
 int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
-    if (!dst || rank < 0 || rank >= c->cfg.M) return ZERO_ERR_INVALID_ARG;
+    if (!dst || rank < 0 || rank >= shard_count(&c->cfg)) return ZERO_ERR_INVALID_ARG;
     const float* src = nullptr;
     switch (which) {
         case ZERO_STATE_MASTER: src = (const float*)c->bufs.master; break;
@@ -637,7 +642,7 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     float* d = (float*)dst;
     for (const zg::Bucket& e : c->buckets) {
-        const int64_t S = (e.end - e.off) / c->cfg.M;
+        const int64_t S = (e.end - e.off) / shard_count(&c->cfg);
         cudaError_t ce = cudaMemcpyAsync(d, src + e.off + rank * S, sizeof(float) * (size_t)S,
                                          cudaMemcpyDeviceToDevice, s);
         if (ce != cudaSuccess) return cuda_fail(ce);

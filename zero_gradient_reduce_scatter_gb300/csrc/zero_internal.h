@@ -54,7 +54,7 @@ struct StepArgs {
     int32_t M;
     float inv_M;          // (float)(1.0 / M)
     int32_t out_shards;   // 1: `out` is the padded shard buffer; 0: the unpadded full buffer
-    int32_t reserved;
+    int32_t groups;       // hybrid sharding: M ranks in `groups` groups (1 = none)
     AdamConsts k;
     Status* status;
     double* partials;     // one fp64 partial sum of squares per CTA of the norm pass

@@ -107,10 +107,31 @@ __device__ __forceinline__ void add8(float acc[8], uint4 q) {
     acc[7] = __fadd_rn(acc[7], bf_hi(q.w));
 }
 
+// Hybrid sharding: rank q = grp * K + k; each group's K values summed in order (the
+// reduce-scatter inside the group), then the group sums in order (the all-reduce of the
+// shard across groups).
+template <int PATH>
+__device__ __noinline__ void rank_sum_grouped(const StepArgs& a, int64_t o, float acc[8]) {
+    const int K = a.M / a.groups;
+    const int64_t g = o - a.gbase;
+    for (int grp = 0; grp < a.groups; ++grp) {
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+        for (int k = 0; k < K; ++k) add8(part, ld_grad<PATH>(a.grads[grp * K + k] + g));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], part[i]);
+    }
+}
+
 template <int MT, int PATH>
 __device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t o, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
+    if (a.groups > 1) {
+        rank_sum_grouped<PATH>(a, o, acc);
+        return;
+    }
     if constexpr (MT > 0) {
         uint4 q[MT];
 #pragma unroll

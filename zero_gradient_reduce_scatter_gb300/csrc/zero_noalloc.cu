@@ -154,6 +154,7 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     a.gbase = 0;
     a.M = M;
     a.inv_M = (float)(1.0 / (double)M);
+    a.groups = 1;
     a.status = status;
     a.partials = partials;
     int64_t need = (a.nvec + zg::kThreadsRsNormOnly - 1) / zg::kThreadsRsNormOnly;
