@@ -160,7 +160,7 @@ def _stream_handle(stream) -> int:
 # ---- host-only planning -----------------------------------------------------------------
 def plan(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused", groups: int = 1) -> dict:
     """Layout sizes of the ZeRO step (host only, no CUDA)."""
-    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups)
+    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups if groups > 1 else 0)
     arr = _i64_array(numel)
     out = Sizes()
     _check(_lib().zero_plan(ctypes.byref(cfg), ctypes.cast(arr, _P), len(numel), ctypes.byref(out)), "zero_plan")
@@ -171,7 +171,7 @@ def layout(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fuse
     """(tensor_offsets, buckets): padded start lane of each tensor and, per bucket,
     (off, n, S, first_tensor)."""
     sizes = plan(numel, M, stage, bucket_bytes, gather, groups)
-    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups)
+    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups if groups > 1 else 0)
     arr = _i64_array(numel)
     toff = (ctypes.c_int64 * max(len(numel), 1))()
     btab = (ctypes.c_int64 * max(4 * sizes["n_buckets"], 1))()
@@ -225,7 +225,7 @@ class ZeroOptimizer:
                        self.ghat.data_ptr() if self.ghat is not None else None, self.param_full.data_ptr(),
                        self.param_shards.data_ptr() if self.param_shards is not None else None,
                        self.scratch.data_ptr())
-        cfg = Config(M, stage, bucket_bytes, GATHER[gather], self.groups)
+        cfg = Config(M, stage, bucket_bytes, GATHER[gather], self.groups if self.groups > 1 else 0)
         arr = _i64_array(self.numel)
         ctx = _P()
         mi = master_init.contiguous()

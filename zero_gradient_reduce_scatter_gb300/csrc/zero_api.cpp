@@ -212,7 +212,10 @@ int check_hyper(const zero_hyper* h) {
 int grid_for(zero_ctx* c, int variant, int64_t work_items) {
     if (c->grid[variant] == 0) {
         int per_sm = 0;
-        if (zg::variant_blocks_per_sm(variant, c->cfg.M, &per_sm) != cudaSuccess || per_sm < 1) per_sm = 1;
+        if (zg::variant_blocks_per_sm(variant, c->cfg.M, c->cfg.groups > 1 ? c->cfg.groups : 1, &per_sm) !=
+                cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
         int g = per_sm * c->sm_count;
         if (g > zg::kMaxPartials) g = zg::kMaxPartials;
         c->grid[variant] = g;

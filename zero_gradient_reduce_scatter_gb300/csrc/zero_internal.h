@@ -115,8 +115,9 @@ int record_cuda_error(cudaError_t e);
 int variant_threads(int variant);
 int variant_ctas_per_sm_cap(int variant);
 
-// Largest number of CTAs of `variant` (for rank count M) resident on one SM.
-cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks);
+// Largest number of CTAs of `variant` (for rank count M, hybrid-sharding groups) resident
+// on one SM.
+cudaError_t variant_blocks_per_sm(int variant, int M, int groups, int* blocks);
 
 // Launchers: `grid` CTAs of variant_threads(variant) threads on `stream`.
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);

@@ -94,7 +94,8 @@ struct Cursor {
 };
 
 // ---------------------------------------------------------------------------------------
-// Reduce-scatter of one vec: acc[i] = sum over ranks (in order) of the bf16 values.
+// Reduce-scatter of one vec: acc[i] = sum over ranks (in order) of the bf16 values at
+// gradient index g (the lane, less the first lane of the gradient buffers).
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void add8(float acc[8], uint4 q) {
     acc[0] = __fadd_rn(acc[0], bf_lo(q.x));
@@ -111,9 +112,8 @@ __device__ __forceinline__ void add8(float acc[8], uint4 q) {
 // reduce-scatter inside the group), then the group sums in order (the all-reduce of the
 // shard across groups).
 template <int PATH>
-__device__ __noinline__ void rank_sum_grouped(const StepArgs& a, int64_t o, float acc[8]) {
+__device__ __forceinline__ void rank_sum_grouped(const StepArgs& a, int64_t g, float acc[8]) {
     const int K = a.M / a.groups;
-    const int64_t g = o - a.gbase;
     for (int grp = 0; grp < a.groups; ++grp) {
         float part[8];
 #pragma unroll
@@ -124,23 +124,22 @@ __device__ __noinline__ void rank_sum_grouped(const StepArgs& a, int64_t o, floa
     }
 }
 
-template <int MT, int PATH>
-__device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t o, float acc[8]) {
+// GROUPED selects the hybrid-sharding order at compile time, so the plain kernels carry no
+// branch that would keep the compiler from issuing the state loads beside the gradient loads.
+template <int MT, int PATH, bool GROUPED>
+__device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t g, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
-    if (a.groups > 1) {
-        rank_sum_grouped<PATH>(a, o, acc);
-        return;
-    }
-    if constexpr (MT > 0) {
+    if constexpr (GROUPED) {
+        rank_sum_grouped<PATH>(a, g, acc);
+    } else if constexpr (MT > 0) {
         uint4 q[MT];
 #pragma unroll
-        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(a.grads[r] + (o - a.gbase));
+        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(a.grads[r] + g);
 #pragma unroll
         for (int r = 0; r < MT; ++r) add8(acc, q[r]);
     } else {
         int r = 0;
-        const int64_t g = o - a.gbase;
         for (; r + 4 <= a.M; r += 4) {
             uint4 q0 = ld_grad<PATH>(a.grads[r] + g), q1 = ld_grad<PATH>(a.grads[r + 1] + g);
             uint4 q2 = ld_grad<PATH>(a.grads[r + 2] + g), q3 = ld_grad<PATH>(a.grads[r + 3] + g);
@@ -297,7 +296,7 @@ __device__ __forceinline__ double block_sum(double x) {
 // ---------------------------------------------------------------------------------------
 // K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool WRITE, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly>
+template <int MT, bool WRITE, bool GROUPED = false, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly>
 __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     SumSq acc;
     const int64_t stride = (int64_t)gridDim.x * THREADS;
@@ -309,7 +308,7 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
             const int64_t o = vi * 8;
             c.seek(o);
             float sum[8], gh[8];
-            rank_sum<MT, kGradLoadRsNorm>(a, o, sum);
+            rank_sum<MT, kGradLoadRsNorm, GROUPED>(a, o - a.gbase, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
             if (WRITE) {
                 st_f4(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
@@ -387,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
 // K4: fused reduce-scatter + AdamW + all-gather epilogue: the averaged gradient never
 // leaves registers. SCALE applies the clip scale computed by K2 (recompute form).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool SCALE>
+template <int MT, bool SCALE, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
     float s = 1.0f;
     if (SCALE) {
@@ -403,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
-        rank_sum<MT, kGradLoadRsAdamw>(a, o, sum);
+        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // full-layout gradients start at lane 0
         load_state(a, o, p, m, v);
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
@@ -541,7 +540,8 @@ __global__ void __launch_bounds__(kThreadsInit) k_save(const float* __restrict__
 // ---------------------------------------------------------------------------------------
 template <template <int> class F>
 struct ByM {
-    static auto get(int M) {
+    static auto get(int M, int groups = 1) {
+        if (groups > 1) return F<-1>::fn();  // hybrid sharding: the grouped, generic-M kernel
         switch (M) {
             case 1: return F<1>::fn();
             case 2: return F<2>::fn();
@@ -553,18 +553,27 @@ struct ByM {
     }
 };
 
-template <int MT> struct RsNormWrite { static auto fn() { return &k_rs_norm<MT, true>; } };
-template <int MT> struct RsNormOnly { static auto fn() { return &k_rs_norm<MT, false>; } };
-template <int MT> struct RsAdamwScaled { static auto fn() { return &k_rs_adamw<MT, true>; } };
-template <int MT> struct RsAdamwPlain { static auto fn() { return &k_rs_adamw<MT, false>; } };
+// MT = -1 stands for the grouped (hybrid-sharding) kernel with a runtime rank count.
+template <int MT> struct RsNormWrite {
+    static auto fn() { return MT < 0 ? &k_rs_norm<0, true, true> : &k_rs_norm<(MT < 0 ? 0 : MT), true>; }
+};
+template <int MT> struct RsNormOnly {
+    static auto fn() { return MT < 0 ? &k_rs_norm<0, false, true> : &k_rs_norm<(MT < 0 ? 0 : MT), false>; }
+};
+template <int MT> struct RsAdamwScaled {
+    static auto fn() { return MT < 0 ? &k_rs_adamw<0, true, true> : &k_rs_adamw<(MT < 0 ? 0 : MT), true>; }
+};
+template <int MT> struct RsAdamwPlain {
+    static auto fn() { return MT < 0 ? &k_rs_adamw<0, false, true> : &k_rs_adamw<(MT < 0 ? 0 : MT), false>; }
+};
 
-const void* variant_fn(int variant, int M) {
+const void* variant_fn(int variant, int M, int groups) {
     switch (variant) {
-        case kVarRsNormWrite: return (const void*)ByM<RsNormWrite>::get(M);
-        case kVarRsNormOnly: return (const void*)ByM<RsNormOnly>::get(M);
+        case kVarRsNormWrite: return (const void*)ByM<RsNormWrite>::get(M, groups);
+        case kVarRsNormOnly: return (const void*)ByM<RsNormOnly>::get(M, groups);
         case kVarAdamw: return (const void*)&k_adamw;
-        case kVarRsAdamwScaled: return (const void*)ByM<RsAdamwScaled>::get(M);
-        case kVarRsAdamwPlain: return (const void*)ByM<RsAdamwPlain>::get(M);
+        case kVarRsAdamwScaled: return (const void*)ByM<RsAdamwScaled>::get(M, groups);
+        case kVarRsAdamwPlain: return (const void*)ByM<RsAdamwPlain>::get(M, groups);
         case kVarGather: return (const void*)&k_gather;
         case kVarInit: return (const void*)&k_init;
         default: return nullptr;
@@ -597,8 +606,8 @@ int variant_ctas_per_sm_cap(int variant) {
     }
 }
 
-cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks) {
-    const void* fn = variant_fn(variant, M);
+cudaError_t variant_blocks_per_sm(int variant, int M, int groups, int* blocks) {
+    const void* fn = variant_fn(variant, M, groups);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, variant_threads(variant), 0);
     const int cap = variant_ctas_per_sm_cap(variant);
@@ -607,8 +616,8 @@ cudaError_t variant_blocks_per_sm(int variant, int M, int* blocks) {
 }
 
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
-    if (write_ghat) ByM<RsNormWrite>::get(a.M)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
-    else ByM<RsNormOnly>::get(a.M)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
+    if (write_ghat) ByM<RsNormWrite>::get(a.M, a.groups)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
+    else ByM<RsNormOnly>::get(a.M, a.groups)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -629,8 +638,8 @@ cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
-    if (apply_scale) ByM<RsAdamwScaled>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
-    else ByM<RsAdamwPlain>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    if (apply_scale) ByM<RsAdamwScaled>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    else ByM<RsAdamwPlain>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -57,7 +57,7 @@ int setup(int dev, int M, void** addr, int* grid_cap) {
     }
     if (!g_grid[dev][M]) {
         int per_sm = 0, sms = 0;
-        cudaError_t e = zg::variant_blocks_per_sm(zg::kVarRsNormOnly, M, &per_sm);
+        cudaError_t e = zg::variant_blocks_per_sm(zg::kVarRsNormOnly, M, 1, &per_sm);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail(e);
         int g = (per_sm < 1 ? 1 : per_sm) * sms;
