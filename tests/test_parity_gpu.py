@@ -239,6 +239,36 @@ def test_step_from_host_buffers_equals_device_step():
         assert torch.equal(a.master, b.master)
 
 
+def test_overlapped_host_steps_equal_device_steps():
+    """Four steps with different gradients, two alternating device buffer sets and no
+    synchronisation between calls: each step's parameters (copied to their own pinned host
+    buffer) equal those of the plain device path."""
+    w = W.small_variant(W.config(4), (300000, 77, 4099), steps=4)
+    dev = torch.device("cuda")
+    a = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    b = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    h, _ = make_hyper(w)
+    sig = W.sigmas(w)
+    sets = [a.new_grad_buffers(), a.new_grad_buffers()]
+    hosts, outs, refs = [], [], []
+    for k in range(w.steps):
+        grads = b.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, grads[r], b.tensor_offsets, sig)
+        b.step(grads, h)
+        refs.append(b.params().clone())
+        hosts.append([g.cpu().pin_memory() for g in grads])
+        outs.append(torch.empty(a.sizes["n"], dtype=torch.bfloat16).pin_memory())
+    torch.cuda.synchronize()
+    copy_stream = torch.cuda.Stream()
+    for k in range(w.steps):
+        a.step_host_overlapped(hosts[k], sets[k % 2], outs[k], h, copy_stream)
+    torch.cuda.synchronize()
+    for k in range(w.steps):
+        assert torch.equal(outs[k], refs[k].cpu()), k
+    assert torch.equal(a.master, b.master)
+
+
 def test_step_counter_and_resume():
     """K steps == K1 steps, save (state + t), restore into a fresh context, K2 steps."""
     w = W.small_variant(W.config(2), (30000, 5000), steps=4)

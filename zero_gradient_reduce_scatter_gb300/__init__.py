@@ -95,6 +95,7 @@ SIGNATURES = {
                                  _P, _P]),
     "zero_step": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_step_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P, _P]),
+    "zero_step_host_overlapped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P, _P, _P]),
     "zero_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
     "zero_apply": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_params": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
@@ -303,6 +304,24 @@ class ZeroOptimizer:
 
     def apply(self, hyper: Hyper, stream=None):
         _check(_lib().zero_apply(self._ctx, self.stage, ctypes.byref(hyper), _stream_handle(stream)), "zero_apply")
+
+    def step_host_overlapped(self, host_grads, dev_grads, host_params: torch.Tensor, hyper: Hyper,
+                             copy_stream, stream=None):
+        """step_host with the host-to-device copies on `copy_stream`, overlapping the previous
+        step's kernels and parameter copy when dev_grads alternates between two sets."""
+        for g in host_grads:
+            if g.is_cuda or g.dtype != torch.bfloat16 or g.numel() != self.sizes["npad"]:
+                raise ValueError("host_grads must be pinned host bf16 tensors of npad elements")
+        if host_params.is_cuda or host_params.numel() != self.sizes["n"]:
+            raise ValueError("host_params must be a pinned host bf16 tensor of n elements")
+        hp = (ctypes.c_void_p * self.M)(*[g.data_ptr() for g in host_grads])
+        dp = (ctypes.c_void_p * self.M)(*[g.data_ptr() for g in dev_grads])
+        for g in dev_grads:
+            if not (g.is_cuda and g.dtype == torch.bfloat16 and g.numel() == self.sizes["npad"]):
+                raise ValueError("dev_grads must be CUDA bf16 tensors of npad elements")
+        _check(_lib().zero_step_host_overlapped(self._ctx, ctypes.cast(hp, _P), ctypes.cast(dp, _P), self.stage,
+                                                ctypes.byref(hyper), host_params.data_ptr(), _stream_handle(stream),
+                                                int(copy_stream.cuda_stream)), "zero_step_host_overlapped")
 
     def gather_params(self, bucket: int = -1, dst: torch.Tensor | None = None, stream=None):
         _check(_lib().zero_gather(self._ctx, bucket, dst.data_ptr() if dst is not None else None,

@@ -51,6 +51,14 @@ struct zero_ctx {
     };
     std::vector<TimedLaunch> events;  // pool; the first `n_timed` are in use
     size_t n_timed;
+    // overlapped host steps: per device gradient set, "its last step has read it"
+    struct GradSet {
+        const void* key;        // dev_grads[0] of the set
+        cudaEvent_t consumed;
+        bool recorded;
+    };
+    std::vector<GradSet> grad_sets;
+    cudaEvent_t h2d_done = nullptr;
 };
 
 namespace {
@@ -585,6 +593,52 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
     return ZERO_OK;
 }
 
+int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
+                              const zero_hyper* h, void* host_params, void* stream, void* copy_stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!host_grads || !dev_grads || !host_params || copy_stream == stream) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < c->cfg.M; ++r)
+        if (!host_grads[r] || !dev_grads[r]) return ZERO_ERR_INVALID_ARG;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
+    cudaError_t e = cudaSuccess;
+    if (!c->h2d_done) {
+        e = cudaEventCreateWithFlags(&c->h2d_done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    zero_ctx::GradSet* set = nullptr;
+    for (auto& g : c->grad_sets)
+        if (g.key == dev_grads[0]) set = &g;
+    if (!set) {
+        if (c->grad_sets.size() >= 8) return ZERO_ERR_INVALID_ARG;  // a handful of buffer sets at most
+        zero_ctx::GradSet g{dev_grads[0], nullptr, false};
+        e = cudaEventCreateWithFlags(&g.consumed, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->grad_sets.push_back(g);
+        set = &c->grad_sets.back();
+    }
+    // the copy may overwrite this device set only after the last step that read it
+    if (set->recorded && (e = cudaStreamWaitEvent(cs, set->consumed, 0)) != cudaSuccess) return cuda_fail(e);
+    const size_t gbytes = (size_t)(2 * c->npad);
+    for (int r = 0; r < c->cfg.M; ++r) {
+        e = cudaMemcpyAsync(dev_grads[r], host_grads[r], gbytes, cudaMemcpyHostToDevice, cs);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(c->h2d_done, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(s, c->h2d_done, 0)) != cudaSuccess) return cuda_fail(e);
+    rc = zero_step(c, (const void* const*)dev_grads, stage, h, stream);
+    if (rc) return rc;
+    if ((e = cudaEventRecord(set->consumed, s)) != cudaSuccess) return cuda_fail(e);
+    set->recorded = true;
+    // on the kernels' stream: the next step's kernels rewrite the parameters after this copy
+    e = cudaMemcpyAsync(host_params, c->bufs.param_full, (size_t)(2 * c->n), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
 int zero_params(zero_ctx* c, void** full_bf16) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!full_bf16) return ZERO_ERR_INVALID_ARG;
@@ -748,6 +802,8 @@ int zero_destroy(zero_ctx* c) {
             cudaEventDestroy(tl.start);
             cudaEventDestroy(tl.stop);
         }
+        for (auto& g : c->grad_sets) cudaEventDestroy(g.consumed);
+        if (c->h2d_done) cudaEventDestroy(c->h2d_done);
     }
     delete c;
     return ZERO_OK;
