@@ -168,6 +168,15 @@ def alg_bytes_per_param(M: int) -> int:
     return 2 * M + 26
 
 
+def real_bytes_per_param(M: int, clip: bool, ghat_mode: str) -> int:
+    """Bytes the step actually moves per parameter: one fused pass without clipping; with
+    clipping either the gradients are read twice (4M + 26) or the fp32 average is written
+    and read back (2M + 34)."""
+    if not clip:
+        return 2 * M + 26
+    return 2 * M + 34 if ghat_mode == "materialize" else 4 * M + 26
+
+
 def kernel_alg_bytes_per_lane(kernel: str, M: int, write_ghat: bool) -> int:
     return {"rs_adamw": 2 * M + 26, "adamw": 4 + 26, "rs_norm": 2 * M + (4 if write_ghat else 0),
             "gather": 4, "norm_final": 0}[kernel]
@@ -368,6 +377,10 @@ def run_ours(args):
                        "parallelism": f"{world} independent emulated jobs (one per GPU)"},
             "gbs_alg": round(gbs_alg, 1), "alg_bytes_per_param": alg_bytes_per_param(w.M),
             "frac_of_peak_alg": round(gbs_alg / peak, 4),
+            "real_bytes_per_param": real_bytes_per_param(w.M, clip, ghat_mode),
+            "gbs_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9, 1),
+            "frac_of_peak_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9
+                                       / peak, 4),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
