@@ -275,7 +275,8 @@ int zero_get_step(zero_ctx* ctx, int64_t* t);
 int zero_set_step(zero_ctx* ctx, int64_t t);
 
 /* Per-kernel timing with CUDA events on the launching stream (off by default). When on,
- * every launch is bracketed by two events. zero_kernel_times waits for them and writes the
+ * every launch is bracketed by two events (up to 65,536 launches between two calls of
+ * zero_kernel_times; later ones run untimed). zero_kernel_times waits for them and writes the
  * summed milliseconds and launch counts of each ZERO_K_* kernel since the last call (each
  * array ZERO_NUM_KERNELS long; either may be NULL), then resets the sums. */
 int zero_set_timing(zero_ctx* ctx, int on);

@@ -6,6 +6,7 @@
 // Built with -ffp-contract=off so the step scalars are plain IEEE double operations.
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <algorithm>
 #include <cstring>
@@ -234,13 +235,16 @@ int grid_for(zero_ctx* c, int variant, int64_t work_items) {
     return (int)(need < c->grid[variant] ? need : c->grid[variant]);
 }
 
-// Event timing around one launch.
+// Event timing around one launch. At most kMaxTimedLaunches launches are recorded between two
+// zero_kernel_times calls; later launches run untimed.
+constexpr size_t kMaxTimedLaunches = 1 << 16;
+
 struct Timed {
     zero_ctx* c;
     cudaStream_t s;
-    zero_ctx::TimedLaunch* ev = nullptr;
+    size_t slot = SIZE_MAX;  // index into c->events (an index stays valid if the pool grows)
     Timed(zero_ctx* ctx, int kernel, cudaStream_t stream) : c(ctx), s(stream) {
-        if (!c->timing) return;
+        if (!c->timing || c->n_timed >= kMaxTimedLaunches) return;
         if (c->n_timed == c->events.size()) {
             zero_ctx::TimedLaunch tl{kernel, nullptr, nullptr};
             if (cudaEventCreate(&tl.start) != cudaSuccess) return;
@@ -250,12 +254,12 @@ struct Timed {
             }
             c->events.push_back(tl);
         }
-        ev = &c->events[c->n_timed++];
-        ev->kernel = kernel;
-        cudaEventRecord(ev->start, s);
+        slot = c->n_timed++;
+        c->events[slot].kernel = kernel;
+        cudaEventRecord(c->events[slot].start, s);
     }
     ~Timed() {
-        if (ev) cudaEventRecord(ev->stop, s);
+        if (slot != SIZE_MAX) cudaEventRecord(c->events[slot].stop, s);
     }
 };
 
