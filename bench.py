@@ -32,6 +32,7 @@ KERNEL_SRC = os.path.join(ROOT, "zero_gradient_reduce_scatter_gb300", "csrc", "z
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+MIB = 1024 * 1024
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -46,6 +47,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
+    ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
+                    help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
+                         "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+    ap.add_argument("--bucket-mib", type=float, default=25.0,
+                    help="bucket size for --mode gather when the workload has none")
     ap.add_argument("--max-params", type=int, default=0,
                     help="keep only the workload's leading tensors up to this many parameters (a small "
                          "case of the same kernels, for profiling); 0 = the whole workload")
@@ -414,10 +420,153 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _timed_region(fn, steps, stream, dist, device):
+    import torch
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist, device)
+    return max_over_ranks(dist, e0.elapsed_time(e1), device), clk
+
+
+def run_stream(args):
+    """ZeRO-2 per-bucket streaming: every bucket reduce-scattered (zero_reduce_bucket, in backward
+    order) from its own buffers, then one zero_apply; per step the same bytes as the
+    materialized clipped step, 2M + 34 per parameter."""
+    import torch
+
+    import workloads as W
+    import zero_gradient_reduce_scatter_gb300 as zg
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    args.config = 1 if args.config == 4 and "--config" not in sys.argv else args.config
+    w = workload(args)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
+                           ghat_buffer=True)
+    full = opt.new_grad_buffers()
+    sig = W.sigmas(w)
+    for r in range(w.M):
+        W.fill_grads(w, r, 0, full[r], opt.tensor_offsets, sig)
+    nb = len(opt.buckets)
+    slices = [[g[opt.buckets[b][0]:opt.buckets[b][0] + opt.bucket_lanes(b)] for g in full] for b in range(nb)]
+    h = zg.Hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 clip=w.clip is not None, max_grad_norm=w.clip or 1.0)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for b in reversed(range(nb)):
+            opt.reduce_bucket(b, slices[b])
+        opt.apply(h)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if opt.sync_status() != 0:
+        raise SystemExit("warm-up step failed")
+    opt.set_timing(True)
+    opt.kernel_times()
+    ms, clk = _timed_region(step, args.steps, stream, dist, device)
+    kt = opt.kernel_times()
+    n, lanes = w.N, opt.sizes["npad"]
+    peak, kind = hbm_peak()
+    ms_step = ms / args.steps
+    rs_ms = kt["rs_norm"][0] / args.steps
+    up_ms = kt["adamw"][0] / kt["adamw"][1]
+    dom = "adamw" if kt["adamw"][0] >= kt["rs_norm"][0] else "rs_norm"
+    dom_bytes, dom_ms = (30 * lanes, up_ms) if dom == "adamw" else ((2 * w.M + 4) * lanes, rs_ms)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC + " (ZeRO-2 per-bucket streaming)", "mode": "stream", "value": world * n * args.steps / (ms / 1e3),
+            "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
+                       "bucket_bytes": w.bucket_bytes, "clip": w.clip},
+            "gbs_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9, 1),
+            "frac_of_peak_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9 / peak, 4),
+            "real_bytes_per_param": 2 * w.M + 34,
+            "frac_of_peak_real": round((2 * w.M + 34) * n / (ms_step / 1e3) / 1e9 / peak, 4),
+            "roofline": {"bound": "hbm", "kernel": "adamw" if dom == "adamw" else "rs_norm_write (all buckets)",
+                         "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4), "traffic": None,
+                         "peak_source": kind, "kernel_share": {k: round(v[0] / ms, 4) for k, v in kt.items() if v[1]}},
+            "gpu_launches": int(sum(c for _, c in kt.values())), "clocks": clk}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_gather(args):
+    """ZeRO-3 per-module gather: every bucket's bf16 parameters all-gathered from the padded
+    shards into a transient buffer, the next bucket prefetched on a side stream; 4 bytes
+    per parameter (2 read, 2 written)."""
+    import dataclasses
+
+    import torch
+
+    import workloads as W
+    import zero_gradient_reduce_scatter_gb300 as zg
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    w = workload(args)
+    if w.bucket_bytes == 0:
+        w = dataclasses.replace(w, bucket_bytes=int(args.bucket_mib * MIB))
+    opt = zg.ZeroOptimizer(w.numel, w.M, 3, W.master_init(w, device), bucket_bytes=w.bucket_bytes, gather="shards")
+    nb = len(opt.buckets)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=device)
+    order = list(range(nb))
+
+    def sweep():
+        for _b, _params in opt.prefetched_buckets(order, stream=stream, side_stream=side):
+            pass
+
+    for _ in range(args.warmup):
+        sweep()
+    torch.cuda.synchronize()
+    opt.set_timing(True)
+    opt.kernel_times()
+    ms, clk = _timed_region(sweep, args.steps, stream, dist, device)
+    kt = opt.kernel_times()
+    n = w.N
+    peak, kind = hbm_peak()
+    g_ms, g_cnt = kt["gather"]
+    achieved = 4 * n * args.steps / (g_ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "params/s and achieved HBM GB/s of the ZeRO-3 per-bucket parameter all-gather", "mode": "gather",
+            "value": world * n * args.steps / (ms / 1e3), "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
+                       "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead"},
+            "roofline": {"bound": "hbm", "kernel": "gather", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": kind,
+                         "alg_bytes_per_param": 4, "avg_launch_ms": round(g_ms / max(g_cnt, 1), 4)},
+            "gpu_launches": int(g_cnt), "clocks": clk}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "stream":
+        run_stream(args)
+    elif args.mode == "gather":
+        run_gather(args)
     else:
         run_ours(args)
 

@@ -450,20 +450,43 @@ __device__ __forceinline__ uint4 splice(uint4 A, uint4 B, int k) {
 // 16-byte-aligned slot of 8 output elements (a0 = the output's misalignment in elements);
 // slots wholly inside the range whose source run lies in one bucket take one aligned
 // 16-byte store (the source run spliced from two aligned loads when it is unaligned);
-// edge slots go element by element.
+// edge slots go element by element. Each thread finds its first bucket once and then walks
+// forward (its indices only grow).
+struct UCursor {
+    const Bucket* tab;
+    int64_t nb, b;
+    Bucket e;
+    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t u) {
+        tab = t;
+        nb = n;
+        b = bucket_of_unpadded(t, n, u);
+        e = tab[b];
+    }
+    __device__ __forceinline__ void seek(int64_t u) {
+        while (u >= e.uoff + e.n && b + 1 < nb) {
+            ++b;
+            e = tab[b];
+        }
+    }
+};
+
 __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
                                                      uint16_t* __restrict__ out, const Bucket* tab, int64_t nb,
                                                      int64_t npad, int64_t u0, int64_t count) {
     const int64_t a0 = (int64_t)((reinterpret_cast<uintptr_t>(out) >> 1) & 7);
     const int64_t nslots = (count + a0 + 7) >> 3;
     const int64_t stride = (int64_t)gridDim.x * kThreadsGather;
-    for (int64_t w = (int64_t)blockIdx.x * kThreadsGather + threadIdx.x; w < nslots; w += stride) {
+    int64_t w = (int64_t)blockIdx.x * kThreadsGather + threadIdx.x;
+    if (w >= nslots) return;
+    UCursor c;
+    c.init(tab, nb, u0 + (w * 8 - a0 > 0 ? w * 8 - a0 : 0));
+    for (; w < nslots; w += stride) {
         const int64_t d0 = w * 8 - a0;  // first output element of the slot (may be < 0)
         if (d0 >= 0 && d0 + 8 <= count) {
             const int64_t u = u0 + d0;
-            const Bucket e = tab[bucket_of_unpadded(tab, nb, u)];
-            if (u + 8 <= e.uoff + e.n) {
-                const int64_t src = u - e.uoff + e.off;
+            c.seek(u);
+            if (u + 8 <= c.e.uoff + c.e.n) {
+                const int64_t src = u - c.e.uoff + c.e.off;
                 const int k = (int)(src & 7);
                 const uint16_t* base = shards + (src - k);
                 if (k == 0) {
@@ -480,8 +503,8 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
             const int64_t d = d0 + i;
             if (d < 0 || d >= count) continue;
             const int64_t uu = u0 + d;
-            const Bucket f = tab[bucket_of_unpadded(tab, nb, uu)];
-            out[d] = shards[uu - f.uoff + f.off];
+            c.seek(uu);
+            out[d] = shards[uu - c.e.uoff + c.e.off];
         }
     }
 }
