@@ -67,6 +67,8 @@ extern "C" {
 #define ZERO_ERR_NOT_COMPUTED  -8  /* the requested value was not computed (no clipping)  */
 #define ZERO_ERR_TOO_LARGE     -9  /* more buckets than zero_grad_norm_noalloc's fixed
                                       scratch holds (ZERO_NOALLOC_MAX_BUCKETS)            */
+#define ZERO_ERR_DEVICE       -10  /* checked build: a kernel rejected an out-of-bounds
+                                      index (and skipped the access); see zero_check_report */
 
 #define ZERO_ALIGN       64  /* shard length granule in lanes: 128 B of bf16, 256 B of fp32 */
 #define ZERO_MAX_RANKS   64  /* largest emulated rank count M                             */
@@ -253,8 +255,17 @@ int zero_get_state(zero_ctx* ctx, int which, int rank, void* dst, void* stream);
 int zero_last_norm(zero_ctx* ctx, double* norm, float* scale);
 
 /* Waits for the last step's stream and returns ZERO_OK, ZERO_ERR_NONFINITE (update
- * skipped), or ZERO_ERR_CUDA. */
+ * skipped), ZERO_ERR_DEVICE (checked build: a bounds check failed) or ZERO_ERR_CUDA. */
 int zero_sync_status(zero_ctx* ctx);
+
+/* Checked builds (compiled with -DZERO_CHECKED; zero_checked_build() returns 1) test every
+ * global index of every kernel against its buffer before the access, record the first
+ * failure and skip the access instead of trapping, so the context stays usable. This stands
+ * in for a memory checker. zero_check_report waits for the last step's stream and returns
+ * the first failing check site (0 = none) and the index it rejected; in normal builds the
+ * tests are compiled out and the site is always 0. */
+int zero_check_report(zero_ctx* ctx, int64_t* site, int64_t* index);
+int zero_checked_build(void);
 
 /* Checkpoint form of the optimizer state: the real lanes of fp32 master, m and v as unpadded
  * vectors of n values in tensor order. This form does not depend on the rank count, bucket

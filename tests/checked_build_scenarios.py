@@ -1,0 +1,117 @@
+"""Scenarios run against the bounds-checked library (libzero_gb300_checked.so).
+
+Executed in a child process by tests/test_checked_build_gpu.py: the library path is switched
+before the binding loads anything. Every scenario also runs its oracle comparison, and after
+each the device must report no failed bounds check. Exits non-zero on the first failure.
+"""
+import ctypes
+import os
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+sys.path.insert(0, HERE)
+
+from zero_gradient_reduce_scatter_gb300 import _build  # noqa: E402
+
+_build.LIB_PATH = _build.build(checked=True)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import oracle as O  # noqa: E402
+import workloads as W  # noqa: E402
+import zero_gradient_reduce_scatter_gb300 as zg  # noqa: E402
+from parity_util import bf16_ulp_diff, make_hyper, run_elementwise, u16  # noqa: E402
+
+
+def clean(opt, what):
+    assert opt.sync_status() == 0, f"{what}: status {opt.sync_status()}"
+    site, idx = opt.check_report()
+    assert site == 0, f"{what}: bounds check {site} failed at index {idx}"
+
+
+def exact(out, what):
+    assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0, what
+    clean(out["opt"], what)
+
+
+def main():
+    assert zg._lib().zero_checked_build() == 1, "not the checked library"
+    dev = torch.device("cuda")
+
+    w = W.small_variant(W.config(1), W.ragged_numel(60, 50, 4000, 11), bucket_bytes=9000, steps=2, clip=1.0)
+    for mode in ("materialize", "recompute"):
+        exact(run_elementwise(w, ghat_mode=mode, ghat_buffer=True), f"fused misaligned stores ({mode})")
+
+    w = W.small_variant(W.config(3), W.ragged_numel(40, 100, 6000, 3), bucket_bytes=15000, steps=2)
+    out = run_elementwise(w, gather="shards")
+    exact(out, "shards + gather")
+    opt = out["opt"]
+    full = opt.params()
+    for b in range(len(opt.buckets)):
+        u0, n = opt.bucket_range(b)
+        raw = torch.zeros(n + 8, dtype=torch.bfloat16, device=dev)
+        opt.gather_bucket(b, raw[3:3 + n])
+        torch.cuda.synchronize()
+        assert torch.equal(raw[3:3 + n].view(torch.int16), full[u0:u0 + n].view(torch.int16))
+    for _b, _p in opt.prefetched_buckets(list(range(len(opt.buckets)))):
+        pass
+    clean(opt, "per-bucket gathers")
+
+    for M in (3, 64):
+        exact(run_elementwise(W.small_variant(W.config(3), (3001, 17, 1), M=M, steps=2), gather="shards"),
+              f"generic M={M}")
+    exact(run_elementwise(W.small_variant(W.config(3), (3,), steps=2), gather="shards"), "3 lanes, 16 ranks")
+
+    wg = W.small_variant(W.config(3), W.ragged_numel(30, 200, 5000, 23), M=8, stage=3, steps=2)
+    exact(run_elementwise(wg, gather="shards", groups=2, ghat_mode="materialize", ghat_buffer=True), "hybrid")
+
+    # ZeRO-2 streaming against the oracle's monolithic step
+    ws = W.small_variant(W.config(1), (70000, 5000, 300, 70000), bucket_bytes=120000, steps=2, clip=1.0)
+    opt = zg.ZeroOptimizer(ws.numel, ws.M, ws.stage, W.master_init(ws, dev), bucket_bytes=ws.bucket_bytes,
+                           ghat_buffer=True)
+    p = O.plan(ws.numel, ws.M, ws.bucket_bytes)
+    st = O.init_state(p, ws.stage, W.master_init(ws, dev).cpu().numpy())
+    h, oh = make_hyper(ws)
+    for k in range(ws.steps):
+        g = opt.new_grad_buffers()
+        for r in range(ws.M):
+            W.fill_grads(ws, r, k, g[r], opt.tensor_offsets)
+        for b in reversed(range(len(opt.buckets))):
+            off = opt.buckets[b][0]
+            opt.reduce_bucket(b, [x[off:off + opt.bucket_lanes(b)].clone() for x in g])
+        opt.apply(h)
+        fullp, _, _, _ = O.zero_step(p, st, [u16(x) for x in g], oh)
+        assert bf16_ulp_diff(u16(opt.params()), fullp) <= 1, "streaming"
+    clean(opt, "streaming")
+
+    # save / reshard / load
+    saved = opt.save_state()
+    w2 = W.small_variant(ws, ws.numel, M=5, stage=3, bucket_bytes=0)
+    opt2 = zg.ZeroOptimizer(w2.numel, w2.M, w2.stage, W.master_init(w2, dev), gather="shards")
+    opt2.load_state(saved)
+    again = opt2.save_state()
+    torch.cuda.synchronize()
+    assert all(torch.equal(again[k], saved[k]) for k in ("master", "m", "v"))
+    clean(opt2, "save / load")
+
+    # the allocation-free norm
+    rows = []
+    for off, n, S, first in opt.buckets:
+        rows += [off, n, S, first]
+    table = (ctypes.c_int64 * len(rows))(*rows)
+    g = opt.new_grad_buffers()
+    for r in range(ws.M):
+        W.fill_grads(ws, r, 9, g[r], opt.tensor_offsets)
+    ptrs = (ctypes.c_void_p * ws.M)(*[x.data_ptr() for x in g])
+    no = torch.empty(1, dtype=torch.float64, device=dev)
+    so = torch.empty(1, dtype=torch.float32, device=dev)
+    rc = zg._lib().zero_grad_norm_noalloc(ctypes.cast(ptrs, ctypes.c_void_p), ws.M, ctypes.cast(table, ctypes.c_void_p),
+                                          len(opt.buckets), 1.0, no.data_ptr(), so.data_ptr(), None)
+    assert rc == 0 and float(no.item()) > 0
+    print("checked build: all scenarios clean")
+
+
+if __name__ == "__main__":
+    main()

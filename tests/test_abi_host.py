@@ -41,8 +41,12 @@ def test_library_exports_every_declared_function(zg):
     assert sorted(zg.SIGNATURES) == names
 
 
+def test_release_build_is_not_the_checked_build(zg):
+    assert zg._lib().zero_checked_build() == 0
+
+
 def test_error_strings(zg):
-    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -99]:
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -99]:
         assert zg._lib().zero_strerror(code)
 
 

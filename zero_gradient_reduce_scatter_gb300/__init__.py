@@ -34,7 +34,7 @@ ZERO_OK = 0
 ERRORS = {
     -1: "ZERO_ERR_INVALID_ARG", -2: "ZERO_ERR_MISALIGNED", -3: "ZERO_ERR_SIZE_MISMATCH",
     -4: "ZERO_ERR_STAGE", -5: "ZERO_ERR_NONFINITE", -6: "ZERO_ERR_CUDA", -7: "ZERO_ERR_BAD_CONTEXT",
-    -8: "ZERO_ERR_NOT_COMPUTED", -9: "ZERO_ERR_TOO_LARGE",
+    -8: "ZERO_ERR_NOT_COMPUTED", -9: "ZERO_ERR_TOO_LARGE", -10: "ZERO_ERR_DEVICE",
 }
 ZERO_ERR_NONFINITE = -5
 ZERO_ERR_NOT_COMPUTED = -8
@@ -107,6 +107,8 @@ SIGNATURES = {
     "zero_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P, _P]),
     "zero_last_norm": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]),
     "zero_sync_status": (ctypes.c_int, [_P]),
+    "zero_check_report": (ctypes.c_int, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "zero_checked_build": (ctypes.c_int, []),
     "zero_get_step": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
     "zero_set_step": (ctypes.c_int, [_P, _I64]),
     "zero_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -444,6 +446,12 @@ class ZeroOptimizer:
         if rc not in (ZERO_OK, ZERO_ERR_NONFINITE):
             _check(rc, "zero_sync_status")
         return rc
+
+    def check_report(self):
+        """(site, index) of the first failed bounds check of a checked build; site 0 = none."""
+        site, idx = _I64(), _I64()
+        _check(_lib().zero_check_report(self._ctx, ctypes.byref(site), ctypes.byref(idx)), "zero_check_report")
+        return site.value, idx.value
 
     @property
     def t(self) -> int:

@@ -18,6 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libzero_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# The bounds-checked variant (every kernel index tested before use; for tests).
+CHECKED_LIB_PATH = os.path.join(BUILD_DIR, "libzero_gb300_checked.so")
 
 SOURCES = ["zero_kernels.cu", "zero_api.cpp", "zero_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,24 +42,29 @@ def _inputs():
     return files
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build libzero_gb300.so if missing or older than its sources; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Build libzero_gb300.so (or, with checked=True, the bounds-checked
+    libzero_gb300_checked.so) if missing or older than its sources; returns its path."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and not is_stale(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    obj_dir = os.path.join(BUILD_DIR, "checked" if checked else "release")
+    os.makedirs(obj_dir, exist_ok=True)
     common = ["-std=c++17", "-O3", "-lineinfo", "-I", INCLUDE, "-I", CSRC,
               "-Xcompiler", "-fPIC,-ffp-contract=off,-fno-fast-math,-Wall"]
+    if checked:
+        common.append("-DZERO_CHECKED")
     procs, objs = [], []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *common, "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
             cmd = [nvcc, *common, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
@@ -71,11 +78,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {src}:\n{out}")
         if verbose and out.strip():
             print(out)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
             "-Xlinker", f"-rpath,{_cuda_lib_dir(nvcc)}"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path

@@ -279,6 +279,9 @@ zg::StepArgs base_args(zero_ctx* c) {
     a.vbeg = 0;
     a.vend = a.nvec;
     a.gbase = 0;
+    a.gext = c->npad;
+    a.npad = c->npad;
+    a.n = c->n;
     a.M = c->cfg.M;
     a.inv_M = (float)(1.0 / (double)c->cfg.M);
     a.groups = c->cfg.groups > 1 ? c->cfg.groups : 1;
@@ -292,7 +295,7 @@ int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStre
     const int grid = grid_for(c, zg::kVarGather, count / 8 + 2);
     Timed tm(c, ZERO_K_GATHER, s);
     cudaError_t e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, out, c->dev_buckets,
-                                      (int64_t)c->buckets.size(), c->npad, u0, count, grid, s);
+                                      (int64_t)c->buckets.size(), c->npad, u0, count, c->status, grid, s);
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
@@ -396,7 +399,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
         Timed tm(c, ZERO_K_INIT, s);
         e = zg::launch_init((const float*)master_init, nullptr, nullptr, (float*)c->bufs.master, (float*)c->bufs.m,
                             (float*)c->bufs.v, (uint16_t*)c->bufs.param_full, (uint16_t*)c->bufs.param_shards,
-                            c->dev_buckets, (int64_t)c->buckets.size(), c->npad, grid, s);
+                            c->dev_buckets, (int64_t)c->buckets.size(), c->npad, c->n, c->status, grid, s);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // host tables above must outlive the copies
     if (e != cudaSuccess) {
@@ -493,6 +496,7 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     a.vbeg = e.off / 8;
     a.vend = e.end / 8;
     a.gbase = e.off;
+    a.gext = e.end - e.off;
     const int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
     cudaError_t err;
     {
@@ -576,7 +580,7 @@ int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
     const int grid = grid_for(c, zg::kVarInit, c->npad);
     cudaError_t e = zg::launch_save((const float*)c->bufs.master, (const float*)c->bufs.m, (const float*)c->bufs.v,
                                     (float*)master, (float*)m, (float*)v, c->dev_buckets,
-                                    (int64_t)c->buckets.size(), c->npad, grid, s);
+                                    (int64_t)c->buckets.size(), c->npad, c->n, c->status, grid, s);
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
@@ -591,7 +595,7 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
     cudaError_t e = zg::launch_init((const float*)master, (const float*)m, (const float*)v, (float*)c->bufs.master,
                                     (float*)c->bufs.m, (float*)c->bufs.v, (uint16_t*)c->bufs.param_full,
                                     (uint16_t*)c->bufs.param_shards, c->dev_buckets, (int64_t)c->buckets.size(),
-                                    c->npad, grid, s);
+                                    c->npad, c->n, c->status, grid, s);
     if (e != cudaSuccess) return cuda_fail(e);
     c->t = t;
     return ZERO_OK;
@@ -737,8 +741,28 @@ int zero_sync_status(zero_ctx* c) {
     zg::Status st;
     int rc = read_status(c, &st);
     if (rc) return rc;
+    if (st.flags & zg::kFlagBounds) return ZERO_ERR_DEVICE;
     if (c->stepped && c->last_clip && (st.flags & zg::kFlagNonfinite)) return ZERO_ERR_NONFINITE;
     return ZERO_OK;
+}
+
+int zero_check_report(zero_ctx* c, int64_t* site, int64_t* index) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!site || !index) return ZERO_ERR_INVALID_ARG;
+    zg::Status st;
+    int rc = read_status(c, &st);
+    if (rc) return rc;
+    *site = st.bad_site;
+    *index = st.bad_index;
+    return ZERO_OK;
+}
+
+int zero_checked_build(void) {
+#ifdef ZERO_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 int zero_get_step(zero_ctx* c, int64_t* t) {
@@ -825,6 +849,7 @@ const char* zero_strerror(int status) {
         case ZERO_ERR_BAD_CONTEXT: return "null, destroyed or unknown context";
         case ZERO_ERR_NOT_COMPUTED: return "value not computed by the last step";
         case ZERO_ERR_TOO_LARGE: return "layout exceeds the fixed scratch of zero_grad_norm_noalloc";
+        case ZERO_ERR_DEVICE: return "a device-side bounds check failed (checked build); see zero_check_report";
         default: return "unknown status";
     }
 }

@@ -26,12 +26,15 @@ struct Status {
     double sumsq;   // sum of squared averaged gradient over real lanes
     double norm;    // sqrt(sumsq)
     float scale;    // clip scale applied to the averaged gradient
-    int32_t flags;  // kFlagNonfinite
-    int64_t reserved[13];
+    int32_t flags;  // kFlagNonfinite | kFlagBounds
+    int64_t bad_site;   // checked builds: first failing bounds check (0 = none) ...
+    int64_t bad_index;  // ... and the index it rejected
+    int64_t reserved[11];
 };
 static_assert(sizeof(Status) == 128, "status word is 128 bytes");
 
 constexpr int32_t kFlagNonfinite = 1;
+constexpr int32_t kFlagBounds = 4;  // checked builds: an index failed its bounds check (sticky)
 
 // Step constants of AdamW, formed on the host in double and rounded once to float.
 struct AdamConsts {
@@ -51,6 +54,9 @@ struct StepArgs {
     int64_t nvec;         // npad / 8: work items of 8 lanes (16 B of bf16)
     int64_t vbeg, vend;   // vec range of the norm pass (the whole layout, or one bucket)
     int64_t gbase;        // lane at which grads[r] starts (0, or the bucket's first lane)
+    int64_t gext;         // lanes in each gradient buffer (bounds checks)
+    int64_t npad;         // padded lanes (bounds checks)
+    int64_t n;            // unpadded parameters (bounds checks)
     int32_t M;
     float inv_M;          // (float)(1.0 / M)
     int32_t out_shards;   // 1: `out` is the padded shard buffer; 0: the unpadded full buffer
@@ -130,14 +136,15 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaS
 // out[d] = bf16 parameter of unpadded index u0 + d, d < count, from the padded shards
 // (out needs only 2-byte alignment).
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb,
-                          int64_t npad, int64_t u0, int64_t count, int grid, cudaStream_t s);
+                          int64_t npad, int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s);
 // State from unpadded fp32 vectors (m_init / v_init may be null: zeros), plus bf16 copies.
 cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init,
                         float* master, float* m, float* v, uint16_t* full, uint16_t* shards,
-                        const Bucket* buckets, int64_t nb, int64_t npad, int grid, cudaStream_t s);
+                        const Bucket* buckets, int64_t nb, int64_t npad, int64_t n, Status* st, int grid,
+                        cudaStream_t s);
 // Real lanes of master / m / v into unpadded vectors (any output may be null).
 cudaError_t launch_save(const float* master, const float* m, const float* v, float* out_master,
                         float* out_m, float* out_v, const Bucket* buckets, int64_t nb, int64_t npad,
-                        int grid, cudaStream_t s);
+                        int64_t n, Status* st, int grid, cudaStream_t s);
 
 }  // namespace zg

@@ -23,6 +23,29 @@ namespace zg {
 namespace {
 
 // ---------------------------------------------------------------------------------------
+// Checked builds (-DZERO_CHECKED): before each global access group the kernels test the
+// index against the bounds of its buffer; a failing test records (site, index) in the
+// status word, raises kFlagBounds and skips the access -- no trap, the context stays usable.
+// Normal builds compile the tests to `true`, i.e. to nothing.
+// ---------------------------------------------------------------------------------------
+#ifdef ZERO_CHECKED
+__device__ __noinline__ bool zg_bounds_fail(Status* st, int site, int64_t idx) {
+    if (atomicCAS(reinterpret_cast<unsigned long long*>(&st->bad_site), 0ull, (unsigned long long)site) == 0ull)
+        st->bad_index = idx;
+    atomicOr(&st->flags, kFlagBounds);
+    return false;
+}
+#define ZG_OK(st, cond, site, idx) ((cond) ? true : zg_bounds_fail((st), (site), (int64_t)(idx)))
+#else
+#define ZG_OK(st, cond, site, idx) true
+#endif
+// check sites
+enum : int {
+    kSiteGradNorm = 1, kSiteGhatWrite, kSitePartial, kSiteStepLanes, kSiteParamFull, kSiteGhatRead,
+    kSiteGatherSrc, kSiteGatherOut, kSiteInit, kSiteSave, kSiteFinalCount
+};
+
+// ---------------------------------------------------------------------------------------
 // bf16 helpers: bf16 is the upper half of a binary32, so widening is a shift.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -220,6 +243,7 @@ __device__ __forceinline__ void store_params(const StepArgs& a, const Cursor& c,
     }
     if (nreal <= 0) return;
     const int64_t u0 = o - c.e.off + c.e.uoff;
+    if (!ZG_OK(a.status, u0 >= 0 && u0 + nreal <= a.n, kSiteParamFull, u0)) return;
     uint16_t* dst = a.out + u0;
     if (nreal == 8) {
         const int al = (int)(u0 & 7);
@@ -308,9 +332,10 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
             const int64_t o = vi * 8;
             c.seek(o);
             float sum[8], gh[8];
+            if (!ZG_OK(a.status, o - a.gbase >= 0 && o - a.gbase + 8 <= a.gext, kSiteGradNorm, o)) continue;
             rank_sum<MT, kGradLoadRsNorm, GROUPED>(a, o - a.gbase, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
-            if (WRITE) {
+            if (WRITE && ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatWrite, o)) {
                 st_f4(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
                 st_f4(a.ghat + o + 4, make_float4(gh[4], gh[5], gh[6], gh[7]));
             }
@@ -318,7 +343,7 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
         }
     }
     const double t = block_sum<THREADS>(acc.value());
-    if (threadIdx.x == 0) a.partials[blockIdx.x] = t;
+    if (threadIdx.x == 0 && ZG_OK(a.status, blockIdx.x < kMaxPartials, kSitePartial, blockIdx.x)) a.partials[blockIdx.x] = t;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -341,13 +366,14 @@ __device__ __forceinline__ double cta_sum_partials(const double* partials, int n
 
 __global__ void __launch_bounds__(kThreads) k_norm_final(Status* st, const double* partials, int nparts,
                                                          double max_norm, int clip) {
+    if (!ZG_OK(st, nparts <= kMaxPartials, kSiteFinalCount, nparts)) return;
     const double sumsq = cta_sum_partials(partials, nparts);
     if (threadIdx.x == 0) {
         const double norm = sqrt(sumsq);
         const bool finite = isfinite(norm);
         st->sumsq = sumsq;
         st->norm = norm;
-        st->flags = (clip && !finite) ? kFlagNonfinite : 0;
+        st->flags = (st->flags & kFlagBounds) | ((clip && !finite) ? kFlagNonfinite : 0);
         st->scale = (clip && finite && norm > max_norm) ? (float)(max_norm / norm) : 1.0f;
     }
 }
@@ -373,6 +399,7 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
         const int64_t o = vi * 8;
         c.seek(o);
         float gh[8], p[8], m[8], v[8];
+        if (!ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatRead, o)) continue;
         const float4 g0 = ld_f4(a.ghat + o), g1 = ld_f4(a.ghat + o + 4);
         load_state(a, o, p, m, v);
         unpack(g0, g1, gh);
@@ -402,6 +429,7 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
+        if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
         rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // full-layout gradients start at lane 0
         load_state(a, o, p, m, v);
         const int nr = c.nreal(o);
@@ -472,7 +500,7 @@ struct UCursor {
 
 __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
                                                      uint16_t* __restrict__ out, const Bucket* tab, int64_t nb,
-                                                     int64_t npad, int64_t u0, int64_t count) {
+                                                     int64_t npad, int64_t u0, int64_t count, Status* st) {
     const int64_t a0 = (int64_t)((reinterpret_cast<uintptr_t>(out) >> 1) & 7);
     const int64_t nslots = (count + a0 + 7) >> 3;
     const int64_t stride = (int64_t)gridDim.x * kThreadsGather;
@@ -489,6 +517,7 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
                 const int64_t src = u - c.e.uoff + c.e.off;
                 const int k = (int)(src & 7);
                 const uint16_t* base = shards + (src - k);
+                if (!ZG_OK(st, src >= 0 && src + 8 <= npad, kSiteGatherSrc, src)) continue;
                 if (k == 0) {
                     st_u4(out + d0, ld_u4(base));
                     continue;
@@ -504,7 +533,9 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
             if (d < 0 || d >= count) continue;
             const int64_t uu = u0 + d;
             c.seek(uu);
-            out[d] = shards[uu - c.e.uoff + c.e.off];
+            const int64_t lane = uu - c.e.uoff + c.e.off;
+            if (!ZG_OK(st, lane >= 0 && lane < npad && uu - c.e.uoff < c.e.n, kSiteGatherSrc, lane)) continue;
+            out[d] = shards[lane];
         }
     }
 }
@@ -517,7 +548,7 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
 __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__ init, const float* __restrict__ m_init,
                                                    const float* __restrict__ v_init, float* master, float* m,
                                                    float* v, uint16_t* full, uint16_t* shards, const Bucket* tab,
-                                                   int64_t nb, int64_t npad) {
+                                                   int64_t nb, int64_t npad, int64_t n, Status* st) {
     const int64_t stride = (int64_t)gridDim.x * kThreadsInit;
     int64_t o = (int64_t)blockIdx.x * kThreadsInit + threadIdx.x;
     if (o >= npad) return;
@@ -527,6 +558,7 @@ __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__
         c.seek(o);
         const bool real = o < c.e.off + c.e.n;
         const int64_t u = o - c.e.off + c.e.uoff;
+        if (!ZG_OK(st, !real || (u >= 0 && u < n), kSiteInit, u)) continue;
         const float x = real ? init[u] : 0.0f;
         master[o] = x;
         m[o] = (real && m_init) ? m_init[u] : 0.0f;
@@ -541,7 +573,8 @@ __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__
 // independent form a checkpoint keeps, loadable under any rank count or bucket size).
 __global__ void __launch_bounds__(kThreadsInit) k_save(const float* __restrict__ master, const float* __restrict__ m,
                                                    const float* __restrict__ v, float* out_master, float* out_m,
-                                                   float* out_v, const Bucket* tab, int64_t nb, int64_t npad) {
+                                                   float* out_v, const Bucket* tab, int64_t nb, int64_t npad,
+                                                   int64_t n, Status* st) {
     const int64_t stride = (int64_t)gridDim.x * kThreadsInit;
     int64_t o = (int64_t)blockIdx.x * kThreadsInit + threadIdx.x;
     if (o >= npad) return;
@@ -551,6 +584,7 @@ __global__ void __launch_bounds__(kThreadsInit) k_save(const float* __restrict__
         c.seek(o);
         if (o >= c.e.off + c.e.n) continue;
         const int64_t u = o - c.e.off + c.e.uoff;
+        if (!ZG_OK(st, u >= 0 && u < n, kSiteSave, u)) continue;
         if (out_master) out_master[u] = master[o];
         if (out_m) out_m[u] = m[o];
         if (out_v) out_v[u] = v[o];
@@ -667,24 +701,26 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaS
 }
 
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb, int64_t npad,
-                          int64_t u0, int64_t count, int grid, cudaStream_t s) {
+                          int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s) {
     if (count <= 0) return cudaSuccess;
-    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count);
+    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init, float* master, float* m,
                         float* v, uint16_t* full, uint16_t* shards, const Bucket* buckets, int64_t nb, int64_t npad,
-                        int grid, cudaStream_t s) {
+                        int64_t n, Status* st, int grid, cudaStream_t s) {
     if (npad <= 0) return cudaSuccess;
-    k_init<<<grid, kThreadsInit, 0, s>>>(master_init, m_init, v_init, master, m, v, full, shards, buckets, nb, npad);
+    k_init<<<grid, kThreadsInit, 0, s>>>(master_init, m_init, v_init, master, m, v, full, shards, buckets, nb, npad, n,
+                                         st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_save(const float* master, const float* m, const float* v, float* out_master, float* out_m,
-                        float* out_v, const Bucket* buckets, int64_t nb, int64_t npad, int grid, cudaStream_t s) {
+                        float* out_v, const Bucket* buckets, int64_t nb, int64_t npad, int64_t n, Status* st, int grid,
+                        cudaStream_t s) {
     if (npad <= 0) return cudaSuccess;
-    k_save<<<grid, kThreadsInit, 0, s>>>(master, m, v, out_master, out_m, out_v, buckets, nb, npad);
+    k_save<<<grid, kThreadsInit, 0, s>>>(master, m, v, out_master, out_m, out_v, buckets, nb, npad, n, st);
     return cudaGetLastError();
 }
 

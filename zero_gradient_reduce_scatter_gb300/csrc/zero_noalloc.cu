@@ -152,6 +152,9 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     a.vbeg = 0;
     a.vend = a.nvec;
     a.gbase = 0;
+    a.gext = npad;
+    a.npad = npad;
+    a.n = uoff;
     a.M = M;
     a.inv_M = (float)(1.0 / (double)M);
     a.groups = 1;
