@@ -296,6 +296,11 @@ int zero_kernel_times(zero_ctx* ctx, double* ms, int64_t* launches);
 /* Launch configuration of the streaming kernels: CTAs in the grid and threads per CTA. */
 int zero_launch_shape(zero_ctx* ctx, int* ctas, int* threads);
 
+/* Caps the grid of every streaming kernel at `ctas` CTAs (0 = no cap, the default: as many
+ * as the GPU holds). Results do not depend on the grid except the norm's summation order;
+ * small and odd grids exist to test the index arithmetic. */
+int zero_set_max_ctas(zero_ctx* ctx, int ctas);
+
 /* Releases the context (not the caller's buffers). Waits for nothing. */
 int zero_destroy(zero_ctx* ctx);
 

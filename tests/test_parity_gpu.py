@@ -379,3 +379,42 @@ def test_hybrid_sharding_matches_oracle(G, K, stage, gather, bucket_bytes, clip)
     for mode in (("materialize", "recompute") if clip else ("auto",)):
         out = run_elementwise(w, gather=gather, groups=G, ghat_mode=mode, ghat_buffer=True)
         assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
+
+
+# ------------------------------------------------------------------------------------------
+# Odd grids: the grid-stride loops and bucket cursors must not depend on the grid
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("clip", [None, 1e-3])
+def test_results_do_not_depend_on_the_grid(clip):
+    w = W.small_variant(W.config(1), ragged(50, 100, 30000, 29), bucket_bytes=60000, steps=2, clip=clip)
+    dev = torch.device("cuda")
+    sig = W.sigmas(w)
+    grads_per_step = []
+    ref = None
+    for cap in (0, 1, 7, 13, 151):
+        for gather in ("fused", "shards"):
+            stage = 3 if gather == "shards" else 2
+            opt = zg.ZeroOptimizer(w.numel, w.M, stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
+                                   gather=gather, ghat_buffer=True)
+            opt.set_max_ctas(cap)
+            h, _ = make_hyper(w)
+            for k in range(w.steps):
+                if len(grads_per_step) <= k:
+                    g = opt.new_grad_buffers()
+                    for r in range(w.M):
+                        W.fill_grads(w, r, k, g[r], opt.tensor_offsets, sig)
+                    grads_per_step.append(g)
+                opt.step(grads_per_step[k], h)
+            assert opt.sync_status() == 0
+            got = (f32(opt.master), f32(opt.m), f32(opt.v), u16(opt.params()))
+            if ref is None:
+                ref = got
+                continue
+            if clip is None:  # nothing depends on the grid
+                for a, b in zip(got, ref):
+                    assert np.array_equal(a.view(np.uint32 if a.dtype == np.float32 else np.uint16),
+                                          b.view(np.uint32 if b.dtype == np.float32 else np.uint16)), (cap, gather)
+            else:  # only the norm's summation order does
+                for a, b in zip(got[:3], ref[:3]):
+                    assert state_errors(a, b) <= 1.0, (cap, gather)
+                assert bf16_ulp_diff(got[3], ref[3]) <= 1

@@ -114,6 +114,7 @@ SIGNATURES = {
     "zero_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "zero_kernel_times": (ctypes.c_int, [_P, _P, _P]),
     "zero_launch_shape": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "zero_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
     "zero_destroy": (ctypes.c_int, [_P]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "zero_last_cuda_error": (ctypes.c_int, []),
@@ -477,6 +478,10 @@ class ZeroOptimizer:
         ctas, thr = ctypes.c_int(), ctypes.c_int()
         _check(_lib().zero_launch_shape(self._ctx, ctypes.byref(ctas), ctypes.byref(thr)), "zero_launch_shape")
         return ctas.value, thr.value
+
+    def set_max_ctas(self, ctas: int):
+        """Cap the grid of the streaming kernels (0 = none); for testing index arithmetic."""
+        _check(_lib().zero_set_max_ctas(self._ctx, int(ctas)), "zero_set_max_ctas")
 
     def close(self):
         if getattr(self, "_ctx", None) is not None and self._ctx.value:

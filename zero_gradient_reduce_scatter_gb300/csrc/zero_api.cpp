@@ -42,8 +42,9 @@ struct zero_ctx {
     // per-bucket streaming (zero_reduce_bucket / zero_apply)
     double* bucket_sums;          // device: one fp64 sum of squares per bucket
     std::vector<char> reduced;    // host: buckets reduced since the last zero_apply
-    // launch shapes, per kernel variant (0 = not computed yet)
+    // launch shapes, per kernel variant (0 = not computed yet), and an optional cap
     int grid[zg::kNumVariants];
+    int max_ctas;
     // timing
     int timing;
     struct TimedLaunch {
@@ -232,7 +233,9 @@ int grid_for(zero_ctx* c, int variant, int64_t work_items) {
     const int threads = zg::variant_threads(variant);
     int64_t need = (work_items + threads - 1) / threads;
     if (need < 1) need = 1;
-    return (int)(need < c->grid[variant] ? need : c->grid[variant]);
+    int g = c->grid[variant];
+    if (c->max_ctas > 0 && c->max_ctas < g) g = c->max_ctas;
+    return (int)(need < g ? need : g);
 }
 
 // Event timing around one launch. At most kMaxTimedLaunches launches are recorded between two
@@ -382,6 +385,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->last_stream = (cudaStream_t)stream;
     c->stepped = 0;
     std::memset(c->grid, 0, sizeof c->grid);
+    c->max_ctas = 0;
     c->timing = 0;
     c->n_timed = 0;
 
@@ -808,6 +812,13 @@ int zero_kernel_times(zero_ctx* c, double* ms, int64_t* launches) {
         if (ms) ms[k] = acc[k];
         if (launches) launches[k] = cnt[k];
     }
+    return ZERO_OK;
+}
+
+int zero_set_max_ctas(zero_ctx* c, int ctas) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (ctas < 0) return ZERO_ERR_INVALID_ARG;
+    c->max_ctas = ctas;
     return ZERO_OK;
 }
 
