@@ -25,8 +25,9 @@
  *    the context only borrows the pointers. The context owns host tables, CUDA events for
  *    optional kernel timing, and nothing else.
  *  - Streams: work is enqueued on the caller's stream (a cudaStream_t passed as void*; NULL
- *    is the legacy default stream). Calls return once the work is enqueued; only
- *    zero_last_norm(), zero_sync_status() and zero_kernel_times() wait for the stream.
+ *    is the legacy default stream). Calls return once the work is enqueued; only zero_init,
+ *    zero_last_norm(), zero_sync_status(), zero_check_report() and zero_kernel_times() wait
+ *    for the stream.
  *  - Device: the context binds to the device that holds its buffers; calls make it current
  *    for their duration and restore the caller's current device.
  *  - Threads: a context must not be used from two threads at once. Different contexts are
@@ -174,8 +175,10 @@ int zero_plan_layout(const zero_config* cfg, const int64_t* numel, int64_t n_ten
 /* Creates a context over the caller's buffers and initialises the state on `stream`:
  * master = master_init scattered into the padded layout (padding 0), m = v = 0, t = 0,
  * param_full = bf16(master_init) (and param_shards = bf16(master) with ZERO_GATHER_SHARDS).
- * master_init: device fp32 [n], unpadded, read during this call's kernels only.
- * Errors: INVALID_ARG, STAGE, MISALIGNED, SIZE_MISMATCH, CUDA. On error *out is NULL. */
+ * master_init: device fp32 [n], unpadded, read during this call's kernels only. Unlike the
+ * step calls, zero_init waits for `stream` before returning (its host-side bucket table must
+ * outlive the upload). Errors: INVALID_ARG, STAGE, MISALIGNED, SIZE_MISMATCH, CUDA. On error
+ * *out is NULL. */
 int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
               const zero_buffers* bufs, const void* master_init, void* stream);
 
