@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
                     help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
                          "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+    ap.add_argument("--groups", type=int, default=1,
+                    help="hybrid sharding: split the workload's M ranks into this many groups (state "
+                         "sharded over M / groups ranks, replicated across groups)")
     ap.add_argument("--bucket-mib", type=float, default=25.0,
                     help="bucket size for --mode gather when the workload has none")
     ap.add_argument("--max-params", type=int, default=0,
@@ -276,7 +279,7 @@ def run_ours(args):
     w = workload(args)
     gather = "fused"
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
-                           gather=gather)
+                           gather=gather, groups=args.groups)
     sig = W.sigmas(w)
     grads = opt.new_grad_buffers()
     for r in range(w.M):
@@ -375,7 +378,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "params": n, "M": w.M, "stage": w.stage,
+            "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
+                                             if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage,
                        "clip": w.clip, "bucket_bytes": w.bucket_bytes, "gather": gather, "ghat_mode": ghat_mode,
                        "padded_lanes": lanes,
                        "l2": f"inputs {(opt.sizes['bytes_grad_each'] * w.M + 12 * lanes) / 1e9:.1f} GB > L2 "
@@ -489,7 +493,8 @@ def run_stream(args):
             "metric": METRIC + " (ZeRO-2 per-bucket streaming)", "mode": "stream", "value": world * n * args.steps / (ms / 1e3),
             "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
+            "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
+                                             if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
                        "bucket_bytes": w.bucket_bytes, "clip": w.clip},
             "gbs_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9, 1),
             "frac_of_peak_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9 / peak, 4),

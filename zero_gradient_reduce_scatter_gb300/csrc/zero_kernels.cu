@@ -133,17 +133,67 @@ __device__ __forceinline__ void add8(float acc[8], uint4 q) {
 
 // Hybrid sharding: rank q = grp * K + k; each group's K values summed in order (the
 // reduce-scatter inside the group), then the group sums in order (the all-reduce of the
-// shard across groups).
+// shard across groups). The ranks are loaded four at a time across group boundaries, so
+// small groups do not serialise the load latency; a group's partial sum (from +0) is added
+// to the total when its last rank has been added.
 template <int PATH>
 __device__ __forceinline__ void rank_sum_grouped(const StepArgs& a, int64_t g, float acc[8]) {
     const int K = a.M / a.groups;
-    for (int grp = 0; grp < a.groups; ++grp) {
-        float part[8];
+    float part[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i] = 0.0f;
-        for (int k = 0; k < K; ++k) add8(part, ld_grad<PATH>(a.grads[grp * K + k] + g));
+    for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+    int kin = 0;
+    auto take = [&](uint4 q) {
+        add8(part, q);
+        if (++kin == K) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], part[i]);
+            for (int i = 0; i < 8; ++i) {
+                acc[i] = __fadd_rn(acc[i], part[i]);
+                part[i] = 0.0f;
+            }
+            kin = 0;
+        }
+    };
+    int r = 0;
+    for (; r + 4 <= a.M; r += 4) {
+        const uint4 q0 = ld_grad<PATH>(a.grads[r] + g), q1 = ld_grad<PATH>(a.grads[r + 1] + g);
+        const uint4 q2 = ld_grad<PATH>(a.grads[r + 2] + g), q3 = ld_grad<PATH>(a.grads[r + 3] + g);
+        take(q0);
+        take(q1);
+        take(q2);
+        take(q3);
+    }
+    for (; r < a.M; ++r) take(ld_grad<PATH>(a.grads[r] + g));
+}
+
+// The same order with a compile-time rank count: all MT loads are issued first (as in the
+// plain kernels), then the values are added group by group.
+template <int MT, int PATH>
+__device__ __forceinline__ void rank_sum_grouped_fixed(const StepArgs& a, int64_t g, float acc[8]) {
+    constexpr int CH = MT < 8 ? MT : 8;  // loads in flight at once (bounds the registers)
+    uint4 q[CH];
+    const int K = MT / a.groups;
+    float part[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+    int kin = 0;
+#pragma unroll
+    for (int r = 0; r < MT; ++r) {
+        if (r % CH == 0) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) q[j] = ld_grad<PATH>(a.grads[r + j] + g);
+        }
+        add8(part, q[r % CH]);
+        // branch-free group flush: compute, then select (a branch here would keep the
+        // compiler from issuing later loads early)
+        const bool last = ++kin == K;
+        kin = last ? 0 : kin;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t = __fadd_rn(acc[i], part[i]);
+            acc[i] = last ? t : acc[i];
+            part[i] = last ? 0.0f : part[i];
+        }
     }
 }
 
@@ -153,7 +203,9 @@ template <int MT, int PATH, bool GROUPED>
 __device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t g, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
-    if constexpr (GROUPED) {
+    if constexpr (GROUPED && MT > 0) {
+        rank_sum_grouped_fixed<MT, PATH>(a, g, acc);
+    } else if constexpr (GROUPED) {
         rank_sum_grouped<PATH>(a, g, acc);
     } else if constexpr (MT > 0) {
         uint4 q[MT];
@@ -598,7 +650,14 @@ __global__ void __launch_bounds__(kThreadsInit) k_save(const float* __restrict__
 template <template <int> class F>
 struct ByM {
     static auto get(int M, int groups = 1) {
-        if (groups > 1) return F<-1>::fn();  // hybrid sharding: the grouped, generic-M kernel
+        if (groups > 1) {  // hybrid sharding: grouped kernels, encoded as F<-M> (F<-64>: generic M)
+            switch (M) {
+                case 4: return F<-4>::fn();
+                case 8: return F<-8>::fn();
+                case 16: return F<-16>::fn();
+                default: return F<-64>::fn();
+            }
+        }
         switch (M) {
             case 1: return F<1>::fn();
             case 2: return F<2>::fn();
@@ -610,18 +669,32 @@ struct ByM {
     }
 };
 
-// MT = -1 stands for the grouped (hybrid-sharding) kernel with a runtime rank count.
+// A negative MT stands for the grouped (hybrid-sharding) kernel of rank count -MT, with -64
+// for the generic (runtime rank count) one.
+constexpr int grouped_mt(int mt) { return mt == -64 ? 0 : -mt; }
 template <int MT> struct RsNormWrite {
-    static auto fn() { return MT < 0 ? &k_rs_norm<0, true, true> : &k_rs_norm<(MT < 0 ? 0 : MT), true>; }
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_norm<grouped_mt(MT), true, true>;
+        else return &k_rs_norm<MT, true>;
+    }
 };
 template <int MT> struct RsNormOnly {
-    static auto fn() { return MT < 0 ? &k_rs_norm<0, false, true> : &k_rs_norm<(MT < 0 ? 0 : MT), false>; }
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_norm<grouped_mt(MT), false, true>;
+        else return &k_rs_norm<MT, false>;
+    }
 };
 template <int MT> struct RsAdamwScaled {
-    static auto fn() { return MT < 0 ? &k_rs_adamw<0, true, true> : &k_rs_adamw<(MT < 0 ? 0 : MT), true>; }
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_adamw<grouped_mt(MT), true, true>;
+        else return &k_rs_adamw<MT, true>;
+    }
 };
 template <int MT> struct RsAdamwPlain {
-    static auto fn() { return MT < 0 ? &k_rs_adamw<0, false, true> : &k_rs_adamw<(MT < 0 ? 0 : MT), false>; }
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_adamw<grouped_mt(MT), false, true>;
+        else return &k_rs_adamw<MT, false>;
+    }
 };
 
 const void* variant_fn(int variant, int M, int groups) {
