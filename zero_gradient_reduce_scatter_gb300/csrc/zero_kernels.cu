@@ -482,8 +482,9 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
         if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
-        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // full-layout gradients start at lane 0
+        // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
         load_state(a, o, p, m, v);
+        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // full-layout gradients start at lane 0
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
         adam_vec<SCALE>(gh, s, p, m, v, a.k);
