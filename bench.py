@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-procs", type=int, default=0,
+                    help="oracle processes for the CPU baseline and the reference arm (0 = one per host core)")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
                     help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
@@ -221,14 +223,15 @@ def ncu_traffic(kernel_key: str, workload_key: str):
 # ------------------------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample of the workload
 # ------------------------------------------------------------------------------------------
-def cpu_baseline(w, target_seconds=15.0):
+def _oracle_sample(w, seed_step):
+    """Inputs of one oracle sample: a 4 Mi-parameter slice of the workload with its M, stage,
+    clip and gradient recipe (gradients drawn for step `seed_step`)."""
     import numpy as np
     import torch
 
     import oracle as O
     import workloads as W
 
-    # sample: a contiguous slice of the workload's parameters, same M / stage / clip
     lanes = 1 << 22
     sample = W.small_variant(w, (lanes,), steps=1)
     p = O.plan(sample.numel, sample.M, sample.bucket_bytes)
@@ -239,19 +242,82 @@ def cpu_baseline(w, target_seconds=15.0):
     grads = []
     for r in range(sample.M):
         g = torch.zeros(p.npad, dtype=torch.bfloat16)
-        W.fill_grads(sample, r, 0, g, [0], sig)
+        W.fill_grads(sample, r, seed_step, g, [0], sig)
         grads.append(g.view(torch.int16).numpy().view(np.uint16))
-    done, t0 = 0, time.perf_counter()
-    while True:
-        O.zero_step(p, st, grads, oh)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= target_seconds or done >= 10000:
-            break
-    rate = done * p.N / el
-    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} oracle steps of a {p.N}-parameter slice of the workload (M={w.M}, "
-                      f"ZeRO-{w.stage}, clip {'on' if w.clip else 'off'}), single thread, {el:.1f} s"}
+    return O, p, st, grads, oh
+
+
+def _oracle_windows(w, worker, windows, seconds, barrier=None):
+    """(parameters stepped, seconds) for each of `windows` timed windows of whole oracle steps."""
+    O, p, st, grads, oh = _oracle_sample(w, worker)
+    out = []
+    for _ in range(windows):
+        if barrier is not None:
+            barrier.wait(timeout=600)
+        done, t0 = 0, time.perf_counter()
+        while True:
+            O.zero_step(p, st, grads, oh)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or done >= 10000:
+                break
+        out.append((done * p.N, el))
+    return out
+
+
+def _oracle_proc(w, worker, windows, seconds, barrier, q):
+    import torch
+    torch.set_num_threads(1)
+    try:
+        q.put((worker, _oracle_windows(w, worker, windows, seconds, barrier)))
+    except BaseException as e:  # reported to the parent, which raises
+        if barrier is not None:
+            barrier.abort()
+        q.put((worker, repr(e)))
+
+
+def oracle_rates(w, procs, windows, seconds):
+    """Aggregate params/s of `procs` concurrent single-threaded oracle processes (spawned), each
+    on its own slice of the workload, per timed window: all parameters stepped in the window
+    over the longest of the processes' window times. One process runs in this one."""
+    if procs <= 1:
+        res = [_oracle_windows(w, 0, windows, seconds)]
+    else:
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        bar, q = ctx.Barrier(procs), ctx.Queue()
+        ps = [ctx.Process(target=_oracle_proc, args=(w, k, windows, seconds, bar, q)) for k in range(procs)]
+        for p in ps:
+            p.start()
+        try:
+            got = dict(q.get(timeout=900) for _ in ps)
+        finally:
+            for p in ps:
+                p.join(timeout=60)
+                if p.is_alive():
+                    p.kill()
+        bad = [v for v in got.values() if isinstance(v, str)]
+        if bad:
+            raise RuntimeError(f"oracle process failed: {bad[0]}")
+        res = list(got.values())
+    return [sum(r[i][0] for r in res) / max(r[i][1] for r in res) for i in range(windows)]
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def cpu_baseline(w, procs=0):
+    """The oracle as it stands on the host cores: one process per core (each single-threaded, on
+    its own 4 Mi-parameter slice, ~1.5 s), plus one process alone (~4 s) for the per-core rate."""
+    procs = procs or host_cores()
+    single = oracle_rates(w, 1, 1, 4.0)[0]
+    multi = oracle_rates(w, procs, 1, 1.5)[0] if procs > 1 else single
+    desc = (f"oracle steps of 4,194,304-parameter slices of the workload (M={w.M}, ZeRO-{w.stage}, "
+            f"clip {'on' if w.clip else 'off'}): {procs} single-threaded processes for ~1.5 s, "
+            f"and one alone for ~4 s (single_thread_value)")
+    return {"value": multi, "unit": "params/s", "cores": procs, "kind": "oracle", "single_thread_value": single,
+            "sample": desc}
 
 
 # ------------------------------------------------------------------------------------------
@@ -305,15 +371,16 @@ def run_ours(args):
     barrier(dist, device)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
         opt.step(grads, h)
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(dist, device)
-    ms_total = e0.elapsed_time(e1)
+    ms_total = ev[0].elapsed_time(ev[-1])
+    step_ms = step_stats([ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)], dist, device)
     ktimes = opt.kernel_times()
     opt.set_timing(False)
     ms_total_max = max_over_ranks(dist, ms_total, device)
@@ -371,12 +438,13 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+        cpu = cpu_baseline(w, args.cpu_procs)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": step_ms["median"],
+            "ms_per_step_min": step_ms["min"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage,
@@ -406,19 +474,18 @@ def run_reference(args):
     if rank != 0:
         return
     w = workload(args)
-    per_step = []
-    cb = None
-    for _ in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, target_seconds=2.0)
-        per_step.append(cb)
-    timed = per_step[args.warmup:]
-    rate = statistics.median(c["value"] for c in timed) if timed else per_step[-1]["value"]
+    procs = args.cpu_procs or host_cores()
+    rates = oracle_rates(w, procs, args.warmup + args.steps, 2.0)
+    timed = rates[args.warmup:] or rates[-1:]
+    rate = statistics.median(timed)
+    sample = (f"per step, ~2 s of oracle steps on 4,194,304-parameter slices of the workload (M={w.M}, "
+              f"ZeRO-{w.stage}, clip {'on' if w.clip else 'off'}) in {procs} single-threaded processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.N / rate * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "params": w.N, "M": w.M, "stage": w.stage, "clip": w.clip},
-        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": cb["sample"]},
+        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": procs, "kind": "oracle", "sample": sample},
         "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -429,15 +496,23 @@ def _timed_region(fn, steps, stream, dist, device):
     barrier(dist, device)
     torch.cuda.synchronize()
     clocks = ClockSampler(device.index)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
         fn()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(dist, device)
-    return max_over_ranks(dist, e0.elapsed_time(e1), device), clk
+    step_ms = step_stats([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)], dist, device)
+    return max_over_ranks(dist, ev[0].elapsed_time(ev[-1]), device), clk, step_ms
+
+
+def step_stats(ms, dist, device):
+    """Median and minimum of the per-step times (CUDA events between steps), each the max over
+    ranks."""
+    return {"median": round(max_over_ranks(dist, statistics.median(ms), device), 4),
+            "min": round(max_over_ranks(dist, min(ms), device), 4)}
 
 
 def run_stream(args):
@@ -479,7 +554,7 @@ def run_stream(args):
         raise SystemExit("warm-up step failed")
     opt.set_timing(True)
     opt.kernel_times()
-    ms, clk = _timed_region(step, args.steps, stream, dist, device)
+    ms, clk, step_ms = _timed_region(step, args.steps, stream, dist, device)
     kt = opt.kernel_times()
     n, lanes = w.N, opt.sizes["npad"]
     peak, kind = hbm_peak()
@@ -492,6 +567,7 @@ def run_stream(args):
         print(json.dumps({
             "metric": METRIC + " (ZeRO-2 per-bucket streaming)", "mode": "stream", "value": world * n * args.steps / (ms / 1e3),
             "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_median": step_ms["median"], "ms_per_step_min": step_ms["min"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
@@ -542,7 +618,7 @@ def run_gather(args):
     torch.cuda.synchronize()
     opt.set_timing(True)
     opt.kernel_times()
-    ms, clk = _timed_region(sweep, args.steps, stream, dist, device)
+    ms, clk, step_ms = _timed_region(sweep, args.steps, stream, dist, device)
     kt = opt.kernel_times()
     n = w.N
     peak, kind = hbm_peak()
@@ -552,7 +628,8 @@ def run_gather(args):
         print(json.dumps({
             "metric": "params/s and achieved HBM GB/s of the ZeRO-3 per-bucket parameter all-gather", "mode": "gather",
             "value": world * n * args.steps / (ms / 1e3), "unit": "params/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "ms_per_step_median": step_ms["median"],
+            "ms_per_step_min": step_ms["min"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
                        "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead"},

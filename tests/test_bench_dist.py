@@ -67,11 +67,16 @@ def test_missing_rank_is_detected_by_timeout():
     assert what != "joined" and took < 60
 
 
+def test_step_stats_single_process():
+    import bench
+    assert bench.step_stats([3.0, 1.0, 2.0, 10.0], None, None) == {"median": 2.5, "min": 1.0}
+
+
 def test_reference_arm_under_torchrun_prints_one_line():
     port = free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
-           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--config", "0"]
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--config", "0", "--cpu-procs", "2"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600,
                        env=dict(os.environ, OMP_NUM_THREADS="1"))
     assert r.returncode == 0, r.stderr[-2000:]
@@ -80,3 +85,5 @@ def test_reference_arm_under_torchrun_prints_one_line():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["n_gpus"] == 2
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+    # two oracle processes, one per core asked for, timed over the same windows
+    assert rec["cpu_baseline"]["cores"] == 2 and rec["cpu_baseline"]["value"] == rec["value"]
