@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="step mode: capture one step (scalars from a device schedule) in a CUDA graph and "
+                         "time its replays; the roofline then covers the whole step")
     ap.add_argument("--cpu-procs", type=int, default=0,
                     help="oracle processes for the CPU baseline and the reference arm (0 = one per host core)")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
@@ -359,8 +362,30 @@ def run_ours(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
+    graph, launches_per_step = None, 0
+    if args.graph:
+        # the step's scalars come from a device schedule, so one captured step replays as the
+        # next step each time; an eager scheduled step first counts the launches of a step
+        if args.warmup + args.steps + 1 > zg.ZERO_MAX_SCHEDULE:
+            raise SystemExit(f"--graph: at most {zg.ZERO_MAX_SCHEDULE - 1} warm-up and timed steps")
+        opt.set_schedule([h] * (args.warmup + args.steps + 1))
+        opt.set_timing(True)
+        opt.kernel_times()
+        opt.step_scheduled(grads)
+        launches_per_step = int(sum(c for _, c in opt.kernel_times().values()))
+        opt.set_timing(False)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            opt.step_scheduled(grads)
+
+        def one_step():
+            graph.replay()
+    else:
+        def one_step():
+            opt.step(grads, h)
+
     for _ in range(args.warmup):
-        opt.step(grads, h)
+        one_step()
     torch.cuda.synchronize()
     if opt.sync_status() != 0:
         raise SystemExit("warm-up step saw a non-finite gradient norm")
@@ -374,7 +399,7 @@ def run_ours(args):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     ev[0].record(stream)
     for i in range(args.steps):
-        opt.step(grads, h)
+        one_step()
         ev[i + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -391,24 +416,35 @@ def run_ours(args):
     alg_b = alg_bytes_per_param(w.M) * n
     gbs_alg = alg_b / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
-    launches = int(sum(c for _, c in ktimes.values()))
-
-    # dominant kernel (largest share of the timed region)
-    dom = max((k for k in ktimes if ktimes[k][1] > 0), key=lambda k: ktimes[k][0])
-    dom_ms = ktimes[dom][0] / ktimes[dom][1]
+    peak_source = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
     lanes = opt.sizes["npad"]
-    dom_bytes = kernel_alg_bytes_per_lane(dom, w.M, ghat_mode == "materialize") * lanes
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    variant = {"rs_adamw": "rs_adamw_scaled" if clip and ghat_mode != "materialize" else "rs_adamw_plain",
-               "adamw": "adamw", "rs_norm": "rs_norm_write" if ghat_mode == "materialize" else "rs_norm_only",
-               "gather": "gather", "norm_final": "norm_final"}[dom]
-    workload_key = f"config{args.config}" + (f"-max{args.max_params}" if args.max_params else "")
-    traffic = ncu_traffic(variant, workload_key)
-    roofline = {"bound": "hbm", "kernel": variant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
-                "kernel_share": {k: round(v[0] / max(ms_total, 1e-9), 4) for k, v in ktimes.items() if v[1]}}
+    if graph is not None:
+        # replays run no per-launch events: the roofline covers the whole step
+        launches = launches_per_step * args.steps
+        roofline = {"bound": "hbm", "kernel": "whole step (CUDA graph replay)", "achieved": round(gbs_alg, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(gbs_alg / peak, 4), "traffic": None,
+                    "peak_source": peak_source, "alg_bytes_per_launch": alg_b, "avg_launch_ms": round(ms_per_step, 4),
+                    "launches_per_step": launches_per_step}
+    else:
+        launches = int(sum(c for _, c in ktimes.values()))
+        # dominant kernel (largest share of the timed region)
+        dom = max((k for k in ktimes if ktimes[k][1] > 0), key=lambda k: ktimes[k][0])
+        dom_ms = ktimes[dom][0] / ktimes[dom][1]
+        dom_bytes = kernel_alg_bytes_per_lane(dom, w.M, ghat_mode == "materialize") * lanes
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        variant = {"rs_adamw": "rs_adamw_scaled" if clip and ghat_mode != "materialize" else "rs_adamw_plain",
+                   "adamw": "adamw", "rs_norm": "rs_norm_write" if ghat_mode == "materialize" else "rs_norm_only",
+                   "gather": "gather", "norm_final": "norm_final"}[dom]
+        workload_key = f"config{args.config}" + (f"-max{args.max_params}" if args.max_params else "")
+        traffic = ncu_traffic(variant, workload_key)
+        roofline = {"bound": "hbm", "kernel": variant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_source,
+                    "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
+                    "kernel_share": {k: round(v[0] / max(ms_total, 1e-9), 4) for k, v in ktimes.items() if v[1]}}
+    if graph is not None:
+        if opt.sync_status() != 0:
+            raise SystemExit("a replayed step found no schedule entry or a non-finite norm")
+        opt.set_schedule(None)  # the host-buffer steps below take host scalars
 
     # ---- end to end through the C ABI with host buffers (pinned) -----------------------
     e2e = None
@@ -450,8 +486,8 @@ def run_ours(args):
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage,
                        "clip": w.clip, "bucket_bytes": w.bucket_bytes, "gather": gather, "ghat_mode": ghat_mode,
                        "padded_lanes": lanes,
-                       "l2": f"inputs {(opt.sizes['bytes_grad_each'] * w.M + 12 * lanes) / 1e9:.1f} GB > L2 "
-                             f"{L2_BYTES / 1e6:.0f} MB; no flush",
+                       "l2": l2_note(opt.sizes["bytes_grad_each"] * w.M + 12 * lanes),
+                       "cuda_graph": bool(args.graph),
                        "parallelism": f"{world} independent emulated jobs (one per GPU)"},
             "gbs_alg": round(gbs_alg, 1), "alg_bytes_per_param": alg_bytes_per_param(w.M),
             "frac_of_peak_alg": round(gbs_alg / peak, 4),
@@ -506,6 +542,14 @@ def _timed_region(fn, steps, stream, dist, device):
     barrier(dist, device)
     step_ms = step_stats([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)], dist, device)
     return max_over_ranks(dist, ev[0].elapsed_time(ev[-1]), device), clk, step_ms
+
+
+def l2_note(input_bytes):
+    """How the timed steps relate to L2 (inputs larger than L2 need no flush between steps)."""
+    if input_bytes > L2_BYTES:
+        return f"inputs {input_bytes / 1e9:.2f} GB > L2 {L2_BYTES / 1e6:.0f} MB; no flush"
+    return (f"inputs {input_bytes / 1e6:.3f} MB fit in L2 {L2_BYTES / 1e6:.0f} MB and are not flushed: "
+            f"a latency figure for a launch-bound step, not a bandwidth one")
 
 
 def step_stats(ms, dist, device):

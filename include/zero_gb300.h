@@ -66,14 +66,20 @@ extern "C" {
 #define ZERO_ERR_CUDA          -6  /* a CUDA runtime call failed; see zero_last_cuda_error */
 #define ZERO_ERR_BAD_CONTEXT   -7  /* null, destroyed or unknown context                 */
 #define ZERO_ERR_NOT_COMPUTED  -8  /* the requested value was not computed (no clipping)  */
-#define ZERO_ERR_TOO_LARGE     -9  /* more buckets than zero_grad_norm_noalloc's fixed
-                                      scratch holds (ZERO_NOALLOC_MAX_BUCKETS)            */
+#define ZERO_ERR_TOO_LARGE     -9  /* a count over a fixed limit: buckets for
+                                      zero_grad_norm_noalloc (ZERO_NOALLOC_MAX_BUCKETS),
+                                      schedule entries (ZERO_MAX_SCHEDULE)                */
 #define ZERO_ERR_DEVICE       -10  /* checked build: a kernel rejected an out-of-bounds
                                       index (and skipped the access); see zero_check_report */
+#define ZERO_ERR_SCHEDULE     -11  /* scheduled steps: a call that needs the host step count
+                                      while a schedule is installed, a scheduled call with
+                                      none, or a step past the schedule's last entry        */
 
 #define ZERO_ALIGN       64  /* shard length granule in lanes: 128 B of bf16, 256 B of fp32 */
 #define ZERO_MAX_RANKS   64  /* largest emulated rank count M                             */
 #define ZERO_NOALLOC_MAX_BUCKETS 2048  /* bucket-table rows zero_grad_norm_noalloc can hold  */
+#define ZERO_MAX_SCHEDULE 1024  /* entries of one step schedule (zero_set_schedule), kept in
+                                   the scratch buffer (40 bytes each)                       */
 
 /* gather modes (zero_config.gather) */
 #define ZERO_GATHER_FUSED  0  /* the AdamW epilogue writes each owner's bf16 values straight
@@ -103,7 +109,8 @@ extern "C" {
 #define ZERO_K_RS_ADAMW     3  /* fused reduce-scatter + AdamW (+ all-gather epilogue)     */
 #define ZERO_K_GATHER       4  /* bf16 shards -> full unpadded buffer                     */
 #define ZERO_K_INIT         5  /* state initialisation                                    */
-#define ZERO_NUM_KERNELS    6
+#define ZERO_K_STEP_BEGIN   6  /* scheduled steps: one thread, counter and scalars         */
+#define ZERO_NUM_KERNELS    7
 
 typedef struct zero_ctx zero_ctx; /* opaque, library-owned */
 
@@ -147,7 +154,8 @@ typedef struct {
     int64_t bytes_param_full;   /* bf16 n                                                  */
     int64_t bytes_param_shards; /* bf16 npad with ZERO_GATHER_SHARDS, else 0               */
     int64_t bytes_grad_each;    /* bf16 npad: each of the M gradient buffers               */
-    int64_t bytes_scratch;      /* status word, norm partials and the bucket table         */
+    int64_t bytes_scratch;      /* status word, norm partials, bucket table, per-bucket
+                                   sums and the step schedule                               */
 } zero_sizes;
 
 /* Device buffers borrowed by a context. All 16-byte aligned (torch allocations are). */
@@ -228,6 +236,44 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
                               int stage, const zero_hyper* hyper, void* host_params, void* stream,
                               void* copy_stream);
 
+/* Steps whose scalars live on the device, for capture in a CUDA graph. The pages define no
+ * interface for this. It serves training loops that capture whole steps as CUDA graphs and
+ * replay them. A captured launch keeps the arguments it was captured with. The per-step
+ * scalars of AdamW (lr and the bias corrections of step t, Loshchilov & Hutter's decoupled
+ * weight decay with Kingma & Ba's corrections) therefore cannot travel as launch arguments.
+ *
+ * zero_set_schedule uploads them for the next `count` steps. Entry i serves step t + 1 + i,
+ * t being the step count at the call. The host forms them exactly as zero_step does, so a
+ * scheduled step is bit-identical to zero_step with the same hyper-parameters.
+ *   per_step  host array of `count` zero_hyper, one per step (schedules of lr, betas, eps,
+ *             weight_decay or max_grad_norm). `clip` and `ghat_mode` must be equal in all
+ *             entries, since they choose the kernels a graph fixes.
+ *   count     entries; 0 (per_step NULL) leaves scheduled mode.
+ * The entries go to the scratch buffer (at most ZERO_MAX_SCHEDULE; a longer run uploads
+ * the next schedule when one ends). The call synchronises `stream` and must not be
+ * captured.
+ *
+ * zero_step_scheduled and zero_apply_scheduled are zero_step and zero_apply without
+ * hyper-parameters. Their first launch is one thread (ZERO_K_STEP_BEGIN). It advances a
+ * step counter kept on the device and copies that step's entry into the status word, which
+ * the update kernels read. They enqueue kernel launches only, so they can be captured, and
+ * every replay is the next step. A step past the last entry changes no state and leaves
+ * the counter where it was. It sets a sticky flag, so later steps skip too, and
+ * zero_sync_status returns ZERO_ERR_SCHEDULE. A new schedule clears the flag and continues
+ * from the last step that ran.
+ *
+ * While a schedule is installed, the device counts the steps. zero_get_step synchronises
+ * the device and reads that count. zero_step, zero_apply, zero_step_host*, zero_set_step
+ * and zero_load_state return ZERO_ERR_SCHEDULE, as do the scheduled calls when no schedule
+ * is installed. Status queries (zero_last_norm, zero_sync_status, zero_check_report)
+ * synchronise the whole device, since replays may run on any stream.
+ * Errors: BAD_CONTEXT, INVALID_ARG (count < 0, per_step NULL with count > 0, a bad entry,
+ * entries with unequal clip or ghat_mode), TOO_LARGE (count > ZERO_MAX_SCHEDULE),
+ * SIZE_MISMATCH (materialize without a ghat buffer), STAGE, MISALIGNED, SCHEDULE, CUDA. */
+int zero_set_schedule(zero_ctx* ctx, const zero_hyper* per_step, int64_t count, void* stream);
+int zero_step_scheduled(zero_ctx* ctx, const void* const* grads, int stage, void* stream);
+int zero_apply_scheduled(zero_ctx* ctx, int stage, void* stream);
+
 /* Device pointer of the full bf16 parameters [n] (valid until the next step). */
 int zero_params(zero_ctx* ctx, void** full_bf16);
 
@@ -258,7 +304,8 @@ int zero_get_state(zero_ctx* ctx, int which, int rank, void* dst, void* stream);
 int zero_last_norm(zero_ctx* ctx, double* norm, float* scale);
 
 /* Waits for the last step's stream and returns ZERO_OK, ZERO_ERR_NONFINITE (update
- * skipped), ZERO_ERR_DEVICE (checked build: a bounds check failed) or ZERO_ERR_CUDA. */
+ * skipped), ZERO_ERR_SCHEDULE (a scheduled step found no entry), ZERO_ERR_DEVICE (checked
+ * build: a bounds check failed) or ZERO_ERR_CUDA. */
 int zero_sync_status(zero_ctx* ctx);
 
 /* Checked builds (compiled with -DZERO_CHECKED; zero_checked_build() returns 1) test every

@@ -67,6 +67,23 @@ def main():
     wg = W.small_variant(W.config(3), W.ragged_numel(30, 200, 5000, 23), M=8, stage=3, steps=2)
     exact(run_elementwise(wg, gather="shards", groups=2, ghat_mode="materialize", ghat_buffer=True), "hybrid")
 
+    # a scheduled step captured in a CUDA graph, replayed past its schedule
+    wq = W.small_variant(W.config(3), W.ragged_numel(20, 300, 5000, 29), M=8, steps=1, clip=0.02)
+    opt = zg.ZeroOptimizer(wq.numel, wq.M, wq.stage, W.master_init(wq, dev), groups=2, gather="shards")
+    gq = opt.new_grad_buffers()
+    for r in range(wq.M):
+        W.fill_grads(wq, r, 0, gq[r], opt.tensor_offsets)
+    hq, _ = make_hyper(wq)
+    opt.set_schedule([hq, hq])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt.step_scheduled(gq)
+    for _ in range(2):
+        graph.replay()
+    clean(opt, "scheduled steps")
+    graph.replay()
+    assert opt.sync_status() == zg.ZERO_ERR_SCHEDULE and opt.check_report()[0] == 0 and opt.t == 2
+
     # ZeRO-2 streaming against the oracle's monolithic step
     ws = W.small_variant(W.config(1), (70000, 5000, 300, 70000), bucket_bytes=120000, steps=2, clip=1.0)
     opt = zg.ZeroOptimizer(ws.numel, ws.M, ws.stage, W.master_init(ws, dev), bucket_bytes=ws.bucket_bytes,

@@ -46,7 +46,7 @@ def test_release_build_is_not_the_checked_build(zg):
 
 
 def test_error_strings(zg):
-    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -99]:
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -11, -99]:
         assert zg._lib().zero_strerror(code)
 
 

@@ -34,16 +34,18 @@ ZERO_OK = 0
 ERRORS = {
     -1: "ZERO_ERR_INVALID_ARG", -2: "ZERO_ERR_MISALIGNED", -3: "ZERO_ERR_SIZE_MISMATCH",
     -4: "ZERO_ERR_STAGE", -5: "ZERO_ERR_NONFINITE", -6: "ZERO_ERR_CUDA", -7: "ZERO_ERR_BAD_CONTEXT",
-    -8: "ZERO_ERR_NOT_COMPUTED", -9: "ZERO_ERR_TOO_LARGE", -10: "ZERO_ERR_DEVICE",
+    -8: "ZERO_ERR_NOT_COMPUTED", -9: "ZERO_ERR_TOO_LARGE", -10: "ZERO_ERR_DEVICE", -11: "ZERO_ERR_SCHEDULE",
 }
 ZERO_ERR_NONFINITE = -5
 ZERO_ERR_NOT_COMPUTED = -8
+ZERO_ERR_SCHEDULE = -11
 ZERO_ALIGN = 64
 ZERO_MAX_RANKS = 64
+ZERO_MAX_SCHEDULE = 1024
 GATHER = {"fused": 0, "shards": 1}
 GHAT = {"auto": 0, "materialize": 1, "recompute": 2}
 STATE = {"master": 0, "m": 1, "v": 2, "ghat": 3}
-KERNELS = ("rs_norm", "norm_final", "adamw", "rs_adamw", "gather", "init")
+KERNELS = ("rs_norm", "norm_final", "adamw", "rs_adamw", "gather", "init", "step_begin")
 
 
 class ZeroError(RuntimeError):
@@ -98,6 +100,9 @@ SIGNATURES = {
     "zero_step_host_overlapped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P, _P, _P]),
     "zero_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
     "zero_apply": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
+    "zero_set_schedule": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
+    "zero_step_scheduled": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
+    "zero_apply_scheduled": (ctypes.c_int, [_P, ctypes.c_int, _P]),
     "zero_params": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     "zero_save_state": (ctypes.c_int, [_P, _P, _P, _P, _P]),
     "zero_load_state": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P]),
@@ -308,6 +313,26 @@ class ZeroOptimizer:
     def apply(self, hyper: Hyper, stream=None):
         _check(_lib().zero_apply(self._ctx, self.stage, ctypes.byref(hyper), _stream_handle(stream)), "zero_apply")
 
+    # ---- steps with device-resident scalars (CUDA graph capture) ----------------------
+    def set_schedule(self, hypers, stream=None):
+        """Upload the hyper-parameters of the next len(hypers) steps (one Hyper each; equal
+        clip and ghat_mode) to the device; None or [] leaves scheduled mode. Synchronises."""
+        hypers = list(hypers or [])
+        arr = (Hyper * len(hypers))(*hypers) if hypers else None
+        _check(_lib().zero_set_schedule(self._ctx, ctypes.cast(arr, _P) if arr is not None else None, len(hypers),
+                                        _stream_handle(stream)), "zero_set_schedule")
+
+    def step_scheduled(self, grads, stream=None):
+        """step() with this step's hyper-parameters taken from the device schedule; only
+        kernel launches, so it can be captured in a CUDA graph (each replay is a step)."""
+        ptrs = self._ptrs(grads)
+        _check(_lib().zero_step_scheduled(self._ctx, ctypes.cast(ptrs, _P), self.stage, _stream_handle(stream)),
+               "zero_step_scheduled")
+
+    def apply_scheduled(self, stream=None):
+        """apply() with this step's hyper-parameters taken from the device schedule."""
+        _check(_lib().zero_apply_scheduled(self._ctx, self.stage, _stream_handle(stream)), "zero_apply_scheduled")
+
     def step_host_overlapped(self, host_grads, dev_grads, host_params: torch.Tensor, hyper: Hyper,
                              copy_stream, stream=None):
         """step_host with the host-to-device copies on `copy_stream`, overlapping the previous
@@ -442,9 +467,10 @@ class ZeroOptimizer:
         return n.value, s.value
 
     def sync_status(self) -> int:
-        """0, or ZERO_ERR_NONFINITE if the last clipped step was skipped."""
+        """0, ZERO_ERR_NONFINITE if the last clipped step was skipped, or ZERO_ERR_SCHEDULE if
+        a scheduled step found no schedule entry."""
         rc = _lib().zero_sync_status(self._ctx)
-        if rc not in (ZERO_OK, ZERO_ERR_NONFINITE):
+        if rc not in (ZERO_OK, ZERO_ERR_NONFINITE, ZERO_ERR_SCHEDULE):
             _check(rc, "zero_sync_status")
         return rc
 

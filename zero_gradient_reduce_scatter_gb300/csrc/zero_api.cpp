@@ -61,6 +61,12 @@ struct zero_ctx {
     };
     std::vector<GradSet> grad_sets;
     cudaEvent_t h2d_done = nullptr;
+    // scheduled steps (zero_set_schedule): the table of per-step scalars (in the scratch
+    // buffer); while active, the step count lives in the device status word
+    zg::ScheduleEntry* dev_sched = nullptr;
+    bool sched_active = false;
+    int sched_clip = 0;
+    int sched_mode = ZERO_GHAT_RECOMPUTE;
 };
 
 namespace {
@@ -248,6 +254,8 @@ struct Timed {
     size_t slot = SIZE_MAX;  // index into c->events (an index stays valid if the pool grows)
     Timed(zero_ctx* ctx, int kernel, cudaStream_t stream) : c(ctx), s(stream) {
         if (!c->timing || c->n_timed >= kMaxTimedLaunches) return;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;  // a graph replays no host timing
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return;
         if (c->n_timed == c->events.size()) {
             zero_ctx::TimedLaunch tl{kernel, nullptr, nullptr};
             if (cudaEventCreate(&tl.start) != cudaSuccess) return;
@@ -379,6 +387,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->partials = (double*)(scratch + zg::kScratchPartials);
     c->dev_buckets = (zg::Bucket*)(scratch + zg::kScratchBuckets);
     c->bucket_sums = (double*)(scratch + zg::scratch_bucket_sums((int64_t)L.buckets.size()));
+    c->dev_sched = (zg::ScheduleEntry*)(scratch + zg::scratch_schedule((int64_t)L.buckets.size()));
     c->reduced.assign(L.buckets.size(), 0);
     c->t = 0;
     c->last_clip = 0;
@@ -418,33 +427,32 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     return ZERO_OK;
 }
 
-int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper* h, void* stream) {
-    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
-    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
-    int rc = check_hyper(h);
-    if (rc) return rc;
+// Which clipped form a step takes (ZERO_GHAT_MATERIALIZE or ZERO_GHAT_RECOMPUTE).
+static int resolve_ghat_mode(const zero_ctx* c, const zero_hyper* h, int* mode) {
+    *mode = ZERO_GHAT_RECOMPUTE;
+    if (!h->clip) return ZERO_OK;
+    int m = h->ghat_mode;
+    if (m == ZERO_GHAT_AUTO) m = (c->cfg.M > 4 && c->bufs.ghat) ? ZERO_GHAT_MATERIALIZE : ZERO_GHAT_RECOMPUTE;
+    if (m == ZERO_GHAT_MATERIALIZE && !c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    *mode = m;
+    return ZERO_OK;
+}
+
+static int check_grads(const zero_ctx* c, const void* const* grads) {
     if (!grads) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r) {
         if (!grads[r]) return ZERO_ERR_INVALID_ARG;
         if (!aligned16(grads[r])) return ZERO_ERR_MISALIGNED;
     }
-    int mode = ZERO_GHAT_RECOMPUTE;
-    if (h->clip) {
-        mode = h->ghat_mode;
-        if (mode == ZERO_GHAT_AUTO) mode = (c->cfg.M > 4 && c->bufs.ghat) ? ZERO_GHAT_MATERIALIZE : ZERO_GHAT_RECOMPUTE;
-        if (mode == ZERO_GHAT_MATERIALIZE && !c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
-    }
-    DeviceGuard guard(c->device);
-    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
-    cudaStream_t s = (cudaStream_t)stream;
+    return ZERO_OK;
+}
 
-    c->t += 1;
-    zg::StepArgs a = base_args(c);
-    for (int r = 0; r < c->cfg.M; ++r) a.grads[r] = (const uint16_t*)grads[r];
-    a.k = adam_consts(h, c->t);
-
+// The kernels of one whole step: reduce-scatter (+ norm and clip), AdamW, all-gather.
+// sched: the scalars come from the device schedule (k_step_begin ran first), not a.k.
+static int launch_step(zero_ctx* c, const zg::StepArgs& a, int clip, int mode, double max_norm, bool sched,
+                       cudaStream_t s) {
     cudaError_t e = cudaSuccess;
-    if (h->clip) {
+    if (clip) {
         const bool write = mode == ZERO_GHAT_MATERIALIZE;
         const int g1 = grid_for(c, write ? zg::kVarRsNormWrite : zg::kVarRsNormOnly, a.nvec);
         {
@@ -453,33 +461,74 @@ int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper
         }
         if (e == cudaSuccess) {
             Timed tm(c, ZERO_K_NORM_FINAL, s);
-            e = zg::launch_norm_final(c->status, c->partials, g1, h->max_grad_norm, 1, s);
+            e = zg::launch_norm_final(c->status, c->partials, g1, max_norm, 1, sched, s);
         }
         if (e == cudaSuccess) {
             if (write) {
                 const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
                 Timed tm(c, ZERO_K_ADAMW, s);
-                e = zg::launch_adamw(a, g3, s);
+                e = zg::launch_adamw(a, sched, g3, s);
             } else {
                 const int g4 = grid_for(c, zg::kVarRsAdamwScaled, a.nvec);
                 Timed tm(c, ZERO_K_RS_ADAMW, s);
-                e = zg::launch_rs_adamw(a, true, g4, s);
+                e = zg::launch_rs_adamw(a, true, sched, g4, s);
             }
         }
     } else {
         const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.nvec);
         Timed tm(c, ZERO_K_RS_ADAMW, s);
-        e = zg::launch_rs_adamw(a, false, g4, s);
+        e = zg::launch_rs_adamw(a, false, sched, g4, s);
     }
     if (e == cudaSuccess && c->cfg.gather == ZERO_GATHER_SHARDS) {
-        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);  // the all-gather
+        const int rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);  // the all-gather
         if (rc) return rc;
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    c->last_clip = h->clip;
+    c->last_clip = clip;
     c->last_stream = s;
     c->stepped = 1;
     return ZERO_OK;
+}
+
+static int launch_step_begin(zero_ctx* c, cudaStream_t s) {
+    Timed tm(c, ZERO_K_STEP_BEGIN, s);
+    const cudaError_t e = zg::launch_step_begin(c->status, c->dev_sched, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+}
+
+int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper* h, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    if ((rc = check_grads(c, grads))) return rc;
+    int mode;
+    if ((rc = resolve_ghat_mode(c, h, &mode))) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    c->t += 1;
+    zg::StepArgs a = base_args(c);
+    for (int r = 0; r < c->cfg.M; ++r) a.grads[r] = (const uint16_t*)grads[r];
+    a.k = adam_consts(h, c->t);
+    return launch_step(c, a, h->clip, mode, h->max_grad_norm, false, s);
+}
+
+int zero_step_scheduled(zero_ctx* c, const void* const* grads, int stage, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_grads(c, grads);
+    if (rc) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    zg::StepArgs a = base_args(c);
+    for (int r = 0; r < c->cfg.M; ++r) a.grads[r] = (const uint16_t*)grads[r];
+    if ((rc = launch_step_begin(c, s))) return rc;
+    return launch_step(c, a, c->sched_clip, c->sched_mode, 0.0, true, s);
 }
 
 int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, void* stream) {
@@ -516,45 +565,124 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     return ZERO_OK;
 }
 
-int zero_apply(zero_ctx* c, int stage, const zero_hyper* h, void* stream) {
-    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+// The rest of a streamed step once every bucket is reduced: norm (+ clip), AdamW, all-gather.
+static int launch_apply(zero_ctx* c, const zg::StepArgs& a, int clip, double max_norm, bool sched, cudaStream_t s) {
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        e = zg::launch_norm_final(c->status, c->bucket_sums, (int)c->buckets.size(), max_norm, clip, sched, s);
+    }
+    if (e == cudaSuccess) {
+        const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
+        Timed tm(c, ZERO_K_ADAMW, s);
+        e = zg::launch_adamw(a, sched, g3, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (c->cfg.gather == ZERO_GATHER_SHARDS) {
+        const int rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);
+        if (rc) return rc;
+    }
+    std::fill(c->reduced.begin(), c->reduced.end(), 0);
+    c->last_clip = clip;
+    c->last_stream = s;
+    c->stepped = 1;
+    return ZERO_OK;
+}
+
+static int check_apply(const zero_ctx* c, int stage) {
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
-    int rc = check_hyper(h);
-    if (rc) return rc;
     if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
     for (char r : c->reduced)
         if (!r) return ZERO_ERR_INVALID_ARG;  // every bucket must be reduced first
+    return ZERO_OK;
+}
+
+int zero_apply(zero_ctx* c, int stage, const zero_hyper* h, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    if ((rc = check_apply(c, stage))) return rc;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     c->t += 1;
     zg::StepArgs a = base_args(c);
     a.k = adam_consts(h, c->t);
-    cudaError_t e;
-    {
-        Timed tm(c, ZERO_K_NORM_FINAL, s);
-        e = zg::launch_norm_final(c->status, c->bucket_sums, (int)c->buckets.size(), h->max_grad_norm, h->clip, s);
-    }
-    if (e == cudaSuccess) {
-        const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
-        Timed tm(c, ZERO_K_ADAMW, s);
-        e = zg::launch_adamw(a, g3, s);
-    }
+    return launch_apply(c, a, h->clip, h->max_grad_norm, false, s);
+}
+
+int zero_apply_scheduled(zero_ctx* c, int stage, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!c->sched_active) return ZERO_ERR_SCHEDULE;
+    int rc = check_apply(c, stage);
+    if (rc) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    zg::StepArgs a = base_args(c);
+    if ((rc = launch_step_begin(c, s))) return rc;
+    return launch_apply(c, a, c->sched_clip, 0.0, true, s);
+}
+
+// The device step counter of scheduled mode (synchronises the device).
+static int read_device_step(zero_ctx* c, int64_t* t) {
+    zg::Status st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&st, c->status, sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (c->cfg.gather == ZERO_GATHER_SHARDS) {
-        rc = gather_range(c, 0, c->n, (uint16_t*)c->bufs.param_full, s);
+    *t = st.t_dev;
+    return ZERO_OK;
+}
+
+int zero_set_schedule(zero_ctx* c, const zero_hyper* h, int64_t count, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (count < 0 || (count > 0 && !h)) return ZERO_ERR_INVALID_ARG;
+    if (count > ZERO_MAX_SCHEDULE) return ZERO_ERR_TOO_LARGE;
+    int mode = ZERO_GHAT_RECOMPUTE;
+    for (int64_t i = 0; i < count; ++i) {
+        int rc = check_hyper(&h[i]);
         if (rc) return rc;
+        if (h[i].clip != h[0].clip || h[i].ghat_mode != h[0].ghat_mode) return ZERO_ERR_INVALID_ARG;
+        if (i == 0 && (rc = resolve_ghat_mode(c, &h[0], &mode))) return rc;
     }
-    std::fill(c->reduced.begin(), c->reduced.end(), 0);
-    c->last_clip = h->clip;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cap != cudaStreamCaptureStatusNone) return ZERO_ERR_INVALID_ARG;
+    if (c->sched_active) {  // continue from the last step that ran
+        int64_t t = 0;
+        const int rc = read_device_step(c, &t);
+        if (rc) return rc;
+        c->t = t;
+    }
+    std::vector<zg::ScheduleEntry> tab((size_t)count);
+    for (int64_t i = 0; i < count; ++i) {
+        tab[(size_t)i].k = adam_consts(&h[i], c->t + 1 + i);
+        tab[(size_t)i].max_norm = h[i].clip ? h[i].max_grad_norm : 0.0;
+    }
+    if (count > 0)
+        e = cudaMemcpyAsync(c->dev_sched, tab.data(), (size_t)count * sizeof(zg::ScheduleEntry),
+                            cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = zg::launch_schedule_install(c->status, c->t, count, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host table must outlive the copy
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->sched_active = count > 0;
+    c->sched_clip = count > 0 ? h[0].clip : 0;
+    c->sched_mode = mode;
     c->last_stream = s;
-    c->stepped = 1;
+    // launch shapes now, outside any capture
+    for (int v = 0; v < zg::kNumVariants; ++v) grid_for(c, v, 1);
     return ZERO_OK;
 }
 
 int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
                    const zero_hyper* h, void* host_params, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!host_grads || !dev_grads || !host_params) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r)
         if (!host_grads[r] || !dev_grads[r]) return ZERO_ERR_INVALID_ARG;
@@ -590,6 +718,7 @@ int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
 
 int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* v, int64_t t, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!master || t < 0) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
@@ -608,6 +737,7 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
 int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
                               const zero_hyper* h, void* host_params, void* stream, void* copy_stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!host_grads || !dev_grads || !host_params || copy_stream == stream) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r)
         if (!host_grads[r] || !dev_grads[r]) return ZERO_ERR_INVALID_ARG;
@@ -723,8 +853,14 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
 static int read_status(zero_ctx* c, zg::Status* out) {
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
-    cudaError_t e = cudaMemcpyAsync(out, c->status, sizeof *out, cudaMemcpyDeviceToHost, c->last_stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    cudaError_t e;
+    if (c->sched_active) {  // replays of captured steps may run on any stream
+        e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaMemcpy(out, c->status, sizeof *out, cudaMemcpyDeviceToHost);
+    } else {
+        e = cudaMemcpyAsync(out, c->status, sizeof *out, cudaMemcpyDeviceToHost, c->last_stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    }
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
@@ -746,6 +882,7 @@ int zero_sync_status(zero_ctx* c) {
     int rc = read_status(c, &st);
     if (rc) return rc;
     if (st.flags & zg::kFlagBounds) return ZERO_ERR_DEVICE;
+    if (st.flags & zg::kFlagSchedule) return ZERO_ERR_SCHEDULE;
     if (c->stepped && c->last_clip && (st.flags & zg::kFlagNonfinite)) return ZERO_ERR_NONFINITE;
     return ZERO_OK;
 }
@@ -772,12 +909,18 @@ int zero_checked_build(void) {
 int zero_get_step(zero_ctx* c, int64_t* t) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!t) return ZERO_ERR_INVALID_ARG;
+    if (c->sched_active) {
+        DeviceGuard guard(c->device);
+        if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+        return read_device_step(c, t);
+    }
     *t = c->t;
     return ZERO_OK;
 }
 
 int zero_set_step(zero_ctx* c, int64_t t) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (t < 0) return ZERO_ERR_INVALID_ARG;
     c->t = t;
     return ZERO_OK;
@@ -861,6 +1004,8 @@ const char* zero_strerror(int status) {
         case ZERO_ERR_NOT_COMPUTED: return "value not computed by the last step";
         case ZERO_ERR_TOO_LARGE: return "layout exceeds the fixed scratch of zero_grad_norm_noalloc";
         case ZERO_ERR_DEVICE: return "a device-side bounds check failed (checked build); see zero_check_report";
+        case ZERO_ERR_SCHEDULE:
+            return "scheduled steps: no schedule installed, a host-step call while one is, or a step past its end";
         default: return "unknown status";
     }
 }

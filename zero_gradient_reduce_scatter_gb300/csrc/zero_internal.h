@@ -20,26 +20,39 @@ struct Bucket {
     int64_t uoff;
 };
 
-// Device status word at the start of the scratch buffer. Written by the norm-finalise
-// kernel; read by the update kernels and, after a stream synchronisation, by the host.
-struct Status {
-    double sumsq;   // sum of squared averaged gradient over real lanes
-    double norm;    // sqrt(sumsq)
-    float scale;    // clip scale applied to the averaged gradient
-    int32_t flags;  // kFlagNonfinite | kFlagBounds
-    int64_t bad_site;   // checked builds: first failing bounds check (0 = none) ...
-    int64_t bad_index;  // ... and the index it rejected
-    int64_t reserved[11];
-};
-static_assert(sizeof(Status) == 128, "status word is 128 bytes");
-
-constexpr int32_t kFlagNonfinite = 1;
-constexpr int32_t kFlagBounds = 4;  // checked builds: an index failed its bounds check (sticky)
-
 // Step constants of AdamW, formed on the host in double and rounded once to float.
 struct AdamConsts {
     float b1, b2, c1, c2, step, isb, decay, eps;
 };
+
+// One entry of a device-resident schedule: the scalars of one step (scheduled steps).
+struct ScheduleEntry {
+    AdamConsts k;
+    double max_norm;  // clip threshold of the step
+};
+
+// Device status word at the start of the scratch buffer. Written by the norm-finalise
+// kernel (norm, scale, flags) and by the step-begin kernel of scheduled steps (counter and
+// this step's scalars); read by the update kernels and, after a synchronisation, by the host.
+struct Status {
+    double sumsq;   // sum of squared averaged gradient over real lanes
+    double norm;    // sqrt(sumsq)
+    float scale;    // clip scale applied to the averaged gradient
+    int32_t flags;  // kFlagNonfinite | kFlagSchedule | kFlagBounds
+    int64_t bad_site;   // checked builds: first failing bounds check (0 = none) ...
+    int64_t bad_index;  // ... and the index it rejected
+    int64_t t_dev;        // scheduled steps: the step count, advanced on the device
+    int64_t sched_base;   // step served by schedule entry 0
+    int64_t sched_count;  // entries in the schedule
+    AdamConsts cur;       // scheduled steps: the scalars of the running step ...
+    double cur_max_norm;  // ... and its clip threshold
+    int64_t reserved[3];
+};
+static_assert(sizeof(Status) == 128, "status word is 128 bytes");
+
+constexpr int32_t kFlagNonfinite = 1;
+constexpr int32_t kFlagSchedule = 2;  // a scheduled step found no entry: it and later ones skip (sticky)
+constexpr int32_t kFlagBounds = 4;    // checked builds: an index failed its bounds check (sticky)
 
 // Everything a streaming kernel needs; passed by value (kernel parameter space).
 struct StepArgs {
@@ -98,8 +111,12 @@ constexpr int64_t kScratchPartials = 256;
 constexpr int64_t kScratchBuckets = kScratchPartials + 8 * kMaxPartials;
 // One fp64 sum of squares per bucket (per-bucket streaming) follows the bucket table.
 inline int64_t scratch_bucket_sums(int64_t n_buckets) { return (kScratchBuckets + 32 * n_buckets + 255) / 256 * 256; }
-inline int64_t scratch_bytes(int64_t n_buckets) {
+// The step schedule (scheduled steps, ZERO_MAX_SCHEDULE entries) follows the bucket sums.
+inline int64_t scratch_schedule(int64_t n_buckets) {
     return (scratch_bucket_sums(n_buckets) + 8 * n_buckets + 255) / 256 * 256;
+}
+inline int64_t scratch_bytes(int64_t n_buckets) {
+    return (scratch_schedule(n_buckets) + (int64_t)sizeof(ScheduleEntry) * ZERO_MAX_SCHEDULE + 255) / 256 * 256;
 }
 
 // Kernel variants, used as keys of the per-context launch-shape cache.
@@ -127,12 +144,19 @@ cudaError_t variant_blocks_per_sm(int variant, int M, int groups, int* blocks);
 
 // Launchers: `grid` CTAs of variant_threads(variant) threads on `stream`.
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
+// sched: the clip threshold is the running scheduled step's (st->cur_max_norm), not max_norm.
 cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm,
-                              int clip, cudaStream_t s);
+                              int clip, bool sched, cudaStream_t s);
 // One CTA: *out = sum of partials[0 .. nparts) in a fixed order.
 cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s);
-cudaError_t launch_adamw(const StepArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
+// sched: the AdamW scalars are the running scheduled step's (st->cur), not a.k.
+cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s);
+cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int grid, cudaStream_t s);
+// Scheduled steps. Install: counter = t, entry 0 serves step t + 1, `count` entries, the
+// schedule flag cleared. Begin (one thread, first launch of every scheduled step): advance
+// the counter and copy its entry into the status word, or raise kFlagSchedule.
+cudaError_t launch_schedule_install(Status* st, int64_t t, int64_t count, cudaStream_t s);
+cudaError_t launch_step_begin(Status* st, const ScheduleEntry* table, cudaStream_t s);
 // out[d] = bf16 parameter of unpadded index u0 + d, d < count, from the padded shards
 // (out needs only 2-byte alignment).
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb,

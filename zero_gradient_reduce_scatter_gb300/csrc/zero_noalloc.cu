@@ -166,7 +166,7 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     // Every partial the finalise kernel reads is written by this call's norm pass, and the
     // status word is written whole, so nothing in the scratch has to be cleared first.
     e = zg::launch_rs_norm(a, false, grid, s);
-    if (e == cudaSuccess) e = zg::launch_norm_final(status, partials, grid, max_grad_norm, 1, s);
+    if (e == cudaSuccess) e = zg::launch_norm_final(status, partials, grid, max_grad_norm, 1, false, s);
     if (e == cudaSuccess) {
         k_copy_result<<<1, 1, 0, s>>>(status, norm_out, scale_out);
         e = cudaGetLastError();
