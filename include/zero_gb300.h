@@ -262,6 +262,8 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * zero_sync_status returns ZERO_ERR_SCHEDULE. A new schedule clears the flag and continues
  * from the last step that ran.
  *
+ * A captured graph borrows the context's buffers like the calls it captured: it must not
+ * be replayed after zero_destroy or once those buffers are freed.
  * While a schedule is installed, the device counts the steps. zero_get_step synchronises
  * the device and reads that count. zero_step, zero_apply, zero_step_host*, zero_set_step
  * and zero_load_state return ZERO_ERR_SCHEDULE, as do the scheduled calls when no schedule

@@ -132,6 +132,9 @@ def test_null_or_unknown_context_rejected_without_touching_cuda(zg):
         assert lib.zero_params(ctx, ctypes.byref(p)) == -7
         assert lib.zero_sync_status(ctx) == -7
         assert lib.zero_set_timing(ctx, 1) == -7
+        assert lib.zero_set_schedule(ctx, ctypes.byref(h), 1, None) == -7
+        assert lib.zero_step_scheduled(ctx, None, 1, None) == -7
+        assert lib.zero_apply_scheduled(ctx, 1, None) == -7
 
 
 def _golden(name):
