@@ -32,6 +32,7 @@ KERNEL_SRC = os.path.join(ROOT, "zero_gradient_reduce_scatter_gb300", "csrc", "z
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+VENDOR_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for context beside the measured copy peak
 MIB = 1024 * 1024
 L2_BYTES = 129 * 1024 * 1024
 
@@ -495,6 +496,7 @@ def run_ours(args):
             "gbs_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9, 1),
             "frac_of_peak_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9
                                        / peak, 4),
+            "frac_of_vendor_hbm_alg": round(gbs_alg / VENDOR_HBM_GBS, 4),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -109,6 +109,33 @@ def test_save_reshard_resume_matches_oracle(tmp_path):
     assert np.array_equal(u16(C.params()), full)
 
 
+@pytest.mark.parametrize("stage,gather,groups", [(1, "fused", 1), (3, "shards", 1), (2, "fused", 2)])
+def test_resume_is_bitwise_continuation(stage, gather, groups):
+    """K steps straight == K1 steps, save, load into a fresh context of the same layout, K2 steps."""
+    dev = torch.device("cuda")
+    w = W.small_variant(W.config(3), NUMEL, M=8, stage=stage, steps=4, clip=0.05)
+    sig = W.sigmas(w)
+    mi = W.master_init(w, dev)
+
+    def make():
+        return zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, gather=gather, groups=groups)
+
+    A = make()
+    _steps(A, w, 4, sig, 0)
+    B = make()
+    _steps(B, w, 2, sig, 0)
+    saved = B.save_state()
+    C = make()
+    C.load_state(saved)
+    assert C.t == 2
+    _steps(C, w, 2, sig, 2)
+    torch.cuda.synchronize()
+    for name in ("master", "m", "v"):
+        assert torch.equal(getattr(A, name).view(torch.int32), getattr(C, name).view(torch.int32)), name
+    assert torch.equal(A.params().view(torch.int16), C.params().view(torch.int16))
+    assert A.t == C.t == 4
+
+
 def test_load_rejects_wrong_sizes():
     dev = torch.device("cuda")
     w = W.small_variant(W.config(2), (1000, 24), steps=1)
