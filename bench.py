@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
                     help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
                          "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+    ap.add_argument("--stream-form", default="auto", choices=["auto", "fused", "reduce-apply"],
+                    help="--mode stream: one fused pass per bucket (no clipping) or reduce-scatter of every "
+                         "bucket then one update (auto: fused when the workload does not clip)")
     ap.add_argument("--groups", type=int, default=1,
                     help="hybrid sharding: split the workload's M ranks into this many groups (state "
                          "sharded over M / groups ranks, replicated across groups)")
@@ -455,8 +458,17 @@ def run_ours(args):
         # while step k computes) and copies the bf16 parameters back to pinned host memory.
         # Two streams are involved, so the region is timed by the host clock between device
         # synchronisations.
-        host_grads = [g.cpu().pin_memory() for g in grads]
-        host_params = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+        # Host memory: every rank on the node pins its M replicas. When they would not fit,
+        # one pinned replica is the source of all M copies (the same bytes move every step).
+        local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+        rep_bytes = 2 * opt.sizes["npad"]
+        distinct = local_world * (w.M * rep_bytes + 2 * n) <= 0.6 * host_mem_available()
+        srcs = [torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
+                for _ in range(w.M if distinct else 1)]
+        for i, hs in enumerate(srcs):
+            hs.copy_(grads[i])
+        host_grads = srcs if distinct else srcs * w.M
+        host_params = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
         sets = [grads, opt.new_grad_buffers()]
         copy_stream = torch.cuda.Stream(device=device)
         for i in range(2):  # warm-up, both device sets
@@ -470,8 +482,10 @@ def run_ours(args):
         e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3, device)
         e2e = {"value": world * n * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "ms_per_step": e2e_ms / args.e2e_steps, "call": "zero_step_host_overlapped",
-               "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2}
-        del host_grads, host_params, sets
+               "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2,
+               "host_gradients": (f"{w.M} pinned replicas" if distinct else
+                                  f"one pinned replica copied to all {w.M} device buffers (host memory)")}
+        del host_grads, host_params, sets, srcs
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -546,6 +560,18 @@ def _timed_region(fn, steps, stream, dist, device):
     return max_over_ranks(dist, ev[0].elapsed_time(ev[-1]), device), clk, step_ms
 
 
+def host_mem_available() -> int:
+    """MemAvailable of this host in bytes (0 if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def l2_note(input_bytes):
     """How the timed steps relate to L2 (inputs larger than L2 need no flush between steps)."""
     if input_bytes > L2_BYTES:
@@ -562,9 +588,11 @@ def step_stats(ms, dist, device):
 
 
 def run_stream(args):
-    """ZeRO-2 per-bucket streaming: every bucket reduce-scattered (zero_reduce_bucket, in backward
-    order) from its own buffers, then one zero_apply; per step the same bytes as the
-    materialized clipped step, 2M + 34 per parameter."""
+    """ZeRO-2 per-bucket streaming, every bucket from its own buffers in backward order.
+    Without clipping (form "fused"): zero_step_bucket reduce-scatters and updates each bucket
+    in one pass, 2M + 26 bytes per parameter. With clipping (form "reduce-apply"): every bucket
+    reduce-scattered into the averaged gradient (zero_reduce_bucket), then one zero_apply,
+    the bytes of the materialized clipped step, 2M + 34 per parameter."""
     import torch
 
     import workloads as W
@@ -576,8 +604,14 @@ def run_stream(args):
     dist = dist_init(world, True)
     args.config = 1 if args.config == 4 and "--config" not in sys.argv else args.config
     w = workload(args)
+    form = args.stream_form
+    if form == "auto":
+        form = "fused" if w.clip is None else "reduce-apply"
+    if form == "fused" and w.clip is not None:
+        raise SystemExit("--stream-form fused needs a workload without clipping")
+    fused = form == "fused"
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
-                           ghat_buffer=True)
+                           ghat_buffer=not fused, groups=args.groups)
     full = opt.new_grad_buffers()
     sig = W.sigmas(w)
     for r in range(w.M):
@@ -589,6 +623,10 @@ def run_stream(args):
     stream = torch.cuda.current_stream()
 
     def step():
+        if fused:
+            for b in reversed(range(nb)):
+                opt.step_bucket(b, slices[b], h)
+            return
         for b in reversed(range(nb)):
             opt.reduce_bucket(b, slices[b])
         opt.apply(h)
@@ -605,10 +643,17 @@ def run_stream(args):
     n, lanes = w.N, opt.sizes["npad"]
     peak, kind = hbm_peak()
     ms_step = ms / args.steps
-    rs_ms = kt["rs_norm"][0] / args.steps
-    up_ms = kt["adamw"][0] / kt["adamw"][1]
-    dom = "adamw" if kt["adamw"][0] >= kt["rs_norm"][0] else "rs_norm"
-    dom_bytes, dom_ms = (30 * lanes, up_ms) if dom == "adamw" else ((2 * w.M + 4) * lanes, rs_ms)
+    if fused:  # per step: one fused launch per bucket
+        real_b = 2 * w.M + 26
+        dom, dom_name = "rs_adamw", "rs_adamw_plain (all buckets)"
+        dom_bytes, dom_ms = real_b * lanes, kt["rs_adamw"][0] / args.steps
+    else:
+        real_b = 2 * w.M + 34
+        rs_ms = kt["rs_norm"][0] / args.steps
+        up_ms = kt["adamw"][0] / kt["adamw"][1]
+        dom = "adamw" if kt["adamw"][0] >= kt["rs_norm"][0] else "rs_norm"
+        dom_name = "adamw" if dom == "adamw" else "rs_norm_write (all buckets)"
+        dom_bytes, dom_ms = (30 * lanes, up_ms) if dom == "adamw" else ((2 * w.M + 4) * lanes, rs_ms)
     if rank == 0:
         print(json.dumps({
             "metric": METRIC + " (ZeRO-2 per-bucket streaming)", "mode": "stream", "value": world * n * args.steps / (ms / 1e3),
@@ -617,12 +662,12 @@ def run_stream(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
-                       "bucket_bytes": w.bucket_bytes, "clip": w.clip},
+                       "bucket_bytes": w.bucket_bytes, "clip": w.clip, "form": form},
             "gbs_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9, 1),
             "frac_of_peak_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9 / peak, 4),
-            "real_bytes_per_param": 2 * w.M + 34,
-            "frac_of_peak_real": round((2 * w.M + 34) * n / (ms_step / 1e3) / 1e9 / peak, 4),
-            "roofline": {"bound": "hbm", "kernel": "adamw" if dom == "adamw" else "rs_norm_write (all buckets)",
+            "real_bytes_per_param": real_b,
+            "frac_of_peak_real": round(real_b * n / (ms_step / 1e3) / 1e9 / peak, 4),
+            "roofline": {"bound": "hbm", "kernel": dom_name,
                          "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4), "traffic": None,
                          "peak_source": kind, "kernel_share": {k: round(v[0] / ms, 4) for k, v in kt.items() if v[1]}},

@@ -215,6 +215,24 @@ int zero_step(zero_ctx* ctx, const void* const* grads, int stage, const zero_hyp
 int zero_reduce_bucket(zero_ctx* ctx, int64_t bucket, const void* const* grads_b, void* stream);
 int zero_apply(zero_ctx* ctx, int stage, const zero_hyper* hyper, void* stream);
 
+/* ZeRO-2 per-bucket step without clipping. Same sources as zero_reduce_bucket: each
+ * bucket's gradient is reduce-scattered as soon as it exists and then freed. Nothing global
+ * stands between a bucket's reduce-scatter and its owners' update when there is no norm to
+ * wait for. So this call does both for bucket `bucket` in one pass: reduce-scatter, AdamW
+ * on the owners' shards of that bucket, and the bucket's bf16 parameters (with
+ * ZERO_GATHER_SHARDS: the shards, then the bucket's all-gather into param_full). That moves
+ * 2M + 26 bytes per lane, with no averaged-gradient round trip and no ghat buffer.
+ * grads_b as in zero_reduce_bucket. Every bucket takes step t + 1. The step is complete,
+ * and t advances, when each bucket has been stepped once, in any order.
+ * hyper->clip must be 0: a clipped step needs every bucket's norm first, which is what
+ * zero_reduce_bucket + zero_apply do. A step must use one form. While some but not all
+ * buckets have been stepped, zero_step, zero_reduce_bucket and a second call for the same
+ * bucket return INVALID_ARG.
+ * Errors: BAD_CONTEXT, INVALID_ARG, MISALIGNED, STAGE, SCHEDULE (a schedule is installed),
+ * CUDA. */
+int zero_step_bucket(zero_ctx* ctx, int64_t bucket, const void* const* grads_b, int stage,
+                     const zero_hyper* hyper, void* stream);
+
 /* zero_step with host-resident data: enqueues the copy of each pinned host gradient
  * host_grads[r] (bf16 [npad]) into the device buffer dev_grads[r], the step, and the copy
  * of the full bf16 parameters into the pinned host buffer host_params (bf16 [n]), all on

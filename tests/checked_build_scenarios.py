@@ -103,6 +103,24 @@ def main():
         assert bf16_ulp_diff(u16(opt.params()), fullp) <= 1, "streaming"
     clean(opt, "streaming")
 
+    # ZeRO-2 fused per-bucket steps (no clipping), ZeRO-3 shards with the per-bucket gather
+    wf = W.small_variant(W.config(1), (70000, 5000, 301, 69999), bucket_bytes=120000, steps=2, stage=3)
+    optf = zg.ZeroOptimizer(wf.numel, wf.M, wf.stage, W.master_init(wf, dev), bucket_bytes=wf.bucket_bytes,
+                            gather="shards")
+    pf = O.plan(wf.numel, wf.M, wf.bucket_bytes)
+    stf = O.init_state(pf, wf.stage, W.master_init(wf, dev).cpu().numpy())
+    hf, ohf = make_hyper(wf)
+    for k in range(wf.steps):
+        g = optf.new_grad_buffers()
+        for r in range(wf.M):
+            W.fill_grads(wf, r, k, g[r], optf.tensor_offsets)
+        for b in reversed(range(len(optf.buckets))):
+            off = optf.buckets[b][0]
+            optf.step_bucket(b, [x[off:off + optf.bucket_lanes(b)].clone() for x in g], hf)
+        fullp, _, _, _ = O.zero_step(pf, stf, [u16(x) for x in g], ohf)
+        assert np.array_equal(u16(optf.params()), fullp), "fused per-bucket steps"
+    clean(optf, "fused per-bucket steps")
+
     # save / reshard / load
     saved = opt.save_state()
     w2 = W.small_variant(ws, ws.numel, M=5, stage=3, bucket_bytes=0)

@@ -2,9 +2,11 @@
 
 ZeRO-2 streaming ("CS336 2026 Lecture 8" Slide 23; "并行训练优化、MoE扩展与系统瓶颈" 2.2.4):
 each bucket is reduce-scattered as soon as its gradients exist (here in backward order, from
-short-lived per-bucket buffers), then one zero_apply finishes the step. The result must match
-the oracle's monolithic step: the averaged gradient bit for bit, the state within the
-tolerances (bit-identical whenever the clip scale rounds the same).
+short-lived per-bucket buffers). With clipping, one zero_apply finishes the step once every
+bucket's norm is in. The result must match the oracle's monolithic step: the averaged
+gradient bit for bit, the state within the tolerances (bit-identical whenever the clip scale
+rounds the same). Without clipping, zero_step_bucket updates each bucket in the same pass,
+and the result must match bit for bit.
 
 ZeRO-3 per-module gather with prefetch (Lecture 8 Slides 24-26; "CS231n Lecture 11" 4.3):
 buckets gathered just in time into transient buffers, the next one on a side stream.
@@ -70,6 +72,63 @@ def test_bucket_streaming_matches_monolithic_oracle(clip):
         assert bf16_ulp_diff(u16(opt.params()), fullp) <= 1
         for name, buf in (("master", opt.master), ("mom", opt.m), ("var", opt.v)):
             assert state_errors(f32(buf), O.flat_state(p, st, name)) <= 1.0, name
+
+
+@pytest.mark.parametrize("stage,gather,groups", [(2, "fused", 1), (3, "shards", 1), (1, "fused", 1),
+                                                  (2, "fused", 2)])
+def test_fused_bucket_steps_match_monolithic_oracle(stage, gather, groups):
+    """Without clipping each bucket is reduce-scattered and updated as soon as its gradients
+    exist (backward order, short-lived buffers); the result equals the oracle's monolithic
+    step bit for bit."""
+    w = W.small_variant(W.config(1), gpt_like(100, 3), bucket_bytes=150_000, steps=3, stage=stage)
+    assert w.clip is None
+    dev = torch.device("cuda")
+    mi = W.master_init(w, dev)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, gather=gather, groups=groups)
+    nb = len(opt.buckets)
+    assert nb >= 5
+    p = O.plan(w.numel, w.M // groups, w.bucket_bytes)
+    st = O.init_state(p, w.stage, f32(mi), groups=groups)
+    h, oh = make_hyper(w)
+    sig = W.sigmas(w)
+    for k in range(w.steps):
+        full = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, full[r], opt.tensor_offsets, sig)
+        for i, b in enumerate(reversed(range(nb))):
+            off = opt.buckets[b][0]
+            bufs = [g[off:off + opt.bucket_lanes(b)].clone() for g in full]
+            opt.step_bucket(b, bufs, h)
+            del bufs  # freed as soon as the bucket is done
+            assert opt.t == (k + 1 if i == nb - 1 else k)
+        fullp, _, _, rc = O.zero_step(p, st, [u16(g) for g in full], oh)
+        assert rc == 0 and opt.sync_status() == 0
+        assert np.array_equal(u16(opt.params()), fullp)
+        for name, buf in (("master", opt.master), ("mom", opt.m), ("var", opt.v)):
+            assert np.array_equal(f32(buf).view(np.uint32), O.flat_state(p, st, name).view(np.uint32)), name
+
+
+def test_fused_bucket_steps_refusals():
+    w = W.small_variant(W.config(1), (3000, 3000, 3000), bucket_bytes=6000, steps=1)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")),
+                           bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+    h, _ = make_hyper(w)
+    hc = zg.Hyper(lr=w.lr, clip=True, max_grad_norm=1.0)
+    assert len(opt.buckets) == 3
+    with pytest.raises(zg.ZeroError):  # clipping needs the norm of every bucket first
+        opt.step_bucket(0, opt.new_bucket_grad_buffers(0), hc)
+    opt.step_bucket(2, opt.new_bucket_grad_buffers(2), h)
+    for call in (lambda: opt.step_bucket(2, opt.new_bucket_grad_buffers(2), h),  # twice in one step
+                 lambda: opt.reduce_bucket(0, opt.new_bucket_grad_buffers(0)),   # the other form
+                 lambda: opt.step(opt.new_grad_buffers(), h)):                   # the whole step
+        with pytest.raises(zg.ZeroError) as e:
+            call()
+        assert e.value.code == -1
+    opt.step_bucket(0, opt.new_bucket_grad_buffers(0), h)
+    opt.step_bucket(1, opt.new_bucket_grad_buffers(1), h)
+    assert opt.t == 1 and opt.sync_status() == 0
+    opt.step(opt.new_grad_buffers(), h)  # a whole step again
+    assert opt.t == 2
 
 
 def test_apply_requires_every_bucket():

@@ -100,6 +100,7 @@ SIGNATURES = {
     "zero_step_host_overlapped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P, _P, _P]),
     "zero_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
     "zero_apply": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
+    "zero_step_bucket": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_set_schedule": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
     "zero_step_scheduled": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
     "zero_apply_scheduled": (ctypes.c_int, [_P, ctypes.c_int, _P]),
@@ -299,16 +300,26 @@ class ZeroOptimizer:
             raise ValueError(f"tensor {i} is not in bucket {bucket}")
         return bucket_buf[o:o + self.numel[i]]
 
-    def reduce_bucket(self, bucket: int, grads_b, stream=None):
+    def _bucket_ptrs(self, bucket: int, grads_b):
         if len(grads_b) != self.M:
             raise ValueError(f"expected {self.M} bucket gradient buffers")
         lanes = self.bucket_lanes(bucket)
         for g in grads_b:
             if not (g.is_cuda and g.dtype == torch.bfloat16 and g.is_contiguous() and g.numel() >= lanes):
                 raise ValueError("bucket gradients must be contiguous CUDA bf16 tensors of M * S_b lanes")
-        ptrs = (ctypes.c_void_p * self.M)(*[g.data_ptr() for g in grads_b])
+        return (ctypes.c_void_p * self.M)(*[g.data_ptr() for g in grads_b])
+
+    def reduce_bucket(self, bucket: int, grads_b, stream=None):
+        ptrs = self._bucket_ptrs(bucket, grads_b)
         _check(_lib().zero_reduce_bucket(self._ctx, bucket, ctypes.cast(ptrs, _P), _stream_handle(stream)),
                "zero_reduce_bucket")
+
+    def step_bucket(self, bucket: int, grads_b, hyper: Hyper, stream=None):
+        """ZeRO-2 without clipping: reduce-scatter and update bucket `bucket` in one pass; the
+        step completes (t advances) once every bucket has been stepped."""
+        ptrs = self._bucket_ptrs(bucket, grads_b)
+        _check(_lib().zero_step_bucket(self._ctx, bucket, ctypes.cast(ptrs, _P), self.stage, ctypes.byref(hyper),
+                                       _stream_handle(stream)), "zero_step_bucket")
 
     def apply(self, hyper: Hyper, stream=None):
         _check(_lib().zero_apply(self._ctx, self.stage, ctypes.byref(hyper), _stream_handle(stream)), "zero_apply")

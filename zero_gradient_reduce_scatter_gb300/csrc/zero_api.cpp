@@ -42,6 +42,9 @@ struct zero_ctx {
     // per-bucket streaming (zero_reduce_bucket / zero_apply)
     double* bucket_sums;          // device: one fp64 sum of squares per bucket
     std::vector<char> reduced;    // host: buckets reduced since the last zero_apply
+    int64_t n_reduced = 0;
+    std::vector<char> bucket_done;  // host: buckets updated by zero_step_bucket in this step
+    int64_t n_bucket_done = 0;
     // launch shapes, per kernel variant (0 = not computed yet), and an optional cap
     int grid[zg::kNumVariants];
     int max_ctas;
@@ -389,6 +392,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->bucket_sums = (double*)(scratch + zg::scratch_bucket_sums((int64_t)L.buckets.size()));
     c->dev_sched = (zg::ScheduleEntry*)(scratch + zg::scratch_schedule((int64_t)L.buckets.size()));
     c->reduced.assign(L.buckets.size(), 0);
+    c->bucket_done.assign(L.buckets.size(), 0);
     c->t = 0;
     c->last_clip = 0;
     c->last_stream = (cudaStream_t)stream;
@@ -499,6 +503,7 @@ static int launch_step_begin(zero_ctx* c, cudaStream_t s) {
 int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper* h, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (c->n_reduced || c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     int rc = check_hyper(h);
     if (rc) return rc;
@@ -519,6 +524,7 @@ int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper
 int zero_step_scheduled(zero_ctx* c, const void* const* grads, int stage, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (c->n_reduced || c->n_bucket_done) return ZERO_ERR_INVALID_ARG;
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     int rc = check_grads(c, grads);
     if (rc) return rc;
@@ -536,6 +542,7 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     const int64_t nb = (int64_t)c->buckets.size();
     if (bucket < 0 || bucket >= nb || !grads_b) return ZERO_ERR_INVALID_ARG;
     if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    if (c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a zero_step_bucket step is in progress
     for (int r = 0; r < c->cfg.M; ++r) {
         if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
         if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
@@ -561,7 +568,60 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
         err = zg::launch_sum_partials(c->partials, g1, c->bucket_sums + bucket, s);
     }
     if (err != cudaSuccess) return cuda_fail(err);
+    if (!c->reduced[(size_t)bucket]) c->n_reduced += 1;
     c->reduced[(size_t)bucket] = 1;
+    return ZERO_OK;
+}
+
+int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, const zero_hyper* h,
+                     void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    const int64_t nb = (int64_t)c->buckets.size();
+    // clipping needs every bucket's norm before any update: zero_reduce_bucket + zero_apply
+    if (h->clip || bucket < 0 || bucket >= nb || !grads_b) return ZERO_ERR_INVALID_ARG;
+    if (c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < c->cfg.M; ++r) {
+        if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
+        if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
+    }
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const zg::Bucket& e = c->buckets[(size_t)bucket];
+    zg::StepArgs a = base_args(c);
+    // The fused kernel addresses gradients by absolute lane: rebase each bucket buffer so that
+    // lane o of the bucket lands on grads_b[r][o - off] (address arithmetic only; the kernel
+    // touches lanes [off, end) alone).
+    for (int r = 0; r < c->cfg.M; ++r)
+        a.grads[r] = (const uint16_t*)((uintptr_t)grads_b[r] - (uintptr_t)(2 * e.off));
+    a.vbeg = e.off / 8;
+    a.vend = e.end / 8;
+    a.gext = e.end;
+    a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
+    const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
+    cudaError_t err;
+    {
+        Timed tm(c, ZERO_K_RS_ADAMW, s);
+        err = zg::launch_rs_adamw(a, false, false, g4, s);
+    }
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (c->cfg.gather == ZERO_GATHER_SHARDS) {  // the bucket's all-gather
+        rc = gather_range(c, e.uoff, e.n, (uint16_t*)c->bufs.param_full + e.uoff, s);
+        if (rc) return rc;
+    }
+    c->bucket_done[(size_t)bucket] = 1;
+    c->last_stream = s;
+    if (++c->n_bucket_done == nb) {  // the step is complete
+        std::fill(c->bucket_done.begin(), c->bucket_done.end(), 0);
+        c->n_bucket_done = 0;
+        c->t += 1;
+        c->last_clip = 0;
+        c->stepped = 1;
+    }
     return ZERO_OK;
 }
 
@@ -583,6 +643,7 @@ static int launch_apply(zero_ctx* c, const zg::StepArgs& a, int clip, double max
         if (rc) return rc;
     }
     std::fill(c->reduced.begin(), c->reduced.end(), 0);
+    c->n_reduced = 0;
     c->last_clip = clip;
     c->last_stream = s;
     c->stepped = 1;

@@ -65,9 +65,10 @@ struct StepArgs {
     const Bucket* buckets;
     int64_t nb;
     int64_t nvec;         // npad / 8: work items of 8 lanes (16 B of bf16)
-    int64_t vbeg, vend;   // vec range of the norm pass (the whole layout, or one bucket)
-    int64_t gbase;        // lane at which grads[r] starts (0, or the bucket's first lane)
-    int64_t gext;         // lanes in each gradient buffer (bounds checks)
+    int64_t vbeg, vend;   // vec range of the norm pass and the fused kernel (the layout, or one bucket)
+    int64_t gbase;        // norm pass: lane at which grads[r] starts (0, or the bucket's first lane)
+    int64_t gext;         // norm pass: lanes in each gradient buffer; fused kernel: end lane of
+                          // the gradients (which it addresses by absolute lane); bounds checks
     int64_t npad;         // padded lanes (bounds checks)
     int64_t n;            // unpadded parameters (bounds checks)
     int32_t M;

@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
 
 // ---------------------------------------------------------------------------------------
 // K4: fused reduce-scatter + AdamW + all-gather epilogue: the averaged gradient never
-// leaves registers. SCALE applies the clip scale computed by K2 (recompute form).
+// leaves registers. SCALE applies the clip scale computed by K2 (recompute form). Runs over
+// vecs [vbeg, vend): the whole layout, or one bucket (ZeRO-2 per-bucket steps).
 // ---------------------------------------------------------------------------------------
 template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false>
 __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
@@ -509,18 +510,18 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
     // clipped M = 4 kernel 1% faster than a register copy made at the start; equal elsewhere)
     const AdamConsts& k = SCHED ? a.status->cur : a.k;
     const int64_t stride = (int64_t)gridDim.x * kThreadsRsAdamw;
-    int64_t vi = (int64_t)blockIdx.x * kThreadsRsAdamw + threadIdx.x;
-    if (vi >= a.nvec) return;
+    int64_t vi = a.vbeg + (int64_t)blockIdx.x * kThreadsRsAdamw + threadIdx.x;
+    if (vi >= a.vend) return;
     Cursor c;
     c.init(a.buckets, a.nb, vi * 8);
-    for (; vi < a.nvec; vi += stride) {
+    for (; vi < a.vend; vi += stride) {
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
         if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
         // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
         load_state(a, o, p, m, v);
-        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // full-layout gradients start at lane 0
+        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // grads[r] is addressed by absolute lane
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
         adam_vec<SCALE>(gh, s, p, m, v, k);
