@@ -48,8 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
-                    help="step mode: capture one step (scalars from a device schedule) in a CUDA graph and "
-                         "time its replays; the roofline then covers the whole step")
+                    help="step and stream modes: capture one step (scalars from a device schedule) in a CUDA "
+                         "graph and time its replays; the roofline then covers the whole step")
     ap.add_argument("--cpu-procs", type=int, default=0,
                     help="oracle processes for the CPU baseline and the reference arm (0 = one per host core)")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
@@ -622,14 +622,35 @@ def run_stream(args):
                  clip=w.clip is not None, max_grad_norm=w.clip or 1.0)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def eager_step(scheduled=False):
         if fused:
             for b in reversed(range(nb)):
-                opt.step_bucket(b, slices[b], h)
+                if scheduled:
+                    opt.step_bucket_scheduled(b, slices[b])
+                else:
+                    opt.step_bucket(b, slices[b], h)
             return
         for b in reversed(range(nb)):
             opt.reduce_bucket(b, slices[b])
-        opt.apply(h)
+        if scheduled:
+            opt.apply_scheduled()
+        else:
+            opt.apply(h)
+
+    step, launches_per_step = eager_step, 0
+    if args.graph:  # one captured step (scalars from a device schedule), replayed
+        if args.warmup + args.steps + 1 > zg.ZERO_MAX_SCHEDULE:
+            raise SystemExit(f"--graph: at most {zg.ZERO_MAX_SCHEDULE - 1} warm-up and timed steps")
+        opt.set_schedule([h] * (args.warmup + args.steps + 1))
+        opt.set_timing(True)
+        opt.kernel_times()
+        eager_step(True)
+        launches_per_step = int(sum(c for _, c in opt.kernel_times().values()))
+        opt.set_timing(False)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            eager_step(True)
+        step = graph.replay
 
     for _ in range(args.warmup):
         step()
@@ -640,10 +661,16 @@ def run_stream(args):
     opt.kernel_times()
     ms, clk, step_ms = _timed_region(step, args.steps, stream, dist, device)
     kt = opt.kernel_times()
+    if args.graph and opt.sync_status() != 0:
+        raise SystemExit("a replayed step found no schedule entry")
     n, lanes = w.N, opt.sizes["npad"]
     peak, kind = hbm_peak()
     ms_step = ms / args.steps
-    if fused:  # per step: one fused launch per bucket
+    if args.graph:  # replays run no per-launch events: the roofline covers the whole step
+        real_b = 2 * w.M + (26 if fused else 34)
+        dom_name, dom_bytes, dom_ms = "whole step (CUDA graph replay)", real_b * w.N, ms_step
+        kt = {"all": (ms, launches_per_step * args.steps)}
+    elif fused:  # per step: one fused launch per bucket
         real_b = 2 * w.M + 26
         dom, dom_name = "rs_adamw", "rs_adamw_plain (all buckets)"
         dom_bytes, dom_ms = real_b * lanes, kt["rs_adamw"][0] / args.steps
@@ -662,7 +689,7 @@ def run_stream(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
-                       "bucket_bytes": w.bucket_bytes, "clip": w.clip, "form": form},
+                       "bucket_bytes": w.bucket_bytes, "clip": w.clip, "form": form, "cuda_graph": bool(args.graph)},
             "gbs_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9, 1),
             "frac_of_peak_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9 / peak, 4),
             "real_bytes_per_param": real_b,

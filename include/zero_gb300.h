@@ -271,8 +271,8 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * the next schedule when one ends). The call synchronises `stream` and must not be
  * captured.
  *
- * zero_step_scheduled and zero_apply_scheduled are zero_step and zero_apply without
- * hyper-parameters. Their first launch is one thread (ZERO_K_STEP_BEGIN). It advances a
+ * zero_step_scheduled, zero_apply_scheduled and zero_step_bucket_scheduled are zero_step,
+ * zero_apply and zero_step_bucket without hyper-parameters. Their first launch is one thread (ZERO_K_STEP_BEGIN). It advances a
  * step counter kept on the device and copies that step's entry into the status word, which
  * the update kernels read. They enqueue kernel launches only, so they can be captured, and
  * every replay is the next step. A step past the last entry changes no state and leaves
@@ -293,6 +293,10 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
 int zero_set_schedule(zero_ctx* ctx, const zero_hyper* per_step, int64_t count, void* stream);
 int zero_step_scheduled(zero_ctx* ctx, const void* const* grads, int stage, void* stream);
 int zero_apply_scheduled(zero_ctx* ctx, int stage, void* stream);
+/* zero_step_bucket with the scalars from the schedule (whose entries must not clip); the
+ * first bucket of each step also launches ZERO_K_STEP_BEGIN. */
+int zero_step_bucket_scheduled(zero_ctx* ctx, int64_t bucket, const void* const* grads_b, int stage,
+                               void* stream);
 
 /* Device pointer of the full bf16 parameters [n] (valid until the next step). */
 int zero_params(zero_ctx* ctx, void** full_bf16);

@@ -135,6 +135,8 @@ def test_null_or_unknown_context_rejected_without_touching_cuda(zg):
         assert lib.zero_set_schedule(ctx, ctypes.byref(h), 1, None) == -7
         assert lib.zero_step_scheduled(ctx, None, 1, None) == -7
         assert lib.zero_apply_scheduled(ctx, 1, None) == -7
+        assert lib.zero_step_bucket(ctx, 0, None, 1, ctypes.byref(h), None) == -7
+        assert lib.zero_step_bucket_scheduled(ctx, 0, None, 1, None) == -7
 
 
 def _golden(name):

@@ -101,6 +101,7 @@ SIGNATURES = {
     "zero_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
     "zero_apply": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_step_bucket": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
+    "zero_step_bucket_scheduled": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int, _P]),
     "zero_set_schedule": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
     "zero_step_scheduled": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
     "zero_apply_scheduled": (ctypes.c_int, [_P, ctypes.c_int, _P]),
@@ -339,6 +340,12 @@ class ZeroOptimizer:
         ptrs = self._ptrs(grads)
         _check(_lib().zero_step_scheduled(self._ctx, ctypes.cast(ptrs, _P), self.stage, _stream_handle(stream)),
                "zero_step_scheduled")
+
+    def step_bucket_scheduled(self, bucket: int, grads_b, stream=None):
+        """step_bucket() with this step's hyper-parameters taken from the device schedule."""
+        ptrs = self._bucket_ptrs(bucket, grads_b)
+        _check(_lib().zero_step_bucket_scheduled(self._ctx, bucket, ctypes.cast(ptrs, _P), self.stage,
+                                                 _stream_handle(stream)), "zero_step_bucket_scheduled")
 
     def apply_scheduled(self, stream=None):
         """apply() with this step's hyper-parameters taken from the device schedule."""

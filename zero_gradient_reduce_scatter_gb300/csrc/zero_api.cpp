@@ -573,24 +573,10 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     return ZERO_OK;
 }
 
-int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, const zero_hyper* h,
-                     void* stream) {
-    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
-    if (c->sched_active) return ZERO_ERR_SCHEDULE;
-    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
-    int rc = check_hyper(h);
-    if (rc) return rc;
-    const int64_t nb = (int64_t)c->buckets.size();
-    // clipping needs every bucket's norm before any update: zero_reduce_bucket + zero_apply
-    if (h->clip || bucket < 0 || bucket >= nb || !grads_b) return ZERO_ERR_INVALID_ARG;
-    if (c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
-    for (int r = 0; r < c->cfg.M; ++r) {
-        if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
-        if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
-    }
-    DeviceGuard guard(c->device);
-    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
-    cudaStream_t s = (cudaStream_t)stream;
+// One bucket of a ZeRO-2 fused per-bucket step (zero_step_bucket[_scheduled]).
+static int step_one_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, const zero_hyper* h,
+                           cudaStream_t s) {
+    const bool sched = h == nullptr;
     const zg::Bucket& e = c->buckets[(size_t)bucket];
     zg::StepArgs a = base_args(c);
     // The fused kernel addresses gradients by absolute lane: rebase each bucket buffer so that
@@ -601,12 +587,14 @@ int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, in
     a.vbeg = e.off / 8;
     a.vend = e.end / 8;
     a.gext = e.end;
-    a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
+    if (!sched) a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
+    int rc;
+    if (sched && c->n_bucket_done == 0 && (rc = launch_step_begin(c, s))) return rc;  // once per step
     const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
     cudaError_t err;
     {
         Timed tm(c, ZERO_K_RS_ADAMW, s);
-        err = zg::launch_rs_adamw(a, false, false, g4, s);
+        err = zg::launch_rs_adamw(a, false, sched, g4, s);
     }
     if (err != cudaSuccess) return cuda_fail(err);
     if (c->cfg.gather == ZERO_GATHER_SHARDS) {  // the bucket's all-gather
@@ -615,14 +603,50 @@ int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, in
     }
     c->bucket_done[(size_t)bucket] = 1;
     c->last_stream = s;
-    if (++c->n_bucket_done == nb) {  // the step is complete
+    if (++c->n_bucket_done == (int64_t)c->buckets.size()) {  // the step is complete
         std::fill(c->bucket_done.begin(), c->bucket_done.end(), 0);
         c->n_bucket_done = 0;
-        c->t += 1;
+        if (!sched) c->t += 1;
         c->last_clip = 0;
         c->stepped = 1;
     }
     return ZERO_OK;
+}
+
+static int check_step_bucket(const zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage) {
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    if (bucket < 0 || bucket >= (int64_t)c->buckets.size() || !grads_b) return ZERO_ERR_INVALID_ARG;
+    if (c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < c->cfg.M; ++r) {
+        if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
+        if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
+    }
+    return ZERO_OK;
+}
+
+int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, const zero_hyper* h,
+                     void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->sched_active) return ZERO_ERR_SCHEDULE;
+    int rc = check_hyper(h);
+    if (rc) return rc;
+    // clipping needs every bucket's norm before any update: zero_reduce_bucket + zero_apply
+    if (h->clip) return ZERO_ERR_INVALID_ARG;
+    if ((rc = check_step_bucket(c, bucket, grads_b, stage))) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    return step_one_bucket(c, bucket, grads_b, h, (cudaStream_t)stream);
+}
+
+int zero_step_bucket_scheduled(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, void* stream) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!c->sched_active) return ZERO_ERR_SCHEDULE;
+    if (c->sched_clip) return ZERO_ERR_INVALID_ARG;
+    int rc = check_step_bucket(c, bucket, grads_b, stage);
+    if (rc) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    return step_one_bucket(c, bucket, grads_b, nullptr, (cudaStream_t)stream);
 }
 
 // The rest of a streamed step once every bucket is reduced: norm (+ clip), AdamW, all-gather.
