@@ -6,7 +6,7 @@ fp32 shard, all-gather of the bf16 parameters. Default workload: the 4B dense-tr
 parameter set (4,092,982,400 params, M = 4, ZeRO-3, clip 1.0).
 
 Prints ONE JSON line (rank 0). Usage:
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 0-4] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload tiny|gpt2s|1p3b|ragged|4b] [--impl ours|reference]
 Multi-GPU: launched by torchrun, one process per GPU; every rank runs its own emulated job
 (weak scaling, no data-path collective); the barrier and the max-over-ranks timing use
 torch.distributed.
@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--workload", default=None, choices=["tiny", "gpt2s", "1p3b", "ragged", "4b"],
+                    help="default: 4b (the 4B dense set) for --mode step and gather, gpt2s for --mode stream")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
@@ -72,7 +73,7 @@ def parse():
 
 def workload(args):
     import workloads as W
-    w = W.config(args.config)
+    w = W.workload(args.workload or "4b")
     if args.max_params and args.max_params < w.N:
         keep, total = [], 0
         for n in w.numel:
@@ -439,7 +440,7 @@ def run_ours(args):
         variant = {"rs_adamw": "rs_adamw_scaled" if clip and ghat_mode != "materialize" else "rs_adamw_plain",
                    "adamw": "adamw", "rs_norm": "rs_norm_write" if ghat_mode == "materialize" else "rs_norm_only",
                    "gather": "gather", "norm_final": "norm_final"}[dom]
-        workload_key = f"config{args.config}" + (f"-max{args.max_params}" if args.max_params else "")
+        workload_key = (args.workload or "4b") + (f"-max{args.max_params}" if args.max_params else "")
         traffic = ncu_traffic(variant, workload_key)
         roofline = {"bound": "hbm", "kernel": variant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_source,
@@ -602,7 +603,7 @@ def run_stream(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = dist_init(world, True)
-    args.config = 1 if args.config == 4 and "--config" not in sys.argv else args.config
+    args.workload = args.workload or "gpt2s"
     w = workload(args)
     form = args.stream_form
     if form == "auto":

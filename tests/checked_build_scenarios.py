@@ -40,11 +40,11 @@ def main():
     assert zg._lib().zero_checked_build() == 1, "not the checked library"
     dev = torch.device("cuda")
 
-    w = W.small_variant(W.config(1), W.ragged_numel(60, 50, 4000, 11), bucket_bytes=9000, steps=2, clip=1.0)
+    w = W.small_variant(W.workload("gpt2s"), W.ragged_numel(60, 50, 4000, 11), bucket_bytes=9000, steps=2, clip=1.0)
     for mode in ("materialize", "recompute"):
         exact(run_elementwise(w, ghat_mode=mode, ghat_buffer=True), f"fused misaligned stores ({mode})")
 
-    w = W.small_variant(W.config(3), W.ragged_numel(40, 100, 6000, 3), bucket_bytes=15000, steps=2)
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(40, 100, 6000, 3), bucket_bytes=15000, steps=2)
     out = run_elementwise(w, gather="shards")
     exact(out, "shards + gather")
     opt = out["opt"]
@@ -60,15 +60,15 @@ def main():
     clean(opt, "per-bucket gathers")
 
     for M in (3, 64):
-        exact(run_elementwise(W.small_variant(W.config(3), (3001, 17, 1), M=M, steps=2), gather="shards"),
+        exact(run_elementwise(W.small_variant(W.workload("ragged"), (3001, 17, 1), M=M, steps=2), gather="shards"),
               f"generic M={M}")
-    exact(run_elementwise(W.small_variant(W.config(3), (3,), steps=2), gather="shards"), "3 lanes, 16 ranks")
+    exact(run_elementwise(W.small_variant(W.workload("ragged"), (3,), steps=2), gather="shards"), "3 lanes, 16 ranks")
 
-    wg = W.small_variant(W.config(3), W.ragged_numel(30, 200, 5000, 23), M=8, stage=3, steps=2)
+    wg = W.small_variant(W.workload("ragged"), W.ragged_numel(30, 200, 5000, 23), M=8, stage=3, steps=2)
     exact(run_elementwise(wg, gather="shards", groups=2, ghat_mode="materialize", ghat_buffer=True), "hybrid")
 
     # a scheduled step captured in a CUDA graph, replayed past its schedule
-    wq = W.small_variant(W.config(3), W.ragged_numel(20, 300, 5000, 29), M=8, steps=1, clip=0.02)
+    wq = W.small_variant(W.workload("ragged"), W.ragged_numel(20, 300, 5000, 29), M=8, steps=1, clip=0.02)
     opt = zg.ZeroOptimizer(wq.numel, wq.M, wq.stage, W.master_init(wq, dev), groups=2, gather="shards")
     gq = opt.new_grad_buffers()
     for r in range(wq.M):
@@ -85,7 +85,7 @@ def main():
     assert opt.sync_status() == zg.ZERO_ERR_SCHEDULE and opt.check_report()[0] == 0 and opt.t == 2
 
     # ZeRO-2 streaming against the oracle's monolithic step
-    ws = W.small_variant(W.config(1), (70000, 5000, 300, 70000), bucket_bytes=120000, steps=2, clip=1.0)
+    ws = W.small_variant(W.workload("gpt2s"), (70000, 5000, 300, 70000), bucket_bytes=120000, steps=2, clip=1.0)
     opt = zg.ZeroOptimizer(ws.numel, ws.M, ws.stage, W.master_init(ws, dev), bucket_bytes=ws.bucket_bytes,
                            ghat_buffer=True)
     p = O.plan(ws.numel, ws.M, ws.bucket_bytes)
@@ -104,7 +104,7 @@ def main():
     clean(opt, "streaming")
 
     # ZeRO-2 fused per-bucket steps (no clipping), ZeRO-3 shards with the per-bucket gather
-    wf = W.small_variant(W.config(1), (70000, 5000, 301, 69999), bucket_bytes=120000, steps=2, stage=3)
+    wf = W.small_variant(W.workload("gpt2s"), (70000, 5000, 301, 69999), bucket_bytes=120000, steps=2, stage=3)
     optf = zg.ZeroOptimizer(wf.numel, wf.M, wf.stage, W.master_init(wf, dev), bucket_bytes=wf.bucket_bytes,
                             gather="shards")
     pf = O.plan(wf.numel, wf.M, wf.bucket_bytes)

@@ -83,17 +83,17 @@ def test_planner_matches_oracle_random(zg):
         _cmp_with_oracle(zg, numel, M, int(rng.integers(1, 4)), bb)
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
-def test_planner_matches_oracle_on_workloads(zg, idx):
-    w = W.config(idx)
+@pytest.mark.parametrize("key", ["tiny", "gpt2s", "1p3b", "ragged", "4b"])
+def test_planner_matches_oracle_on_workloads(zg, key):
+    w = W.workload(key)
     _cmp_with_oracle(zg, list(w.numel), w.M, w.stage, w.bucket_bytes)
 
 
 def test_workload_sizes(zg):
-    assert W.config(1).N == 123_570_432 and zg.plan(W.config(1).numel, 8, 2, 25 * 1024 * 1024)["n_buckets"] > 1
-    assert W.config(2).N == 1_310_885_888
-    assert W.config(4).N == 4_092_982_400
-    n3 = np.array(W.config(3).numel)
+    assert W.workload("gpt2s").N == 123_570_432 and zg.plan(W.workload("gpt2s").numel, 8, 2, 25 * 1024 * 1024)["n_buckets"] > 1
+    assert W.workload("1p3b").N == 1_310_885_888
+    assert W.workload("4b").N == 4_092_982_400
+    n3 = np.array(W.workload("ragged").numel)
     assert len(n3) == 2000 and n3.min() >= 1024 and n3.max() <= 2 ** 22 + 64
     assert (n3 % 2 == 1).mean() >= 0.25
 

@@ -56,7 +56,7 @@ def _oracle_continue(w, state, hosts):
 
 def test_save_reshard_resume_matches_oracle(tmp_path):
     dev = torch.device("cuda")
-    wA = W.small_variant(W.config(3), NUMEL, M=4, steps=2)                  # ZeRO-3, clip, M = 4
+    wA = W.small_variant(W.workload("ragged"), NUMEL, M=4, steps=2)                  # ZeRO-3, clip, M = 4
     sig = W.sigmas(wA)
     A = zg.ZeroOptimizer(wA.numel, wA.M, wA.stage, W.master_init(wA, dev), gather="shards")
     hostsA = _steps(A, wA, 2, sig, 0)
@@ -74,7 +74,7 @@ def test_save_reshard_resume_matches_oracle(tmp_path):
         assert np.array_equal(f32(saved[k]).view(np.uint32), O.flat_state(pA, stA, n)[uA >= 0].view(np.uint32)), k
 
     # reshard into M = 6, ZeRO-2, small buckets (generic-M kernels, several buckets)
-    wB = W.small_variant(W.config(3), NUMEL, M=6, stage=2, bucket_bytes=30000, steps=2)
+    wB = W.small_variant(W.workload("ragged"), NUMEL, M=6, stage=2, bucket_bytes=30000, steps=2)
     B = zg.ZeroOptimizer(wB.numel, wB.M, wB.stage, W.master_init(wB, dev), bucket_bytes=wB.bucket_bytes)
     B.load_state(saved)
     assert B.t == 2
@@ -95,7 +95,7 @@ def test_save_reshard_resume_matches_oracle(tmp_path):
     # through a checkpoint file into M = 8, ZeRO-1
     path = tmp_path / "ckpt.pt"
     torch.save(B.state_dict(), path)
-    wC = W.small_variant(W.config(3), NUMEL, M=8, stage=1, steps=1)
+    wC = W.small_variant(W.workload("ragged"), NUMEL, M=8, stage=1, steps=1)
     C = zg.ZeroOptimizer(wC.numel, wC.M, wC.stage, W.master_init(wC, dev))
     C.load_state_dict(torch.load(path))
     assert C.t == 4
@@ -113,7 +113,7 @@ def test_save_reshard_resume_matches_oracle(tmp_path):
 def test_resume_is_bitwise_continuation(stage, gather, groups):
     """K steps straight == K1 steps, save, load into a fresh context of the same layout, K2 steps."""
     dev = torch.device("cuda")
-    w = W.small_variant(W.config(3), NUMEL, M=8, stage=stage, steps=4, clip=0.05)
+    w = W.small_variant(W.workload("ragged"), NUMEL, M=8, stage=stage, steps=4, clip=0.05)
     sig = W.sigmas(w)
     mi = W.master_init(w, dev)
 
@@ -138,7 +138,7 @@ def test_resume_is_bitwise_continuation(stage, gather, groups):
 
 def test_load_rejects_wrong_sizes():
     dev = torch.device("cuda")
-    w = W.small_variant(W.config(2), (1000, 24), steps=1)
+    w = W.small_variant(W.workload("1p3b"), (1000, 24), steps=1)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
     with pytest.raises(ValueError):
         opt.load_state({"master": torch.zeros(10, device=dev), "t": 0})

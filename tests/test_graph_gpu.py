@@ -65,16 +65,16 @@ def check_against(opt, twin, p, st, full, norm, clip, exact_twin=True):
 
 CASES = {
     # plain fused kernel (no clip), ZeRO-2, several buckets
-    "fused-noclip-M8": (lambda: W.small_variant(W.config(1), W.ragged_numel(30, 100, 9000, 5), bucket_bytes=40000),
+    "fused-noclip-M8": (lambda: W.small_variant(W.workload("gpt2s"), W.ragged_numel(30, 100, 9000, 5), bucket_bytes=40000),
                         dict(), 1),
     # clip, M = 4: norm pass + scaled fused kernel; ZeRO-3 with the separate all-gather
-    "recompute-M4-shards": (lambda: W.small_variant(W.config(4), W.ragged_numel(25, 200, 12000, 9), clip=0.02),
+    "recompute-M4-shards": (lambda: W.small_variant(W.workload("4b"), W.ragged_numel(25, 200, 12000, 9), clip=0.02),
                             dict(gather="shards"), 1),
     # clip, M = 16: norm pass writing the average + AdamW from it
-    "materialize-M16": (lambda: W.small_variant(W.config(3), W.ragged_numel(25, 200, 8000, 15), clip=0.02),
+    "materialize-M16": (lambda: W.small_variant(W.workload("ragged"), W.ragged_numel(25, 200, 8000, 15), clip=0.02),
                         dict(ghat_buffer=True), 1),
     # hybrid sharding, 2 groups of 4
-    "hybrid-2x4": (lambda: W.small_variant(W.config(3), W.ragged_numel(20, 300, 7000, 19), M=8, clip=0.02),
+    "hybrid-2x4": (lambda: W.small_variant(W.workload("ragged"), W.ragged_numel(20, 300, 7000, 19), M=8, clip=0.02),
                    dict(), 2),
 }
 
@@ -148,7 +148,7 @@ def test_captured_step_replays_match_zero_step_and_oracle(case):
 
 
 def test_scheduled_calls_without_schedule_are_refused():
-    w = W.small_variant(W.config(0), (5000,))
+    w = W.small_variant(W.workload("tiny"), (5000,))
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")))
     grads = opt.new_grad_buffers()
     with pytest.raises(zg.ZeroError) as e:
@@ -170,7 +170,7 @@ def test_scheduled_calls_without_schedule_are_refused():
 
 def test_captured_streaming_step_matches_oracle():
     """ZeRO-2: every bucket's reduce-scatter and the scheduled apply in one graph."""
-    w = W.small_variant(W.config(1), W.ragged_numel(40, 100, 6000, 27), bucket_bytes=30000, clip=1e-3)
+    w = W.small_variant(W.workload("gpt2s"), W.ragged_numel(40, 100, 6000, 27), bucket_bytes=30000, clip=1e-3)
     dev = torch.device("cuda")
     mi = W.master_init(w, dev)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
@@ -203,7 +203,7 @@ def test_captured_streaming_step_matches_oracle():
 def test_captured_fused_bucket_steps_match_oracle(gather):
     """ZeRO-2 without clipping: every bucket's fused reduce-scatter + update in one graph,
     replayed under an lr schedule; bit-identical to the oracle's monolithic step."""
-    w = W.small_variant(W.config(1), W.ragged_numel(40, 100, 6000, 31), bucket_bytes=30000, stage=3)
+    w = W.small_variant(W.workload("gpt2s"), W.ragged_numel(40, 100, 6000, 31), bucket_bytes=30000, stage=3)
     dev = torch.device("cuda")
     mi = W.master_init(w, dev)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, gather=gather)

@@ -78,11 +78,11 @@ def streamed_norm(p, grads, pinned):
     return math.sqrt(acc)
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_full_size_workload(idx):
-    w = W.config(idx)
+@pytest.mark.parametrize("key", ["gpt2s", "1p3b", "ragged", "4b"])
+def test_full_size_workload(key):
+    w = W.workload(key)
     dev = torch.device("cuda")
-    rng = np.random.default_rng(1000 + idx)
+    rng = np.random.default_rng(1000 + W.KEYS.index(key))
     mi = W.master_init(w, dev)
     # the launch configuration bench.py times: fused all-gather, automatic averaged-gradient mode
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, gather="fused")

@@ -45,12 +45,12 @@ def ragged(count, lo, hi, seed):
 # The five workloads' recipes at reduced sizes (and the tiny one at full size)
 # ------------------------------------------------------------------------------------------
 def test_tiny_workload_full_size():
-    out = run_elementwise(W.config(0))
+    out = run_elementwise(W.workload("tiny"))
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
 
 def test_gpt2_small_recipe_multi_bucket_stage2():
-    w = W.small_variant(W.config(1), gpt_like(100, 3), bucket_bytes=150_000, steps=4)
+    w = W.small_variant(W.workload("gpt2s"), gpt_like(100, 3), bucket_bytes=150_000, steps=4)
     p = O.plan(w.numel, w.M, w.bucket_bytes)
     assert p.nb >= 5
     out = run_elementwise(w)
@@ -60,7 +60,7 @@ def test_gpt2_small_recipe_multi_bucket_stage2():
 def test_ragged_multi_bucket_fused_epilogue_all_alignments():
     """Odd tensor sizes and small buckets: the unpadded start of the buckets falls on every
     alignment class of the fused all-gather stores (16-, 8-, 4- and 2-byte)."""
-    w = W.small_variant(W.config(1), ragged(60, 50, 4000, 11), bucket_bytes=9000, steps=3, clip=1.0)
+    w = W.small_variant(W.workload("gpt2s"), ragged(60, 50, 4000, 11), bucket_bytes=9000, steps=3, clip=1.0)
     p = O.plan(w.numel, w.M, w.bucket_bytes)
     shifts = {int(p.b_off[b] - sum(p.b_n[:b])) % 8 for b in range(p.nb)}
     assert 0 in shifts and 4 in shifts and (shifts & {2, 6}) and (shifts & {1, 3, 5, 7}), shifts
@@ -71,7 +71,7 @@ def test_ragged_multi_bucket_fused_epilogue_all_alignments():
 
 @pytest.mark.parametrize("ghat_mode", ["materialize", "recompute"])
 def test_dense_1p3b_recipe_clip_stage1(ghat_mode):
-    w = W.small_variant(W.config(2), gpt_like(128, 2, layernorm=False, vocab=2000), steps=3)
+    w = W.small_variant(W.workload("1p3b"), gpt_like(128, 2, layernorm=False, vocab=2000), steps=3)
     out = run_elementwise(w, ghat_mode=ghat_mode, ghat_buffer=True)
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
     if ghat_mode == "materialize":
@@ -84,13 +84,13 @@ def test_dense_1p3b_recipe_clip_stage1(ghat_mode):
 
 @pytest.mark.parametrize("gather", ["shards", "fused"])
 def test_ragged_recipe_stage3_m16(gather):
-    w = W.small_variant(W.config(3), ragged(150, 2 ** 10, 2 ** 15, 7), steps=3)
+    w = W.small_variant(W.workload("ragged"), ragged(150, 2 ** 10, 2 ** 15, 7), steps=3)
     out = run_elementwise(w, gather=gather)
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
 
 def test_dense_4b_recipe_stage3_m4():
-    w = W.small_variant(W.config(4), gpt_like(160, 2, layernorm=False, vocab=1500), steps=3)
+    w = W.small_variant(W.workload("4b"), gpt_like(160, 2, layernorm=False, vocab=1500), steps=3)
     out = run_elementwise(w)
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
@@ -102,26 +102,26 @@ def test_dense_4b_recipe_stage3_m4():
 def test_rank_counts_including_generic_kernel(M):
     """M outside {1,2,4,8,16} runs the generic rank loop; non-power-of-two M makes
     (float)(1/M) inexact, which both sides apply the same way."""
-    w = W.small_variant(W.config(3), (3001, 17, 8192, 1, 555), M=M, steps=2)
+    w = W.small_variant(W.workload("ragged"), (3001, 17, 8192, 1, 555), M=M, steps=2)
     out = run_elementwise(w, gather="shards")
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
 
 def test_fewer_params_than_ranks():
     """3 real lanes over 16 ranks: 15 owners hold only padding."""
-    w = W.small_variant(W.config(3), (3,), steps=3)
+    w = W.small_variant(W.workload("ragged"), (3,), steps=3)
     out = run_elementwise(w, gather="shards")
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
 
 def test_zero_size_and_unit_tensors():
-    w = W.small_variant(W.config(1), (0, 1, 0, 1, 2, 0, 5000, 1), bucket_bytes=40, steps=2)
+    w = W.small_variant(W.workload("gpt2s"), (0, 1, 0, 1, 2, 0, 5000, 1), bucket_bytes=40, steps=2)
     out = run_elementwise(w)
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
 
 
 def test_padding_garbage_is_ignored():
-    w = W.small_variant(W.config(4), (1001, 77, 3), steps=2)
+    w = W.small_variant(W.workload("4b"), (1001, 77, 3), steps=2)
     out = run_elementwise(w, garbage_in_padding=True)
     assert out["bf16_ulp"] == 0 and out["state_err"] == 0.0
     # padding lanes of the state stay exactly zero
@@ -132,8 +132,8 @@ def test_padding_garbage_is_ignored():
 
 
 def test_large_threshold_equals_no_clip():
-    w_clip = W.small_variant(W.config(2), (20000, 3000), clip=1e9, steps=2)
-    w_off = W.small_variant(W.config(2), (20000, 3000), clip=None, steps=2)
+    w_clip = W.small_variant(W.workload("1p3b"), (20000, 3000), clip=1e9, steps=2)
+    w_off = W.small_variant(W.workload("1p3b"), (20000, 3000), clip=None, steps=2)
     a = run_elementwise(w_clip)["opt"]
     b = run_elementwise(w_off)["opt"]
     assert a.last_norm()[1] == 1.0
@@ -141,7 +141,7 @@ def test_large_threshold_equals_no_clip():
 
 
 def test_nonfinite_gradient_skips_step_and_reports():
-    w = W.small_variant(W.config(4), (4096, 100), steps=1)
+    w = W.small_variant(W.workload("4b"), (4096, 100), steps=1)
     dev = torch.device("cuda")
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
     before = opt.master.clone()
@@ -161,7 +161,7 @@ def test_nonfinite_gradient_skips_step_and_reports():
 
 
 def test_deterministic_rerun():
-    w = W.small_variant(W.config(2), gpt_like(64, 2, layernorm=False, vocab=3000), steps=2)
+    w = W.small_variant(W.workload("1p3b"), gpt_like(64, 2, layernorm=False, vocab=3000), steps=2)
     a = run_elementwise(w)
     b = run_elementwise(w)
     assert a["opt"].last_norm() == b["opt"].last_norm()
@@ -169,7 +169,7 @@ def test_deterministic_rerun():
 
 
 def test_invalid_step_arguments_rejected_on_host():
-    w = W.small_variant(W.config(0), (4096,), steps=1)
+    w = W.small_variant(W.workload("tiny"), (4096,), steps=1)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")))
     grads = opt.new_grad_buffers()
     h, _ = make_hyper(w)
@@ -198,7 +198,7 @@ def test_invalid_step_arguments_rejected_on_host():
 # Other entry points: per-rank state, per-bucket gather, host-buffer step, step counter
 # ------------------------------------------------------------------------------------------
 def test_get_state_per_rank_matches_oracle_shards():
-    w = W.small_variant(W.config(2), (5000, 123, 9000), bucket_bytes=12000, steps=2)
+    w = W.small_variant(W.workload("1p3b"), (5000, 123, 9000), bucket_bytes=12000, steps=2)
     out = run_elementwise(w, ghat_mode="materialize", ghat_buffer=True)
     opt, st = out["opt"], out["oracle_state"]
     for r in range(w.M):
@@ -208,7 +208,7 @@ def test_get_state_per_rank_matches_oracle_shards():
 
 
 def test_gather_per_bucket_rebuilds_params():
-    w = W.small_variant(W.config(3), ragged(40, 100, 3000, 3), bucket_bytes=8000, steps=2)
+    w = W.small_variant(W.workload("ragged"), ragged(40, 100, 3000, 3), bucket_bytes=8000, steps=2)
     out = run_elementwise(w, gather="shards")
     opt, p = out["opt"], out["plan"]
     assert p.nb > 3
@@ -220,7 +220,7 @@ def test_gather_per_bucket_rebuilds_params():
 
 
 def test_step_from_host_buffers_equals_device_step():
-    w = W.small_variant(W.config(4), (70000, 13), steps=2)
+    w = W.small_variant(W.workload("4b"), (70000, 13), steps=2)
     dev = torch.device("cuda")
     a = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
     b = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
@@ -243,7 +243,7 @@ def test_overlapped_host_steps_equal_device_steps():
     """Four steps with different gradients, two alternating device buffer sets and no
     synchronisation between calls: each step's parameters (copied to their own pinned host
     buffer) equal those of the plain device path."""
-    w = W.small_variant(W.config(4), (300000, 77, 4099), steps=4)
+    w = W.small_variant(W.workload("4b"), (300000, 77, 4099), steps=4)
     dev = torch.device("cuda")
     a = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
     b = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
@@ -271,7 +271,7 @@ def test_overlapped_host_steps_equal_device_steps():
 
 def test_step_counter_and_resume():
     """K steps == K1 steps, save (state + t), restore into a fresh context, K2 steps."""
-    w = W.small_variant(W.config(2), (30000, 5000), steps=4)
+    w = W.small_variant(W.workload("1p3b"), (30000, 5000), steps=4)
     dev = torch.device("cuda")
     h, _ = make_hyper(w)
     sig = W.sigmas(w)
@@ -300,7 +300,7 @@ def test_step_counter_and_resume():
 
 
 def test_kernel_timing_counts_launches():
-    w = W.small_variant(W.config(2), (200000,), steps=1)
+    w = W.small_variant(W.workload("1p3b"), (200000,), steps=1)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")), ghat_buffer=True)
     grads = opt.new_grad_buffers()
     h, _ = make_hyper(w)
@@ -326,7 +326,7 @@ def _guarded(nbytes, dev):
 @pytest.mark.parametrize("gather,mode", [("shards", "materialize"), ("fused", "recompute"), ("fused", "materialize")])
 def test_guard_bands_untouched(gather, mode):
     import ctypes
-    w = W.small_variant(W.config(3), ragged(30, 100, 5000, 9), M=8, bucket_bytes=20000, steps=2)
+    w = W.small_variant(W.workload("ragged"), ragged(30, 100, 5000, 9), M=8, bucket_bytes=20000, steps=2)
     dev = torch.device("cuda")
     s = zg.plan(w.numel, w.M, w.stage, w.bucket_bytes, gather)
     toff, _ = zg.layout(w.numel, w.M, w.stage, w.bucket_bytes, gather)
@@ -374,7 +374,7 @@ def test_guard_bands_untouched(gather, mode):
     (2, 4, 3, "shards", 0, 1.0), (4, 2, 1, "fused", 40000, 1.0), (3, 2, 2, "fused", 0, None),
     (2, 8, 3, "fused", 0, 1.0), (8, 1, 1, "fused", 0, 1.0)])
 def test_hybrid_sharding_matches_oracle(G, K, stage, gather, bucket_bytes, clip):
-    w = W.small_variant(W.config(3), ragged(40, 200, 6000, 23), M=G * K, stage=stage,
+    w = W.small_variant(W.workload("ragged"), ragged(40, 200, 6000, 23), M=G * K, stage=stage,
                         bucket_bytes=bucket_bytes, clip=clip, steps=3)
     for mode in (("materialize", "recompute") if clip else ("auto",)):
         out = run_elementwise(w, gather=gather, groups=G, ghat_mode=mode, ghat_buffer=True)
@@ -386,7 +386,7 @@ def test_hybrid_sharding_matches_oracle(G, K, stage, gather, bucket_bytes, clip)
 # ------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("clip", [None, 1e-3])
 def test_results_do_not_depend_on_the_grid(clip):
-    w = W.small_variant(W.config(1), ragged(50, 100, 30000, 29), bucket_bytes=60000, steps=2, clip=clip)
+    w = W.small_variant(W.workload("gpt2s"), ragged(50, 100, 30000, 29), bucket_bytes=60000, steps=2, clip=clip)
     dev = torch.device("cuda")
     sig = W.sigmas(w)
     grads_per_step = []

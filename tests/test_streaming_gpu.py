@@ -40,7 +40,7 @@ def gpt_like(d, layers, vocab=1000):
 
 @pytest.mark.parametrize("clip", [None, 1e-3])
 def test_bucket_streaming_matches_monolithic_oracle(clip):
-    w = W.small_variant(W.config(1), gpt_like(100, 3), bucket_bytes=150_000, steps=3, clip=clip)
+    w = W.small_variant(W.workload("gpt2s"), gpt_like(100, 3), bucket_bytes=150_000, steps=3, clip=clip)
     dev = torch.device("cuda")
     mi = W.master_init(w, dev)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
@@ -80,7 +80,7 @@ def test_fused_bucket_steps_match_monolithic_oracle(stage, gather, groups):
     """Without clipping each bucket is reduce-scattered and updated as soon as its gradients
     exist (backward order, short-lived buffers); the result equals the oracle's monolithic
     step bit for bit."""
-    w = W.small_variant(W.config(1), gpt_like(100, 3), bucket_bytes=150_000, steps=3, stage=stage)
+    w = W.small_variant(W.workload("gpt2s"), gpt_like(100, 3), bucket_bytes=150_000, steps=3, stage=stage)
     assert w.clip is None
     dev = torch.device("cuda")
     mi = W.master_init(w, dev)
@@ -109,7 +109,7 @@ def test_fused_bucket_steps_match_monolithic_oracle(stage, gather, groups):
 
 
 def test_fused_bucket_steps_refusals():
-    w = W.small_variant(W.config(1), (3000, 3000, 3000), bucket_bytes=6000, steps=1)
+    w = W.small_variant(W.workload("gpt2s"), (3000, 3000, 3000), bucket_bytes=6000, steps=1)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")),
                            bucket_bytes=w.bucket_bytes, ghat_buffer=True)
     h, _ = make_hyper(w)
@@ -132,7 +132,7 @@ def test_fused_bucket_steps_refusals():
 
 
 def test_apply_requires_every_bucket():
-    w = W.small_variant(W.config(1), (3000, 3000, 3000), bucket_bytes=6000, steps=1)
+    w = W.small_variant(W.workload("gpt2s"), (3000, 3000, 3000), bucket_bytes=6000, steps=1)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")),
                            bucket_bytes=w.bucket_bytes, ghat_buffer=True)
     h, _ = make_hyper(w)
@@ -149,7 +149,7 @@ def test_apply_requires_every_bucket():
 
 @pytest.mark.parametrize("order", ["forward", "backward"])
 def test_prefetched_gather_per_bucket(order):
-    w = W.small_variant(W.config(3), W.ragged_numel(60, 100, 8000, 13), bucket_bytes=25000, steps=2)
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(60, 100, 8000, 13), bucket_bytes=25000, steps=2)
     dev = torch.device("cuda")
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
                            gather="shards")
@@ -174,7 +174,7 @@ def test_prefetched_gather_per_bucket(order):
 
 
 def test_gather_bucket_into_unaligned_buffer():
-    w = W.small_variant(W.config(3), W.ragged_numel(20, 300, 5000, 17), bucket_bytes=9000, steps=1)
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(20, 300, 5000, 17), bucket_bytes=9000, steps=1)
     dev = torch.device("cuda")
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
                            gather="shards")

@@ -37,7 +37,7 @@ def _table(opt):
 
 
 def test_noalloc_norm_matches_step_norm_on_two_calls():
-    w = W.small_variant(W.config(2), W.ragged_numel(80, 100, 20000, 5), bucket_bytes=60000, clip=1.0, steps=2)
+    w = W.small_variant(W.workload("1p3b"), W.ragged_numel(80, 100, 20000, 5), bucket_bytes=60000, clip=1.0, steps=2)
     dev = torch.device("cuda")
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes)
     assert len(opt.buckets) > 3

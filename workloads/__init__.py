@@ -102,32 +102,37 @@ def ragged_numel(count: int = 2000, lo: int = 2 ** 10, hi: int = 2 ** 22, seed: 
     return tuple(sizes)
 
 
-def config(idx: int) -> Workload:
-    """The five standard workloads (0: tiny; 1: GPT-2-small shaped; 2: 1.3B; 3: ragged; 4: 4B)."""
-    if idx == 0:
+KEYS = ("tiny", "gpt2s", "1p3b", "ragged", "4b")
+
+
+def workload(key: str) -> Workload:
+    """The five standard workloads, by short name: "tiny" (4096 params, M=2), "gpt2s"
+    (GPT-2-small shaped, M=8), "1p3b" (1.3B dense, M=8), "ragged" (2000 tensors, M=16),
+    "4b" (4B dense, M=4)."""
+    if key == "tiny":
         return Workload("tiny: one 4096-element tensor, M=2, ZeRO-1, no clip, 3 steps",
                         (4096,), M=2, stage=1, bucket_bytes=0, clip=None, steps=3, sigma_mode="const")
-    if idx == 1:
+    if key == "gpt2s":
         return Workload("GPT-2-small shaped (123,570,432 params, d=768, 12 layers), M=8, ZeRO-2, 25 MiB buckets, "
                         "no clip, 10 steps",
                         _transformer_numel(768, 12, True), M=8, stage=2, bucket_bytes=25 * MIB, clip=None,
                         steps=10, sigma_mode="loguniform")
-    if idx == 2:
+    if key == "1p3b":
         return Workload("1.3B dense transformer shaped (1,310,885,888 params, d=2048, 24 layers), M=8, ZeRO-1, "
                         "clip 1.0, 5 steps",
                         _transformer_numel(2048, 24, False), M=8, stage=1, bucket_bytes=0, clip=1.0, steps=5,
                         sigma_mode="loguniform")
-    if idx == 3:
+    if key == "ragged":
         return Workload("ragged: 2000 tensors log-uniform in 1K..4M with primes, M=16, ZeRO-3, clip 1.0, "
                         "1% exact zeros, 5 steps",
                         ragged_numel(), M=16, stage=3, bucket_bytes=0, clip=1.0, steps=5, sigma_mode="const",
                         zero_frac=0.01)
-    if idx == 4:
+    if key == "4b":
         return Workload("4B dense transformer shaped (4,092,982,400 params, d=3200, 32 layers), M=4, ZeRO-3, "
                         "clip 1.0, 3 steps",
                         _transformer_numel(3200, 32, False), M=4, stage=3, bucket_bytes=0, clip=1.0, steps=3,
                         sigma_mode="loguniform")
-    raise ValueError(f"no workload {idx}")
+    raise ValueError(f"no workload {key!r} (known: {', '.join(KEYS)})")
 
 
 def small_variant(w: Workload, numel: tuple, name: str | None = None, **kw) -> Workload:
