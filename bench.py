@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--groups", type=int, default=1,
                     help="hybrid sharding: split the workload's M ranks into this many groups (state "
                          "sharded over M / groups ranks, replicated across groups)")
+    ap.add_argument("--overlap", default="buckets", choices=["none", "launch", "buckets"],
+                    help="--mode stream (fused form) and gather: programmatic launch overlap of the per-bucket "
+                         "kernels (zero_set_launch_overlap); the roofline then covers the whole step or sweep")
     ap.add_argument("--bucket-mib", type=float, default=25.0,
                     help="bucket size for --mode gather when the workload has none")
     ap.add_argument("--max-params", type=int, default=0,
@@ -639,6 +642,17 @@ def run_stream(args):
             opt.apply(h)
 
     step, launches_per_step = eager_step, 0
+    overlapped = fused and not args.graph and args.overlap != "none"
+    if overlapped:
+        # the buckets' slices exist before the step and its calls run back to back on one
+        # stream, as the "buckets" mode requires; per-launch events would bracket launches
+        # that overlap, so one eager step counts the launches and the region runs untimed
+        opt.set_launch_overlap(args.overlap)
+        opt.set_timing(True)
+        opt.kernel_times()
+        eager_step()
+        launches_per_step = int(sum(c for _, c in opt.kernel_times().values()))
+        opt.set_timing(False)
     if args.graph:  # one captured step (scalars from a device schedule), replayed
         if args.warmup + args.steps + 1 > zg.ZERO_MAX_SCHEDULE:
             raise SystemExit(f"--graph: at most {zg.ZERO_MAX_SCHEDULE - 1} warm-up and timed steps")
@@ -658,18 +672,24 @@ def run_stream(args):
     torch.cuda.synchronize()
     if opt.sync_status() != 0:
         raise SystemExit("warm-up step failed")
-    opt.set_timing(True)
+    opt.set_timing(not overlapped)
     opt.kernel_times()
     ms, clk, step_ms = _timed_region(step, args.steps, stream, dist, device)
     kt = opt.kernel_times()
     if args.graph and opt.sync_status() != 0:
         raise SystemExit("a replayed step found no schedule entry")
+    if overlapped and opt.sync_status() != 0:
+        raise SystemExit("an overlapped step failed")
     n, lanes = w.N, opt.sizes["npad"]
     peak, kind = hbm_peak()
     ms_step = ms / args.steps
     if args.graph:  # replays run no per-launch events: the roofline covers the whole step
         real_b = 2 * w.M + (26 if fused else 34)
         dom_name, dom_bytes, dom_ms = "whole step (CUDA graph replay)", real_b * w.N, ms_step
+        kt = {"all": (ms, launches_per_step * args.steps)}
+    elif overlapped:  # launches overlap: the roofline covers the whole step
+        real_b = 2 * w.M + 26
+        dom_name, dom_bytes, dom_ms = f"whole step ({args.overlap}-overlapped bucket launches)", real_b * lanes, ms_step
         kt = {"all": (ms, launches_per_step * args.steps)}
     elif fused:  # per step: one fused launch per bucket
         real_b = 2 * w.M + 26
@@ -690,7 +710,8 @@ def run_stream(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + (f"; hybrid sharding: {args.groups} groups of {w.M // args.groups}"
                                              if args.groups > 1 else ""), "params": n, "M": w.M, "stage": w.stage, "buckets": nb,
-                       "bucket_bytes": w.bucket_bytes, "clip": w.clip, "form": form, "cuda_graph": bool(args.graph)},
+                       "bucket_bytes": w.bucket_bytes, "clip": w.clip, "form": form, "cuda_graph": bool(args.graph),
+                       "launch_overlap": args.overlap if overlapped else "none"},
             "gbs_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9, 1),
             "frac_of_peak_alg": round(alg_bytes_per_param(w.M) * n / (ms_step / 1e3) / 1e9 / peak, 4),
             "real_bytes_per_param": real_b,
@@ -732,16 +753,23 @@ def run_gather(args):
         for _b, _params in opt.prefetched_buckets(order, stream=stream, side_stream=side):
             pass
 
+    overlapped = args.overlap != "none"
+    opt.set_launch_overlap(args.overlap)
     for _ in range(args.warmup):
         sweep()
     torch.cuda.synchronize()
-    opt.set_timing(True)
+    # with overlap, per-launch events would bracket launches that overlap: the region runs
+    # untimed and the roofline covers the whole sweep
+    opt.set_timing(not overlapped)
     opt.kernel_times()
     ms, clk, step_ms = _timed_region(sweep, args.steps, stream, dist, device)
     kt = opt.kernel_times()
     n = w.N
     peak, kind = hbm_peak()
-    g_ms, g_cnt = kt["gather"]
+    if overlapped:
+        g_ms, g_cnt = ms, nb * args.steps
+    else:
+        g_ms, g_cnt = kt["gather"]
     achieved = 4 * n * args.steps / (g_ms / 1e3) / 1e9
     if rank == 0:
         print(json.dumps({
@@ -751,8 +779,11 @@ def run_gather(args):
             "ms_per_step_min": step_ms["min"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
-                       "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead"},
-            "roofline": {"bound": "hbm", "kernel": "gather", "achieved": round(achieved, 1), "peak": peak,
+                       "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead",
+                       "launch_overlap": args.overlap},
+            "roofline": {"bound": "hbm", "kernel": "gather" + (f" (whole sweep, {args.overlap}-overlapped launches)"
+                                                               if overlapped else ""),
+                         "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": kind,
                          "alg_bytes_per_param": 4, "avg_launch_ms": round(g_ms / max(g_cnt, 1), 4)},
             "gpu_launches": int(g_cnt), "clocks": clk}), flush=True)

@@ -121,6 +121,33 @@ def main():
         assert np.array_equal(u16(optf.params()), fullp), "fused per-bucket steps"
     clean(optf, "fused per-bucket steps")
 
+    # the same with overlapped per-bucket launches: fused bucket steps back to back, then
+    # per-bucket gathers back to back into disjoint buffers
+    optf.set_launch_overlap("buckets")
+    side = torch.cuda.Stream(device=dev)
+    for k in range(wf.steps, wf.steps + 2):
+        g = optf.new_grad_buffers()
+        for r in range(wf.M):
+            W.fill_grads(wf, r, k, g[r], optf.tensor_offsets)
+        bufs = {b: [x[optf.buckets[b][0]:optf.buckets[b][0] + optf.bucket_lanes(b)].clone() for x in g]
+                for b in range(len(optf.buckets))}
+        side.wait_stream(torch.cuda.current_stream())
+        for b in reversed(range(len(optf.buckets))):
+            optf.step_bucket(b, bufs[b], hf, stream=side)
+        torch.cuda.synchronize()
+        fullp, _, _, _ = O.zero_step(pf, stf, [u16(x) for x in g], ohf)
+        assert np.array_equal(u16(optf.params()), fullp), "overlapped per-bucket steps"
+    outs = [torch.empty(optf.bucket_range(b)[1] + 1, dtype=torch.bfloat16, device=dev)[1:]
+            for b in range(len(optf.buckets))]
+    for b in range(len(optf.buckets)):
+        optf.gather_bucket(b, outs[b], stream=side)
+    torch.cuda.synchronize()
+    fullv = optf.params()
+    for b in range(len(optf.buckets)):
+        u0, n = optf.bucket_range(b)
+        assert torch.equal(outs[b].view(torch.int16), fullv[u0:u0 + n].view(torch.int16)), "overlapped gathers"
+    clean(optf, "overlapped per-bucket launches")
+
     # save / reshard / load
     saved = opt.save_state()
     w2 = W.small_variant(ws, ws.numel, M=5, stage=3, bucket_bytes=0)

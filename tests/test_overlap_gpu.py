@@ -1,0 +1,193 @@
+"""Launch overlap of the per-bucket kernels (zero_set_launch_overlap).
+
+The per-bucket forms stream buckets one after another: ZeRO-2 reduce-scatter + update as
+each bucket's gradients appear ("CS336 2026 Lecture 8" Slides 23 and 26), ZeRO-3 gathers
+just before each module with prefetch (Slides 24-26; "CS231n Lecture 11" 4.3). With
+programmatic dependent launch a bucket's kernel may start while the previous one finishes.
+Whatever the mode, results must equal the oracle's monolithic step bit for bit, and the
+gathered parameters must equal the full parameter buffer.
+
+Under "buckets" the caller must not enqueue, directly before a per-bucket call on the same
+stream, a kernel that writes what the call reads; the tests below produce gradients the
+way a data-parallel trainer does (on the compute stream, handed to the update stream by an
+event) or ahead of time. Under "launch" any producer may precede the call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import zero_gradient_reduce_scatter_gb300 as zg
+from parity_util import f32, make_hyper, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    yield
+
+
+def gpt_like(d, layers, vocab=1000):
+    sizes = [vocab * d]
+    for _ in range(layers):
+        sizes += [d, d, 3 * d * d, d * d, d, d, 4 * d * d, 4 * d * d]
+    return tuple(sizes + [d, d])
+
+
+def _bucket_slices(opt, full, b):
+    off = opt.buckets[b][0]
+    return [g[off:off + opt.bucket_lanes(b)] for g in full]
+
+
+# producer patterns of the bucket gradients
+def _inline(opt, full, order, h, stream):
+    """Each bucket's buffers are copied on the update stream right before its call (a
+    foreign kernel directly precedes every call: allowed only under "launch")."""
+    for b in order:
+        with torch.cuda.stream(stream):
+            bufs = [x.clone() for x in _bucket_slices(opt, full, b)]
+        opt.step_bucket(b, bufs, h, stream=stream)
+
+
+def _event_handoff(opt, full, order, h, stream):
+    """Trainer pattern: buckets produced on the compute stream, each handed to the update
+    stream by an event; the update stream holds only event waits and bucket launches."""
+    compute = torch.cuda.current_stream()
+    keep = []
+    for b in order:
+        with torch.cuda.stream(compute):
+            bufs = [x.clone() for x in _bucket_slices(opt, full, b)]
+            torch.cuda._sleep(20_000)  # a slow backward: the update stream must wait for it
+            ev = torch.cuda.Event()
+            ev.record(compute)
+        stream.wait_event(ev)
+        opt.step_bucket(b, bufs, h, stream=stream)
+        keep.append(bufs)
+        for x in bufs:
+            x.record_stream(stream)
+    return keep
+
+
+def _ahead(opt, full, order, h, stream):
+    """All bucket buffers exist before the first call: the calls run back to back."""
+    bufs = {b: [x.clone() for x in _bucket_slices(opt, full, b)] for b in order}
+    stream.wait_stream(torch.cuda.current_stream())
+    for b in order:
+        opt.step_bucket(b, bufs[b], h, stream=stream)
+        for x in bufs[b]:
+            x.record_stream(stream)
+    return bufs
+
+
+CASES = [
+    ("launch", "inline", 2, "fused", 1),
+    ("launch", "event", 3, "shards", 1),
+    ("buckets", "event", 2, "fused", 1),
+    ("buckets", "ahead", 2, "fused", 1),
+    ("buckets", "ahead", 3, "shards", 1),
+    ("buckets", "event", 1, "fused", 2),
+]
+
+
+@pytest.mark.parametrize("mode,producer,stage,gather,groups", CASES)
+def test_overlapped_bucket_steps_match_oracle(mode, producer, stage, gather, groups):
+    w = W.small_variant(W.workload("gpt2s"), gpt_like(96, 3), bucket_bytes=120_000, steps=3, stage=stage)
+    dev = torch.device("cuda")
+    mi = W.master_init(w, dev)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, gather=gather, groups=groups)
+    opt.set_launch_overlap(mode)
+    nb = len(opt.buckets)
+    assert nb >= 5
+    p = O.plan(w.numel, w.M // groups, w.bucket_bytes)
+    st = O.init_state(p, w.stage, f32(mi), groups=groups)
+    h, oh = make_hyper(w)
+    sig = W.sigmas(w)
+    stream = torch.cuda.Stream(device=dev)
+    produce = {"inline": _inline, "event": _event_handoff, "ahead": _ahead}[producer]
+    for k in range(w.steps):
+        full = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, full[r], opt.tensor_offsets, sig)
+        torch.cuda.synchronize()
+        produce(opt, full, list(reversed(range(nb))), h, stream)
+        # a kernel consumer enqueued right after the last bucket sees the finished step
+        with torch.cuda.stream(stream):
+            seen = opt.params().clone()
+        torch.cuda.synchronize()
+        assert opt.t == k + 1
+        fullp, _, _, rc = O.zero_step(p, st, [u16(g) for g in full], oh)
+        assert rc == 0 and opt.sync_status() == 0
+        assert np.array_equal(u16(seen), fullp), k
+        for name, buf in (("master", opt.master), ("mom", opt.m), ("var", opt.v)):
+            assert np.array_equal(f32(buf).view(np.uint32), O.flat_state(p, st, name).view(np.uint32)), (k, name)
+
+
+@pytest.mark.parametrize("order", ["forward", "backward"])
+def test_overlapped_prefetched_gather(order):
+    """ZeRO-3 gathers on a side stream, one bucket ahead, into two transient buffers that a
+    slow consumer holds: a gather overlaps the previous gather but never overwrites a buffer
+    before the consumer's event says it is free. Three sweeps with a step between each."""
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(60, 100, 8000, 13), bucket_bytes=25000, steps=3)
+    dev = torch.device("cuda")
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
+                           gather="shards")
+    opt.set_launch_overlap("buckets")
+    h, _ = make_hyper(w)
+    nb = len(opt.buckets)
+    assert nb > 4
+    seq = list(range(nb)) if order == "forward" else list(reversed(range(nb)))
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    for k in range(w.steps):
+        grads = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, grads[r], opt.tensor_offsets)
+        opt.step(grads, h)
+        check = torch.full((opt.sizes["n"],), -1, dtype=torch.int16, device=dev)
+        for b, params in opt.prefetched_buckets(seq, stream=stream, side_stream=side):
+            torch.cuda._sleep(100_000)  # a slow "module" keeps the buffer busy
+            u0, n = opt.bucket_range(b)
+            check[u0:u0 + n].copy_(params.view(torch.int16))
+        torch.cuda.synchronize()
+        assert torch.equal(check, opt.params().view(torch.int16)), k
+
+
+def test_back_to_back_gathers_into_one_buffer():
+    """Gathers into overlapping destinations keep their order: each waits for the one
+    before (the library compares destinations), so the later values win."""
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(40, 300, 9000, 21), bucket_bytes=20000, steps=1)
+    dev = torch.device("cuda")
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
+                           gather="shards")
+    opt.set_launch_overlap("buckets")
+    full = opt.params()
+    nb = len(opt.buckets)
+    sizes = [opt.bucket_range(b)[1] for b in range(nb)]
+    big = max(range(nb), key=lambda b: sizes[b])
+    buf = torch.zeros(max(sizes) + 16, dtype=torch.bfloat16, device=dev)
+    for b in range(nb):
+        if b == big:
+            continue
+        opt.gather_bucket(big, buf)
+        opt.gather_bucket(b, buf[3:])  # overlaps the first gather's destination
+        torch.cuda.synchronize()
+        ub, nbig = opt.bucket_range(big)
+        u0, n = opt.bucket_range(b)
+        assert torch.equal(buf[3:3 + n].view(torch.int16), full[u0:u0 + n].view(torch.int16)), b
+        assert torch.equal(buf[:3].view(torch.int16), full[ub:ub + 3].view(torch.int16)), b
+        if 3 + n < nbig:
+            assert torch.equal(buf[3 + n:nbig].view(torch.int16), full[ub + 3 + n:ub + nbig].view(torch.int16)), b
+
+
+def test_set_launch_overlap_refusals():
+    w = W.small_variant(W.workload("gpt2s"), (3000, 3000), bucket_bytes=6000, steps=1)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")),
+                           bucket_bytes=w.bucket_bytes)
+    for bad in (-1, 3):
+        assert zg._lib().zero_set_launch_overlap(opt._ctx, bad) == -1
+    opt.set_launch_overlap("none")

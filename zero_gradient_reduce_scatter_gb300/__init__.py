@@ -45,6 +45,7 @@ ZERO_MAX_SCHEDULE = 1024
 GATHER = {"fused": 0, "shards": 1}
 GHAT = {"auto": 0, "materialize": 1, "recompute": 2}
 STATE = {"master": 0, "m": 1, "v": 2, "ghat": 3}
+OVERLAP = {"none": 0, "launch": 1, "buckets": 2}
 KERNELS = ("rs_norm", "norm_final", "adamw", "rs_adamw", "gather", "init", "step_begin")
 
 
@@ -122,6 +123,7 @@ SIGNATURES = {
     "zero_kernel_times": (ctypes.c_int, [_P, _P, _P]),
     "zero_launch_shape": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "zero_set_max_ctas": (ctypes.c_int, [_P, ctypes.c_int]),
+    "zero_set_launch_overlap": (ctypes.c_int, [_P, ctypes.c_int]),
     "zero_destroy": (ctypes.c_int, [_P]),
     "zero_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "zero_last_cuda_error": (ctypes.c_int, []),
@@ -522,6 +524,12 @@ class ZeroOptimizer:
         ctas, thr = ctypes.c_int(), ctypes.c_int()
         _check(_lib().zero_launch_shape(self._ctx, ctypes.byref(ctas), ctypes.byref(thr)), "zero_launch_shape")
         return ctas.value, thr.value
+
+    def set_launch_overlap(self, mode: str):
+        """Programmatic launch overlap of the per-bucket kernels: "none", "launch" (each waits
+        for its predecessor before touching memory) or "buckets" (consecutive per-bucket
+        launches of this optimizer on one stream overlap; see zero_set_launch_overlap)."""
+        _check(_lib().zero_set_launch_overlap(self._ctx, OVERLAP[mode]), "zero_set_launch_overlap")
 
     def set_max_ctas(self, ctas: int):
         """Cap the grid of the streaming kernels (0 = none); for testing index arithmetic."""

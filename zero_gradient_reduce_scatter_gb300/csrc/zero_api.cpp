@@ -70,6 +70,15 @@ struct zero_ctx {
     bool sched_active = false;
     int sched_clip = 0;
     int sched_mode = ZERO_GHAT_RECOMPUTE;
+    // launch overlap (zero_set_launch_overlap): the library's kernel launches are counted;
+    // after a per-bucket launch that a successor may overlap, its count, stream, kind
+    // (ZERO_K_RS_ADAMW or ZERO_K_GATHER) and, for a gather, the destination bytes
+    int overlap = ZERO_OVERLAP_NONE;
+    uint64_t seq = 0;
+    uint64_t chain_seq = ~0ull;
+    cudaStream_t chain_stream = nullptr;
+    int chain_kind = -1;
+    uintptr_t chain_lo = 0, chain_hi = 0;
 };
 
 namespace {
@@ -256,6 +265,7 @@ struct Timed {
     cudaStream_t s;
     size_t slot = SIZE_MAX;  // index into c->events (an index stays valid if the pool grows)
     Timed(zero_ctx* ctx, int kernel, cudaStream_t stream) : c(ctx), s(stream) {
+        ++c->seq;  // every kernel launch of the library passes through here
         if (!c->timing || c->n_timed >= kMaxTimedLaunches) return;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;  // a graph replays no host timing
         if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return;
@@ -304,13 +314,43 @@ zg::StepArgs base_args(zero_ctx* c) {
     return a;
 }
 
-// out[0 .. count) = parameters of unpadded indices [u0, u0 + count).
-int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStream_t s) {
+// Programmatic-launch mode of a per-bucket kernel of `kind` about to be launched on s.
+// It may overlap its predecessor (wait last) only under ZERO_OVERLAP_BUCKETS, when the
+// caller allows it for this launch and the library's previous kernel launch was a
+// per-bucket launch of the same kind on the same stream, with nothing launched since.
+int pdl_mode(const zero_ctx* c, int kind, cudaStream_t s, bool may_overlap) {
+    if (c->overlap == ZERO_OVERLAP_NONE) return zg::kPdlNone;
+    if (c->overlap == ZERO_OVERLAP_BUCKETS && may_overlap && c->chain_seq == c->seq && c->chain_stream == s &&
+        c->chain_kind == kind)
+        return zg::kPdlWaitLast;
+    return zg::kPdlWaitFirst;
+}
+
+// After a per-bucket launch: a successor of the same kind may overlap it.
+void note_chain(zero_ctx* c, int kind, cudaStream_t s, uintptr_t lo = 0, uintptr_t hi = 0) {
+    c->chain_seq = c->seq;
+    c->chain_stream = s;
+    c->chain_kind = kind;
+    c->chain_lo = lo;
+    c->chain_hi = hi;
+}
+
+// out[0 .. count) = parameters of unpadded indices [u0, u0 + count). may_overlap: the
+// launch may overlap a directly preceding gather into a disjoint destination.
+int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStream_t s, bool may_overlap = false) {
     const int grid = grid_for(c, zg::kVarGather, count / 8 + 2);
-    Timed tm(c, ZERO_K_GATHER, s);
-    cudaError_t e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, out, c->dev_buckets,
-                                      (int64_t)c->buckets.size(), c->npad, u0, count, c->status, grid, s);
-    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(out), hi = lo + 2 * (uintptr_t)(count > 0 ? count : 0);
+    const bool disjoint = hi <= c->chain_lo || lo >= c->chain_hi;
+    const int pdl = pdl_mode(c, ZERO_K_GATHER, s, may_overlap && disjoint);
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_GATHER, s);
+        e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, out, c->dev_buckets, (int64_t)c->buckets.size(),
+                              c->npad, u0, count, c->status, grid, s, pdl);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (count > 0 && pdl != zg::kPdlNone) note_chain(c, ZERO_K_GATHER, s, lo, hi);
+    return ZERO_OK;
 }
 
 }  // namespace
@@ -591,12 +631,16 @@ static int step_one_bucket(zero_ctx* c, int64_t bucket, const void* const* grads
     int rc;
     if (sched && c->n_bucket_done == 0 && (rc = launch_step_begin(c, s))) return rc;  // once per step
     const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
+    // launch overlap: buckets after the first of a step may overlap the bucket before;
+    // scheduled steps launch as ordinary kernels
+    a.pdl = sched ? zg::kPdlNone : pdl_mode(c, ZERO_K_RS_ADAMW, s, c->n_bucket_done > 0);
     cudaError_t err;
     {
         Timed tm(c, ZERO_K_RS_ADAMW, s);
         err = zg::launch_rs_adamw(a, false, sched, g4, s);
     }
     if (err != cudaSuccess) return cuda_fail(err);
+    if (a.pdl != zg::kPdlNone) note_chain(c, ZERO_K_RS_ADAMW, s);
     if (c->cfg.gather == ZERO_GATHER_SHARDS) {  // the bucket's all-gather
         rc = gather_range(c, e.uoff, e.n, (uint16_t*)c->bufs.param_full + e.uoff, s);
         if (rc) return rc;
@@ -732,6 +776,7 @@ int zero_set_schedule(zero_ctx* c, const zero_hyper* h, int64_t count, void* str
         if (i == 0 && (rc = resolve_ghat_mode(c, &h[0], &mode))) return rc;
     }
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -775,6 +820,7 @@ int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_
     int rc = check_hyper(h);
     if (rc) return rc;
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t gbytes = (size_t)(2 * c->npad);
@@ -792,6 +838,7 @@ int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!master && !m && !v) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     const int grid = grid_for(c, zg::kVarInit, c->npad);
@@ -830,6 +877,7 @@ int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* 
     int rc = check_hyper(h);
     if (rc) return rc;
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
     cudaError_t e = cudaSuccess;
@@ -887,7 +935,7 @@ int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
         u0 = c->buckets[(size_t)bucket].uoff;
         count = c->buckets[(size_t)bucket].n;
     }
-    return gather_range(c, u0, count, out + u0, (cudaStream_t)stream);
+    return gather_range(c, u0, count, out + u0, (cudaStream_t)stream, true);
 }
 
 int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
@@ -898,7 +946,7 @@ int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     const zg::Bucket& e = c->buckets[(size_t)bucket];
-    return gather_range(c, e.uoff, e.n, (uint16_t*)dst, (cudaStream_t)stream);
+    return gather_range(c, e.uoff, e.n, (uint16_t*)dst, (cudaStream_t)stream, true);
 }
 
 int zero_bucket_info(zero_ctx* c, int64_t bucket, int64_t* uoff, int64_t* n) {
@@ -922,6 +970,7 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
     }
     if (!src) return ZERO_ERR_SIZE_MISMATCH;
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     float* d = (float*)dst;
@@ -937,6 +986,7 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
 
 static int read_status(zero_ctx* c, zg::Status* out) {
     DeviceGuard guard(c->device);
+    ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaError_t e;
     if (c->sched_active) {  // replays of captured steps may run on any stream
@@ -1040,6 +1090,14 @@ int zero_kernel_times(zero_ctx* c, double* ms, int64_t* launches) {
         if (ms) ms[k] = acc[k];
         if (launches) launches[k] = cnt[k];
     }
+    return ZERO_OK;
+}
+
+int zero_set_launch_overlap(zero_ctx* c, int mode) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (mode < ZERO_OVERLAP_NONE || mode > ZERO_OVERLAP_BUCKETS) return ZERO_ERR_INVALID_ARG;
+    c->overlap = mode;
+    c->chain_seq = ~0ull;  // nothing launched so far may be overlapped
     return ZERO_OK;
 }
 

@@ -78,6 +78,14 @@ struct StepArgs {
     AdamConsts k;
     Status* status;
     double* partials;     // one fp64 partial sum of squares per CTA of the norm pass
+    int32_t pdl;          // PdlMode of kernels launched with programmatic stream serialization
+};
+
+// Programmatic dependent launch of the per-bucket kernels (zero_set_launch_overlap).
+enum PdlMode : int32_t {
+    kPdlNone = 0,       // ordinary launch
+    kPdlWaitFirst = 1,  // waits for the preceding kernel before its first memory access
+    kPdlWaitLast = 2,   // works at once; waits for the preceding kernel before exiting
 };
 
 // Launch shapes and load paths of the streaming kernels, chosen by measurement on GB300
@@ -152,6 +160,8 @@ cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, do
 cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s);
 // sched: the AdamW scalars are the running scheduled step's (st->cur), not a.k.
 cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s);
+// a.pdl != kPdlNone (plain, unscheduled form only): launched with programmatic stream
+// serialization in that mode.
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int grid, cudaStream_t s);
 // Scheduled steps. Install: counter = t, entry 0 serves step t + 1, `count` entries, the
 // schedule flag cleared. Begin (one thread, first launch of every scheduled step): advance
@@ -160,8 +170,10 @@ cudaError_t launch_schedule_install(Status* st, int64_t t, int64_t count, cudaSt
 cudaError_t launch_step_begin(Status* st, const ScheduleEntry* table, cudaStream_t s);
 // out[d] = bf16 parameter of unpadded index u0 + d, d < count, from the padded shards
 // (out needs only 2-byte alignment).
+// pdl != kPdlNone: launched with programmatic stream serialization in that mode.
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb,
-                          int64_t npad, int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s);
+                          int64_t npad, int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s,
+                          int pdl = kPdlNone);
 // State from unpadded fp32 vectors (m_init / v_init may be null: zeros), plus bf16 copies.
 cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init,
                         float* master, float* m, float* v, uint16_t* full, uint16_t* shards,

@@ -17,6 +17,8 @@
 
 #include <cuda_bf16.h>
 
+#include <utility>
+
 #include "zero_internal.h"
 
 namespace zg {
@@ -80,6 +82,27 @@ __device__ __forceinline__ uint4 ld_grad(const uint16_t* p) {
 __device__ __forceinline__ float4 ld_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
 __device__ __forceinline__ void st_u4(uint16_t* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
+
+// ---------------------------------------------------------------------------------------
+// Programmatic dependent launch (kernels launched with programmatic stream serialization,
+// which may start while the kernel before them on the stream is still running).
+// kPdlWaitFirst: griddepcontrol.wait (the preceding grid complete, its writes visible)
+// before any memory access, then let the next such kernel launch. kPdlWaitLast: let the
+// next kernel launch at once, do the work, and wait only before exiting, so that the
+// kernel still completes after its predecessor. The destructor runs the exit wait on every
+// return path. ON = false compiles to nothing (the kernels of ordinary launches).
+// ---------------------------------------------------------------------------------------
+template <bool ON>
+struct PdlScope {
+    const int32_t mode;
+    __device__ __forceinline__ explicit PdlScope(int32_t m) : mode(ON ? m : (int32_t)kPdlNone) {
+        if (ON && mode == kPdlWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (ON && mode != kPdlNone) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    __device__ __forceinline__ ~PdlScope() {
+        if (ON && mode == kPdlWaitLast) asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+};
 
 // ---------------------------------------------------------------------------------------
 // Bucket cursor: which bucket a (non-decreasing) lane index falls in.
@@ -497,8 +520,9 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
 // leaves registers. SCALE applies the clip scale computed by K2 (recompute form). Runs over
 // vecs [vbeg, vend): the whole layout, or one bucket (ZeRO-2 per-bucket steps).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false>
+template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false, bool PDL = false>
 __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
+    const PdlScope<PDL> pdl(a.pdl);
     float s = 1.0f;
     if (SCALE) {
         if (a.status->flags & (SCHED ? (kFlagNonfinite | kFlagSchedule) : kFlagNonfinite)) return;
@@ -588,9 +612,12 @@ struct UCursor {
     }
 };
 
+template <bool PDL>
 __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
                                                      uint16_t* __restrict__ out, const Bucket* tab, int64_t nb,
-                                                     int64_t npad, int64_t u0, int64_t count, Status* st) {
+                                                     int64_t npad, int64_t u0, int64_t count, Status* st,
+                                                     int32_t pdl_mode) {
+    const PdlScope<PDL> pdl(pdl_mode);
     const int64_t a0 = (int64_t)((reinterpret_cast<uintptr_t>(out) >> 1) & 7);
     const int64_t nslots = (count + a0 + 7) >> 3;
     const int64_t stride = (int64_t)gridDim.x * kThreadsGather;
@@ -734,6 +761,12 @@ template <int MT> struct RsAdamwPlain {
         else return &k_rs_adamw<MT, false>;
     }
 };
+template <int MT> struct RsAdamwPlainPdl {
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_adamw<grouped_mt(MT), false, true, false, true>;
+        else return &k_rs_adamw<MT, false, false, false, true>;
+    }
+};
 template <int MT> struct RsAdamwScaledSched {
     static auto fn() {
         if constexpr (MT < 0) return &k_rs_adamw<grouped_mt(MT), true, true, true>;
@@ -754,10 +787,26 @@ const void* variant_fn(int variant, int M, int groups) {
         case kVarAdamw: return (const void*)&k_adamw<false>;
         case kVarRsAdamwScaled: return (const void*)ByM<RsAdamwScaled>::get(M, groups);
         case kVarRsAdamwPlain: return (const void*)ByM<RsAdamwPlain>::get(M, groups);
-        case kVarGather: return (const void*)&k_gather;
+        case kVarGather: return (const void*)&k_gather<false>;
         case kVarInit: return (const void*)&k_init;
         default: return nullptr;
     }
+}
+
+// Launch with programmatic stream serialization (see PdlScope).
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*fn)(P...), int grid, int threads, cudaStream_t s, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, std::forward<A>(args)...);
 }
 
 }  // namespace
@@ -834,6 +883,8 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int
         else ByM<RsAdamwPlainSched>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
     } else if (apply_scale) {
         ByM<RsAdamwScaled>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    } else if (a.pdl != kPdlNone) {
+        return launch_pdl(ByM<RsAdamwPlainPdl>::get(a.M, a.groups), grid, kThreadsRsAdamw, s, a);
     } else {
         ByM<RsAdamwPlain>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
     }
@@ -841,9 +892,12 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int
 }
 
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb, int64_t npad,
-                          int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s) {
+                          int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s, int pdl) {
     if (count <= 0) return cudaSuccess;
-    k_gather<<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count, st);
+    if (pdl != kPdlNone)
+        return launch_pdl(&k_gather<true>, grid, kThreadsGather, s, shards, out, buckets, nb, npad, u0, count, st,
+                          (int32_t)pdl);
+    k_gather<false><<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count, st, (int32_t)kPdlNone);
     return cudaGetLastError();
 }
 
