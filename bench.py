@@ -314,6 +314,24 @@ def oracle_rates(w, procs, windows, seconds):
     return [sum(r[i][0] for r in res) / max(r[i][1] for r in res) for i in range(windows)]
 
 
+def copy_rate(pairs, stream) -> float:
+    """GB/s of plain copies dst.copy_(src) of every (dst, src) pair, back to back on `stream`
+    (best of two passes, CUDA events)."""
+    import torch
+    best = 0.0
+    nbytes = sum(src.numel() * src.element_size() for _, src in pairs)
+    for _ in range(2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return best
+
+
 def host_cores():
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
@@ -478,6 +496,10 @@ def run_ours(args):
         for i in range(2):  # warm-up, both device sets
             opt.step_host_overlapped(host_grads, sets[i], host_params, h, copy_stream)
         torch.cuda.synchronize()
+        # the host link's rate right now, by plain copies of the same bytes: pinned host-to-
+        # device bandwidth on a shared host varies over minutes, and it bounds this number
+        h2d_gbs = copy_rate([(sets[0][r], host_grads[r]) for r in range(w.M)], copy_stream)
+        d2h_gbs = copy_rate([(host_params, opt.params())], copy_stream)
         barrier(dist, device)
         t0 = time.perf_counter()
         for i in range(args.e2e_steps):
@@ -488,7 +510,9 @@ def run_ours(args):
                "ms_per_step": e2e_ms / args.e2e_steps, "call": "zero_step_host_overlapped",
                "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2,
                "host_gradients": (f"{w.M} pinned replicas" if distinct else
-                                  f"one pinned replica copied to all {w.M} device buffers (host memory)")}
+                                  f"one pinned replica copied to all {w.M} device buffers (host memory)"),
+               "h2d_copy_gbs": round(h2d_gbs, 1), "d2h_copy_gbs": round(d2h_gbs, 1),
+               "copy_floor_ms": round(sum(g.numel() * 2 for g in host_grads) / h2d_gbs / 1e6, 2)}
         del host_grads, host_params, sets, srcs
 
     cpu = None
