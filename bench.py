@@ -64,7 +64,7 @@ def parse():
                     help="hybrid sharding: split the workload's M ranks into this many groups (state "
                          "sharded over M / groups ranks, replicated across groups)")
     ap.add_argument("--overlap", default="buckets", choices=["none", "launch", "buckets"],
-                    help="--mode stream (fused form) and gather: programmatic launch overlap of the per-bucket "
+                    help="--mode stream and gather: programmatic launch overlap of the per-bucket "
                          "kernels (zero_set_launch_overlap); the roofline then covers the whole step or sweep")
     ap.add_argument("--bucket-mib", type=float, default=25.0,
                     help="bucket size for --mode gather when the workload has none")
@@ -666,7 +666,7 @@ def run_stream(args):
             opt.apply(h)
 
     step, launches_per_step = eager_step, 0
-    overlapped = fused and not args.graph and args.overlap != "none"
+    overlapped = not args.graph and args.overlap != "none"
     if overlapped:
         # the buckets' slices exist before the step and its calls run back to back on one
         # stream, as the "buckets" mode requires; per-launch events would bracket launches
@@ -712,7 +712,7 @@ def run_stream(args):
         dom_name, dom_bytes, dom_ms = "whole step (CUDA graph replay)", real_b * w.N, ms_step
         kt = {"all": (ms, launches_per_step * args.steps)}
     elif overlapped:  # launches overlap: the roofline covers the whole step
-        real_b = 2 * w.M + 26
+        real_b = 2 * w.M + (26 if fused else 34)
         dom_name, dom_bytes, dom_ms = f"whole step ({args.overlap}-overlapped bucket launches)", real_b * lanes, ms_step
         kt = {"all": (ms, launches_per_step * args.steps)}
     elif fused:  # per step: one fused launch per bucket

@@ -155,7 +155,8 @@ typedef struct {
     int64_t bytes_param_shards; /* bf16 npad with ZERO_GATHER_SHARDS, else 0               */
     int64_t bytes_grad_each;    /* bf16 npad: each of the M gradient buffers               */
     int64_t bytes_scratch;      /* status word, norm partials, bucket table, per-bucket
-                                   sums and the step schedule                               */
+                                   sums, the step schedule and per-bucket norm partials
+                                   (9,728 bytes per bucket)                                 */
 } zero_sizes;
 
 /* Device buffers borrowed by a context. All 16-byte aligned (torch allocations are). */
@@ -376,8 +377,8 @@ int zero_launch_shape(zero_ctx* ctx, int* ctas, int* threads);
 int zero_set_max_ctas(zero_ctx* ctx, int ctas);
 
 /* Launch overlap of the per-bucket kernels: those of zero_step_bucket (the fused
- * reduce-scatter + AdamW of one bucket) and of zero_gather_bucket / zero_gather (one
- * bucket's all-gather). The pages stream buckets one after another (ZeRO-2 reduce-scatter as
+ * reduce-scatter + AdamW of one bucket), of zero_reduce_bucket (one bucket's reduce-scatter
+ * and sum of squares) and of zero_gather_bucket / zero_gather (one bucket's all-gather). The pages stream buckets one after another (ZeRO-2 reduce-scatter as
  * gradients appear, "CS336 2026 Lecture 8" Slides 23 and 26; ZeRO-3 per-module gather with
  * prefetch, Slides 24-26); each such launch is short (tens of microseconds), so the ramp-up
  * and tail of every launch cost a visible share. Overlap uses programmatic dependent launch:
@@ -389,8 +390,9 @@ int zero_set_max_ctas(zero_ctx* ctx, int ctas);
  *                        launch itself overlaps. Correct whatever precedes the call.
  *  ZERO_OVERLAP_BUCKETS  as LAUNCH, except that a per-bucket kernel that directly follows a
  *                        per-bucket kernel of the same kind from this context on the same
- *                        stream (a fused bucket step after another bucket of the same step; a
- *                        gather after a gather into a disjoint destination) does its work at
+ *                        stream (a fused bucket step or a bucket reduction after another
+ *                        bucket of the same step; a gather after a gather into a disjoint
+ *                        destination) does its work at
  *                        once and waits for its predecessor only before it exits. It still
  *                        completes after its predecessor, so stream order holds for whatever
  *                        is enqueued later. The library decides this from its own launches;
@@ -400,7 +402,9 @@ int zero_set_max_ctas(zero_ctx* ctx, int ctas);
  *                        writes. Work ordered by an event wait (cudaStreamWaitEvent) is not
  *                        affected: that dependency is kept whole. The first bucket of every
  *                        step, and every step of a schedule (zero_step_bucket_scheduled),
- *                        waits for its predecessor as under LAUNCH.
+ *                        waits for its predecessor as under LAUNCH. Under either mode each
+ *                        bucket reduction keeps its norm partials in a region of the scratch
+ *                        buffer of its own (zero_plan sizes the scratch for it).
  * With overlap, per-kernel event timing (zero_set_timing) brackets launches that may run
  * concurrently; time the whole sequence instead. Errors: BAD_CONTEXT, INVALID_ARG. */
 #define ZERO_OVERLAP_NONE    0

@@ -102,6 +102,21 @@ def main():
         fullp, _, _, _ = O.zero_step(p, st, [u16(x) for x in g], oh)
         assert bf16_ulp_diff(u16(opt.params()), fullp) <= 1, "streaming"
     clean(opt, "streaming")
+    # the same with overlapped bucket reductions (per-bucket partial regions)
+    opt.set_launch_overlap("buckets")
+    for k in range(ws.steps, ws.steps + 2):
+        g = opt.new_grad_buffers()
+        for r in range(ws.M):
+            W.fill_grads(ws, r, k, g[r], opt.tensor_offsets)
+        bufs = {b: [x[opt.buckets[b][0]:opt.buckets[b][0] + opt.bucket_lanes(b)].clone() for x in g]
+                for b in range(len(opt.buckets))}
+        for b in reversed(range(len(opt.buckets))):
+            opt.reduce_bucket(b, bufs[b])
+        opt.apply(h)
+        fullp, _, _, _ = O.zero_step(p, st, [u16(x) for x in g], oh)
+        assert bf16_ulp_diff(u16(opt.params()), fullp) <= 1, "overlapped streaming"
+    clean(opt, "overlapped streaming")
+    opt.set_launch_overlap("none")
 
     # ZeRO-2 fused per-bucket steps (no clipping), ZeRO-3 shards with the per-bucket gather
     wf = W.small_variant(W.workload("gpt2s"), (70000, 5000, 301, 69999), bucket_bytes=120000, steps=2, stage=3)

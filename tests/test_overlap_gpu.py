@@ -19,7 +19,7 @@ import torch
 import oracle as O
 import workloads as W
 import zero_gradient_reduce_scatter_gb300 as zg
-from parity_util import f32, make_hyper, u16
+from parity_util import REL_NORM, f32, make_hyper, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -191,3 +191,101 @@ def test_set_launch_overlap_refusals():
     for bad in (-1, 3):
         assert zg._lib().zero_set_launch_overlap(opt._ctx, bad) == -1
     opt.set_launch_overlap("none")
+
+
+def _reduce_ahead(opt, full, order, stream):
+    bufs = {b: [x.clone() for x in _bucket_slices(opt, full, b)] for b in order}
+    stream.wait_stream(torch.cuda.current_stream())
+    for b in order:
+        opt.reduce_bucket(b, bufs[b], stream=stream)
+        for x in bufs[b]:
+            x.record_stream(stream)
+    return bufs
+
+
+def _reduce_event(opt, full, order, stream):
+    compute = torch.cuda.current_stream()
+    keep = []
+    for b in order:
+        bufs = [x.clone() for x in _bucket_slices(opt, full, b)]
+        torch.cuda._sleep(20_000)
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        stream.wait_event(ev)
+        opt.reduce_bucket(b, bufs, stream=stream)
+        keep.append(bufs)
+        for x in bufs:
+            x.record_stream(stream)
+    return keep
+
+
+@pytest.mark.parametrize("mode,producer,groups", [("launch", "event", 1), ("buckets", "event", 1),
+                                                   ("buckets", "ahead", 1), ("buckets", "ahead", 2)])
+def test_overlapped_bucket_reductions_match_ordinary_launches(mode, producer, groups):
+    """ZeRO-2 streaming with clipping (every bucket reduced, then one apply): with overlapped
+    reductions the averaged gradient, the norm and the whole state equal those of ordinary
+    launches bit for bit (same grid, same partial sums), and the oracle's step within the
+    parity tolerances (averaged gradient bit-exact)."""
+    w = W.small_variant(W.workload("gpt2s"), gpt_like(96, 3), bucket_bytes=120_000, steps=3, clip=1e-3)
+    dev = torch.device("cuda")
+    mi = W.master_init(w, dev)
+    ref = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True, groups=groups)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True, groups=groups)
+    opt.set_launch_overlap(mode)
+    nb = len(opt.buckets)
+    assert nb >= 5
+    p = O.plan(w.numel, w.M // groups, w.bucket_bytes)
+    st = O.init_state(p, w.stage, f32(mi), groups=groups)
+    h, oh = make_hyper(w)
+    sig = W.sigmas(w)
+    stream = torch.cuda.Stream(device=dev)
+    order = list(reversed(range(nb)))
+    for k in range(w.steps):
+        full = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, full[r], opt.tensor_offsets, sig)
+        torch.cuda.synchronize()
+        for b in order:
+            ref.reduce_bucket(b, _bucket_slices(ref, full, b))
+        ref.apply(h)
+        (_reduce_event if producer == "event" else _reduce_ahead)(opt, full, order, stream)
+        opt.apply(h, stream=stream)
+        torch.cuda.synchronize()
+        assert opt.sync_status() == 0 and ref.sync_status() == 0
+        assert opt.last_norm() == ref.last_norm(), k
+        for a, b_ in ((opt.ghat, ref.ghat), (opt.master, ref.master), (opt.m, ref.m), (opt.v, ref.v),
+                      (opt.params(), ref.params())):
+            assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), k
+        fullp, norm, _, rc = O.zero_step(p, st, [u16(g) for g in full], oh)
+        assert rc == 0
+        assert np.array_equal(f32(opt.ghat).view(np.uint32), O.flat_state(p, st, "ghat").view(np.uint32)), k
+        assert abs(opt.last_norm()[0] - norm) <= REL_NORM * norm
+
+
+def test_bucket_reduced_twice_in_one_step():
+    """A bucket reduced a second time in a step (after the next bucket) replaces its first
+    reduction; the repeated call waits for what came before, so the second values win."""
+    w = W.small_variant(W.workload("gpt2s"), (30000, 20000, 25000), bucket_bytes=60_000, steps=1, clip=1e-3)
+    dev = torch.device("cuda")
+    mi = W.master_init(w, dev)
+    ref = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+    opt.set_launch_overlap("buckets")
+    assert len(opt.buckets) == 3
+    h, _ = make_hyper(w)
+    full = opt.new_grad_buffers()
+    for r in range(w.M):
+        W.fill_grads(w, r, 0, full[r], opt.tensor_offsets)
+    junk = [torch.full_like(x, 3.0) for x in _bucket_slices(opt, full, 1)]
+    good = {b: [x.clone() for x in _bucket_slices(opt, full, b)] for b in range(3)}
+    torch.cuda.synchronize()
+    for b, bufs in ((2, good[2]), (1, junk), (0, good[0]), (1, good[1])):
+        opt.reduce_bucket(b, bufs)
+    opt.apply(h)
+    for b in (2, 1, 0):
+        ref.reduce_bucket(b, good[b])
+    ref.apply(h)
+    torch.cuda.synchronize()
+    assert opt.last_norm() == ref.last_norm()
+    for a, b_ in ((opt.ghat, ref.ghat), (opt.master, ref.master), (opt.params(), ref.params())):
+        assert torch.equal(a.view(torch.int16), b_.view(torch.int16))

@@ -41,6 +41,7 @@ struct zero_ctx {
     int stepped;
     // per-bucket streaming (zero_reduce_bucket / zero_apply)
     double* bucket_sums;          // device: one fp64 sum of squares per bucket
+    double* bucket_partials;      // device: kBucketPartials norm partials per bucket (launch overlap)
     std::vector<char> reduced;    // host: buckets reduced since the last zero_apply
     int64_t n_reduced = 0;
     std::vector<char> bucket_done;  // host: buckets updated by zero_step_bucket in this step
@@ -431,6 +432,7 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->dev_buckets = (zg::Bucket*)(scratch + zg::kScratchBuckets);
     c->bucket_sums = (double*)(scratch + zg::scratch_bucket_sums((int64_t)L.buckets.size()));
     c->dev_sched = (zg::ScheduleEntry*)(scratch + zg::scratch_schedule((int64_t)L.buckets.size()));
+    c->bucket_partials = (double*)(scratch + zg::scratch_bucket_partials((int64_t)L.buckets.size()));
     c->reduced.assign(L.buckets.size(), 0);
     c->bucket_done.assign(L.buckets.size(), 0);
     c->t = 0;
@@ -597,7 +599,21 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     a.vend = e.end / 8;
     a.gbase = e.off;
     a.gext = e.end - e.off;
-    const int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
+    int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
+    double* parts = c->partials;
+    int sum_pdl = zg::kPdlNone;
+    if (c->overlap != ZERO_OVERLAP_NONE) {
+        // launch overlap: the bucket's partials in a region of its own, so that the next
+        // bucket's reduction may run while this bucket's sum is still being formed; the
+        // reduction may overlap its predecessor when it follows the previous bucket's
+        // reduction of this step (a bucket reduced twice in one step waits)
+        if (g1 > zg::kBucketPartials) g1 = zg::kBucketPartials;
+        parts = c->bucket_partials + (size_t)bucket * zg::kBucketPartials;
+        a.partials = parts;
+        a.part_cap = zg::kBucketPartials;
+        a.pdl = pdl_mode(c, ZERO_K_RS_NORM, s, c->n_reduced > 0 && !c->reduced[(size_t)bucket]);
+        sum_pdl = c->overlap == ZERO_OVERLAP_BUCKETS ? zg::kPdlTriggerWait : zg::kPdlWaitFirst;
+    }
     cudaError_t err;
     {
         Timed tm(c, ZERO_K_RS_NORM, s);
@@ -605,9 +621,10 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     }
     if (err == cudaSuccess) {
         Timed tm(c, ZERO_K_NORM_FINAL, s);
-        err = zg::launch_sum_partials(c->partials, g1, c->bucket_sums + bucket, s);
+        err = zg::launch_sum_partials(parts, g1, c->bucket_sums + bucket, s, sum_pdl);
     }
     if (err != cudaSuccess) return cuda_fail(err);
+    if (c->overlap != ZERO_OVERLAP_NONE) note_chain(c, ZERO_K_RS_NORM, s);
     if (!c->reduced[(size_t)bucket]) c->n_reduced += 1;
     c->reduced[(size_t)bucket] = 1;
     return ZERO_OK;

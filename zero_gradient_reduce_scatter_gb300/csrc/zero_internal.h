@@ -79,6 +79,7 @@ struct StepArgs {
     Status* status;
     double* partials;     // one fp64 partial sum of squares per CTA of the norm pass
     int32_t pdl;          // PdlMode of kernels launched with programmatic stream serialization
+    int32_t part_cap;     // partial sums `partials` holds (0: kMaxPartials; bounds checks)
 };
 
 // Programmatic dependent launch of the per-bucket kernels (zero_set_launch_overlap).
@@ -86,6 +87,7 @@ enum PdlMode : int32_t {
     kPdlNone = 0,       // ordinary launch
     kPdlWaitFirst = 1,  // waits for the preceding kernel before its first memory access
     kPdlWaitLast = 2,   // works at once; waits for the preceding kernel before exiting
+    kPdlTriggerWait = 3,  // lets the next kernel launch at once, then waits like kPdlWaitFirst
 };
 
 // Launch shapes and load paths of the streaming kernels, chosen by measurement on GB300
@@ -124,8 +126,15 @@ inline int64_t scratch_bucket_sums(int64_t n_buckets) { return (kScratchBuckets 
 inline int64_t scratch_schedule(int64_t n_buckets) {
     return (scratch_bucket_sums(n_buckets) + 8 * n_buckets + 255) / 256 * 256;
 }
-inline int64_t scratch_bytes(int64_t n_buckets) {
+// Per-bucket norm partials (zero_reduce_bucket with launch overlap: one region of
+// kBucketPartials per bucket, so that the reductions of consecutive buckets never share one)
+// follow the schedule.
+constexpr int kBucketPartials = 1216;  // 152 SMs x 8 CTAs of the norm pass that writes the average
+inline int64_t scratch_bucket_partials(int64_t n_buckets) {
     return (scratch_schedule(n_buckets) + (int64_t)sizeof(ScheduleEntry) * ZERO_MAX_SCHEDULE + 255) / 256 * 256;
+}
+inline int64_t scratch_bytes(int64_t n_buckets) {
+    return (scratch_bucket_partials(n_buckets) + 8 * (int64_t)kBucketPartials * n_buckets + 255) / 256 * 256;
 }
 
 // Kernel variants, used as keys of the per-context launch-shape cache.
@@ -152,12 +161,14 @@ int variant_ctas_per_sm_cap(int variant);
 cudaError_t variant_blocks_per_sm(int variant, int M, int groups, int* blocks);
 
 // Launchers: `grid` CTAs of variant_threads(variant) threads on `stream`.
+// a.pdl != kPdlNone (write_ghat only): launched with programmatic stream serialization.
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
 // sched: the clip threshold is the running scheduled step's (st->cur_max_norm), not max_norm.
 cudaError_t launch_norm_final(Status* st, const double* partials, int nparts, double max_norm,
                               int clip, bool sched, cudaStream_t s);
 // One CTA: *out = sum of partials[0 .. nparts) in a fixed order.
-cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s);
+cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s,
+                                int pdl = kPdlNone);
 // sched: the AdamW scalars are the running scheduled step's (st->cur), not a.k.
 cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s);
 // a.pdl != kPdlNone (plain, unscheduled form only): launched with programmatic stream

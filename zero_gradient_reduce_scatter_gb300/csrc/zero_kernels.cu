@@ -89,8 +89,10 @@ __device__ __forceinline__ void st_u4(uint16_t* p, uint4 x) { __stcs(reinterpret
 // kPdlWaitFirst: griddepcontrol.wait (the preceding grid complete, its writes visible)
 // before any memory access, then let the next such kernel launch. kPdlWaitLast: let the
 // next kernel launch at once, do the work, and wait only before exiting, so that the
-// kernel still completes after its predecessor. The destructor runs the exit wait on every
-// return path. ON = false compiles to nothing (the kernels of ordinary launches).
+// kernel still completes after its predecessor. kPdlTriggerWait: let the next kernel launch
+// at once, then wait before any memory access (for a kernel whose successor does not depend
+// on it). The destructor runs the exit wait on every return path. ON = false compiles to
+// nothing (the kernels of ordinary launches).
 // ---------------------------------------------------------------------------------------
 template <bool ON>
 struct PdlScope {
@@ -98,6 +100,7 @@ struct PdlScope {
     __device__ __forceinline__ explicit PdlScope(int32_t m) : mode(ON ? m : (int32_t)kPdlNone) {
         if (ON && mode == kPdlWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (ON && mode != kPdlNone) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (ON && mode == kPdlTriggerWait) asm volatile("griddepcontrol.wait;" ::: "memory");
     }
     __device__ __forceinline__ ~PdlScope() {
         if (ON && mode == kPdlWaitLast) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -395,8 +398,10 @@ __device__ __forceinline__ double block_sum(double x) {
 // ---------------------------------------------------------------------------------------
 // K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool WRITE, bool GROUPED = false, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly>
+template <int MT, bool WRITE, bool GROUPED = false, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly,
+          bool PDL = false>
 __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
+    const PdlScope<PDL> pdl(a.pdl);
     SumSq acc;
     const int64_t stride = (int64_t)gridDim.x * THREADS;
     int64_t vi = a.vbeg + (int64_t)blockIdx.x * THREADS + threadIdx.x;
@@ -418,7 +423,9 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
         }
     }
     const double t = block_sum<THREADS>(acc.value());
-    if (threadIdx.x == 0 && ZG_OK(a.status, blockIdx.x < kMaxPartials, kSitePartial, blockIdx.x)) a.partials[blockIdx.x] = t;
+    if (threadIdx.x == 0 && ZG_OK(a.status, blockIdx.x < (a.part_cap > 0 ? a.part_cap : kMaxPartials), kSitePartial,
+                                  blockIdx.x))
+        a.partials[blockIdx.x] = t;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -482,7 +489,10 @@ __global__ void k_step_begin(Status* st, const ScheduleEntry* table) {
 }
 
 // Per-bucket streaming: the sum of one bucket's CTA partials into the bucket's slot.
-__global__ void __launch_bounds__(kThreads) k_sum_partials(const double* partials, int nparts, double* out) {
+template <bool PDL>
+__global__ void __launch_bounds__(kThreads) k_sum_partials(const double* partials, int nparts, double* out,
+                                                           int32_t pdl_mode) {
+    const PdlScope<PDL> pdl(pdl_mode);
     const double t = cta_sum_partials(partials, nparts);
     if (threadIdx.x == 0) *out = t;
 }
@@ -743,6 +753,12 @@ template <int MT> struct RsNormWrite {
         else return &k_rs_norm<MT, true>;
     }
 };
+template <int MT> struct RsNormWritePdl {
+    static auto fn() {
+        if constexpr (MT < 0) return &k_rs_norm<grouped_mt(MT), true, true, kThreadsRsNormWrite, true>;
+        else return &k_rs_norm<MT, true, false, kThreadsRsNormWrite, true>;
+    }
+};
 template <int MT> struct RsNormOnly {
     static auto fn() {
         if constexpr (MT < 0) return &k_rs_norm<grouped_mt(MT), false, true>;
@@ -845,6 +861,8 @@ cudaError_t variant_blocks_per_sm(int variant, int M, int groups, int* blocks) {
 }
 
 cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
+    if (write_ghat && a.pdl != kPdlNone)
+        return launch_pdl(ByM<RsNormWritePdl>::get(a.M, a.groups), grid, kThreadsRsNormWrite, s, a);
     if (write_ghat) ByM<RsNormWrite>::get(a.M, a.groups)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
     else ByM<RsNormOnly>::get(a.M, a.groups)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
     return cudaGetLastError();
@@ -866,8 +884,9 @@ cudaError_t launch_step_begin(Status* st, const ScheduleEntry* table, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s) {
-    k_sum_partials<<<1, kThreads, 0, s>>>(partials, nparts, out);
+cudaError_t launch_sum_partials(const double* partials, int nparts, double* out, cudaStream_t s, int pdl) {
+    if (pdl != kPdlNone) return launch_pdl(&k_sum_partials<true>, 1, kThreads, s, partials, nparts, out, (int32_t)pdl);
+    k_sum_partials<false><<<1, kThreads, 0, s>>>(partials, nparts, out, (int32_t)kPdlNone);
     return cudaGetLastError();
 }
 
