@@ -79,8 +79,22 @@ __device__ __forceinline__ uint4 ld_grad(const uint16_t* p) {
     else if constexpr (PATH == kLoadReadOnly) return __ldg(reinterpret_cast<const uint4*>(p));
     else return ld_u4(p);
 }
-__device__ __forceinline__ float4 ld_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ void st_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
+// fp32 vector accesses under a cache policy (CachePolicy; chosen per kernel by measurement).
+template <int P>
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+    if constexpr (P == kCacheStreaming) return __ldcs(q);
+    else if constexpr (P == kCacheAllLevels) return __ldca(q);
+    else if constexpr (P == kCacheGlobal) return __ldcg(q);
+    else return *q;
+}
+template <int P>
+__device__ __forceinline__ void st_f4(float* p, float4 x) {
+    float4* q = reinterpret_cast<float4*>(p);
+    if constexpr (P == kCacheStreaming) __stcs(q, x);
+    else if constexpr (P == kCacheGlobal) __stcg(q, x);
+    else *q = x;
+}
 __device__ __forceinline__ void st_u4(uint16_t* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
 
 // ---------------------------------------------------------------------------------------
@@ -286,23 +300,25 @@ __device__ __forceinline__ void unpack(float4 a, float4 b, float x[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+template <int P>
 __device__ __forceinline__ void load_state(const StepArgs& a, int64_t o, float p[8], float m[8], float v[8]) {
-    float4 p0 = ld_f4(a.master + o), p1 = ld_f4(a.master + o + 4);
-    float4 m0 = ld_f4(a.m + o), m1 = ld_f4(a.m + o + 4);
-    float4 v0 = ld_f4(a.v + o), v1 = ld_f4(a.v + o + 4);
+    float4 p0 = ld_f4<P>(a.master + o), p1 = ld_f4<P>(a.master + o + 4);
+    float4 m0 = ld_f4<P>(a.m + o), m1 = ld_f4<P>(a.m + o + 4);
+    float4 v0 = ld_f4<P>(a.v + o), v1 = ld_f4<P>(a.v + o + 4);
     unpack(p0, p1, p);
     unpack(m0, m1, m);
     unpack(v0, v1, v);
 }
 
+template <int P>
 __device__ __forceinline__ void store_state(const StepArgs& a, int64_t o, const float p[8], const float m[8],
                                             const float v[8]) {
-    st_f4(a.master + o, make_float4(p[0], p[1], p[2], p[3]));
-    st_f4(a.master + o + 4, make_float4(p[4], p[5], p[6], p[7]));
-    st_f4(a.m + o, make_float4(m[0], m[1], m[2], m[3]));
-    st_f4(a.m + o + 4, make_float4(m[4], m[5], m[6], m[7]));
-    st_f4(a.v + o, make_float4(v[0], v[1], v[2], v[3]));
-    st_f4(a.v + o + 4, make_float4(v[4], v[5], v[6], v[7]));
+    st_f4<P>(a.master + o, make_float4(p[0], p[1], p[2], p[3]));
+    st_f4<P>(a.master + o + 4, make_float4(p[4], p[5], p[6], p[7]));
+    st_f4<P>(a.m + o, make_float4(m[0], m[1], m[2], m[3]));
+    st_f4<P>(a.m + o + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_f4<P>(a.v + o, make_float4(v[0], v[1], v[2], v[3]));
+    st_f4<P>(a.v + o + 4, make_float4(v[4], v[5], v[6], v[7]));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -416,8 +432,8 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
             rank_sum<MT, kGradLoadRsNorm, GROUPED>(a, o - a.gbase, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
             if (WRITE && ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatWrite, o)) {
-                st_f4(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
-                st_f4(a.ghat + o + 4, make_float4(gh[4], gh[5], gh[6], gh[7]));
+                st_f4<kGhatStoreRsNorm>(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
+                st_f4<kGhatStoreRsNorm>(a.ghat + o + 4, make_float4(gh[4], gh[5], gh[6], gh[7]));
             }
             acc.add8(gh);
         }
@@ -516,11 +532,11 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
         c.seek(o);
         float gh[8], p[8], m[8], v[8];
         if (!ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatRead, o)) continue;
-        const float4 g0 = ld_f4(a.ghat + o), g1 = ld_f4(a.ghat + o + 4);
-        load_state(a, o, p, m, v);
+        const float4 g0 = ld_f4<kGhatLoadAdamw>(a.ghat + o), g1 = ld_f4<kGhatLoadAdamw>(a.ghat + o + 4);
+        load_state<kStateLoadAdamw>(a, o, p, m, v);
         unpack(g0, g1, gh);
         adam_vec<true>(gh, s, p, m, v, k);
-        store_state(a, o, p, m, v);
+        store_state<kStateStoreAdamw>(a, o, p, m, v);
         store_params(a, c, o, c.nreal(o), p);
     }
 }
@@ -554,12 +570,12 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         float sum[8], gh[8], p[8], m[8], v[8];
         if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
         // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
-        load_state(a, o, p, m, v);
+        load_state<kStateLoadRsAdamw>(a, o, p, m, v);
         rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // grads[r] is addressed by absolute lane
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
         adam_vec<SCALE>(gh, s, p, m, v, k);
-        store_state(a, o, p, m, v);
+        store_state<kStateStoreRsAdamw>(a, o, p, m, v);
         store_params(a, c, o, nr, p);
     }
 }
