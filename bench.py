@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--workload", default=None, choices=["tiny", "gpt2s", "1p3b", "ragged", "4b"],
                     help="default: 4b (the 4B dense set) for --mode step and gather, gpt2s for --mode stream")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=6)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -501,17 +501,23 @@ def run_ours(args):
         h2d_gbs = copy_rate([(sets[0][r], host_grads[r]) for r in range(w.M)], copy_stream)
         d2h_gbs = copy_rate([(host_params, opt.params())], copy_stream)
         barrier(dist, device)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         t0 = time.perf_counter()
+        marks[0].record(stream)
         for i in range(args.e2e_steps):
             opt.step_host_overlapped(host_grads, sets[i % 2], host_params, h, copy_stream)
+            marks[i + 1].record(stream)  # after the step's parameters reached the host
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3, device)
+        e2e_step_ms = [round(marks[i].elapsed_time(marks[i + 1]), 2) for i in range(args.e2e_steps)]
+        h2d_after = copy_rate([(sets[0][r], host_grads[r]) for r in range(w.M)], copy_stream)
         e2e = {"value": world * n * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "ms_per_step": e2e_ms / args.e2e_steps, "call": "zero_step_host_overlapped",
                "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2,
                "host_gradients": (f"{w.M} pinned replicas" if distinct else
                                   f"one pinned replica copied to all {w.M} device buffers (host memory)"),
                "h2d_copy_gbs": round(h2d_gbs, 1), "d2h_copy_gbs": round(d2h_gbs, 1),
+               "h2d_copy_gbs_after": round(h2d_after, 1), "step_ms": e2e_step_ms,
                "copy_floor_ms": round(sum(g.numel() * 2 for g in host_grads) / h2d_gbs / 1e6, 2)}
         del host_grads, host_params, sets, srcs
 
