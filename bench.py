@@ -28,7 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) per fused ZeRO step"
-KERNEL_SRC = os.path.join(ROOT, "zero_gradient_reduce_scatter_gb300", "csrc", "zero_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "zero_gradient_reduce_scatter_gb300", "csrc", f)
+               for f in ("zero_kernels.cu", "zero_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -214,8 +215,13 @@ def hbm_peak():
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel sources (the kernels and the header that holds their launch shapes
+    and cache policies): an ncu traffic figure counts only while this is unchanged."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key: str, workload_key: str):
