@@ -168,12 +168,15 @@ def test_scheduled_calls_without_schedule_are_refused():
     assert e.value.code == zg.ZERO_ERR_SCHEDULE
 
 
-def test_captured_streaming_step_matches_oracle():
-    """ZeRO-2: every bucket's reduce-scatter and the scheduled apply in one graph."""
+@pytest.mark.parametrize("overlap", ["none", "buckets"])
+def test_captured_streaming_step_matches_oracle(overlap):
+    """ZeRO-2: every bucket's reduce-scatter and the scheduled apply in one graph (with
+    launch overlap, the bucket reductions are captured with programmatic dependencies)."""
     w = W.small_variant(W.workload("gpt2s"), W.ragged_numel(40, 100, 6000, 27), bucket_bytes=30000, clip=1e-3)
     dev = torch.device("cuda")
     mi = W.master_init(w, dev)
     opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+    opt.set_launch_overlap(overlap)
     nb = len(opt.buckets)
     assert nb >= 4
     p = O.plan(w.numel, w.M, w.bucket_bytes)
