@@ -132,6 +132,11 @@ constexpr int kStateLoadAdamw = kCacheAllLevels;
 constexpr int kGhatLoadAdamw = kCacheAllLevels;
 constexpr int kStateStoreAdamw = kCacheDefault;
 constexpr int kGhatStoreRsNorm = kCacheStreaming;
+// The gather's 16-byte shard loads and parameter stores: plain ones ran the full-range
+// gather of the 4B layout at 6.77-6.78 TB/s against 6.57-6.58 with evict-first ones (.ca /
+// .cg pairs 6.76); the per-bucket launches were the same under every pair (4.66-4.69 TB/s).
+constexpr int kGatherLoad = kCacheDefault;
+constexpr int kGatherStore = kCacheDefault;
 constexpr int kThreads = 256;         // CTA size of the single-CTA norm finalise
 
 // Scratch layout (bytes from the scratch base; every part 256-byte aligned).

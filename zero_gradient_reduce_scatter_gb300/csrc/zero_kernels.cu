@@ -88,6 +88,22 @@ __device__ __forceinline__ float4 ld_f4(const float* p) {
     else if constexpr (P == kCacheGlobal) return __ldcg(q);
     else return *q;
 }
+// 16-byte bf16 accesses under a cache policy (the gather's).
+template <int P>
+__device__ __forceinline__ uint4 ld_u4p(const uint16_t* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    if constexpr (P == kCacheStreaming) return __ldcs(q);
+    else if constexpr (P == kCacheAllLevels) return __ldca(q);
+    else if constexpr (P == kCacheGlobal) return __ldcg(q);
+    else return *q;
+}
+template <int P>
+__device__ __forceinline__ void st_u4p(uint16_t* p, uint4 x) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+    if constexpr (P == kCacheStreaming) __stcs(q, x);
+    else if constexpr (P == kCacheGlobal) __stcg(q, x);
+    else *q = x;
+}
 template <int P>
 __device__ __forceinline__ void st_f4(float* p, float4 x) {
     float4* q = reinterpret_cast<float4*>(p);
@@ -663,11 +679,11 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
                 const uint16_t* base = shards + (src - k);
                 if (!ZG_OK(st, src >= 0 && src + 8 <= npad, kSiteGatherSrc, src)) continue;
                 if (k == 0) {
-                    st_u4(out + d0, ld_u4(base));
+                    st_u4p<kGatherStore>(out + d0, ld_u4p<kGatherLoad>(base));
                     continue;
                 }
                 if (src - k + 8 < npad) {
-                    st_u4(out + d0, splice(ld_u4(base), ld_u4(base + 8), k));
+                    st_u4p<kGatherStore>(out + d0, splice(ld_u4p<kGatherLoad>(base), ld_u4p<kGatherLoad>(base + 8), k));
                     continue;
                 }
             }
