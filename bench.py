@@ -216,11 +216,16 @@ def hbm_peak():
 
 def kernel_sha() -> str:
     """Hash of the kernel sources (the kernels and the header that holds their launch shapes
-    and cache policies): an ncu traffic figure counts only while this is unchanged."""
+    and cache policies) with comments and blank space removed: an ncu traffic figure counts
+    only while the code is unchanged."""
+    import re
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -153,7 +153,7 @@ inline int64_t scratch_schedule(int64_t n_buckets) {
 // Per-bucket norm partials (zero_reduce_bucket with launch overlap: one region of
 // kBucketPartials per bucket, so that the reductions of consecutive buckets never share one)
 // follow the schedule.
-constexpr int kBucketPartials = 1216;  // 152 SMs x 8 CTAs of the norm pass that writes the average
+constexpr int kBucketPartials = 1216;  // the largest grid of that norm pass on GB300: 152 SMs x 8 CTAs of 256 threads
 inline int64_t scratch_bucket_partials(int64_t n_buckets) {
     return (scratch_schedule(n_buckets) + (int64_t)sizeof(ScheduleEntry) * ZERO_MAX_SCHEDULE + 255) / 256 * 256;
 }
