@@ -289,3 +289,44 @@ def test_bucket_reduced_twice_in_one_step():
     assert opt.last_norm() == ref.last_norm()
     for a, b_ in ((opt.ghat, ref.ghat), (opt.master, ref.master), (opt.params(), ref.params())):
         assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
+
+
+@pytest.mark.parametrize("ctas", [1, 7])
+def test_overlap_with_tiny_grids(ctas):
+    """Grids capped at 1 or 7 CTAs keep many overlapped bucket kernels resident at once, each
+    waiting at its end for the one before: fused bucket steps and clipped bucket reductions
+    must still equal ordinary launches bit for bit."""
+    dev = torch.device("cuda")
+    for clip in (None, 1e-3):
+        w = W.small_variant(W.workload("gpt2s"), W.ragged_numel(40, 100, 6000, 41), bucket_bytes=20000, steps=2,
+                            clip=clip)
+        mi = W.master_init(w, dev)
+        ref = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+        opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=True)
+        for o in (ref, opt):
+            o.set_max_ctas(ctas)
+        opt.set_launch_overlap("buckets")
+        nb = len(opt.buckets)
+        assert nb >= 8
+        h, _ = make_hyper(w)
+        stream = torch.cuda.Stream(device=dev)
+        for k in range(w.steps):
+            full = opt.new_grad_buffers()
+            for r in range(w.M):
+                W.fill_grads(w, r, k, full[r], opt.tensor_offsets)
+            torch.cuda.synchronize()
+            order = list(reversed(range(nb)))
+            if clip is None:
+                for b in order:
+                    ref.step_bucket(b, _bucket_slices(ref, full, b), h)
+                _ahead(opt, full, order, h, stream)
+            else:
+                for b in order:
+                    ref.reduce_bucket(b, _bucket_slices(ref, full, b))
+                ref.apply(h)
+                _reduce_ahead(opt, full, order, stream)
+                opt.apply(h, stream=stream)
+            torch.cuda.synchronize()
+            assert opt.sync_status() == 0 and ref.sync_status() == 0
+            for a, b_ in ((opt.master, ref.master), (opt.m, ref.m), (opt.v, ref.v), (opt.params(), ref.params())):
+                assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), (clip, k)
