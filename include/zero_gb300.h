@@ -378,35 +378,36 @@ int zero_set_max_ctas(zero_ctx* ctx, int ctas);
 
 /* Launch overlap of the per-bucket kernels: those of zero_step_bucket (the fused
  * reduce-scatter + AdamW of one bucket), of zero_reduce_bucket (one bucket's reduce-scatter
- * and sum of squares) and of zero_gather_bucket / zero_gather (one bucket's all-gather). The pages stream buckets one after another (ZeRO-2 reduce-scatter as
- * gradients appear, "CS336 2026 Lecture 8" Slides 23 and 26; ZeRO-3 per-module gather with
- * prefetch, Slides 24-26); each such launch is short (tens of microseconds), so the ramp-up
- * and tail of every launch cost a visible share. Overlap uses programmatic dependent launch:
- * the kernel is launched with programmatic stream serialization and may start while the
- * kernel before it on the stream is still finishing.
+ * and sum of squares) and of zero_gather_bucket / zero_gather (one bucket's all-gather).
+ * The pages stream buckets one after another (ZeRO-2 reduce-scatter as gradients appear,
+ * "CS336 2026 Lecture 8" Slides 23 and 26; ZeRO-3 per-module gather with prefetch, Slides
+ * 24-26); each such launch is short (tens of microseconds), so the ramp-up and tail of every
+ * launch cost a visible share. Overlap uses programmatic dependent launch: the kernel is
+ * launched with programmatic stream serialization and may start while the kernel before it
+ * on the stream is still finishing.
  *  ZERO_OVERLAP_NONE     ordinary launches (the default).
  *  ZERO_OVERLAP_LAUNCH   each per-bucket kernel waits for the preceding kernel to complete,
  *                        its writes visible, before its first memory access; only the
  *                        launch itself overlaps. Correct whatever precedes the call.
  *  ZERO_OVERLAP_BUCKETS  as LAUNCH, except that a per-bucket kernel that directly follows a
  *                        per-bucket kernel of the same kind from this context on the same
- *                        stream (a fused bucket step or a bucket reduction after another
- *                        bucket of the same step; a gather after a gather into a disjoint
- *                        destination) does its work at
- *                        once and waits for its predecessor only before it exits. It still
- *                        completes after its predecessor, so stream order holds for whatever
- *                        is enqueued later. The library decides this from its own launches;
- *                        the caller guarantees the rest: the kernel that the caller enqueues
- *                        on the stream directly before such a call must not write what the
- *                        call reads (gradient slices; the parameter shards) nor access what it
- *                        writes. Work ordered by an event wait (cudaStreamWaitEvent) is not
- *                        affected: that dependency is kept whole. The first bucket of every
- *                        step, and every step of a schedule (zero_step_bucket_scheduled),
- *                        waits for its predecessor as under LAUNCH. Under either mode each
- *                        bucket reduction keeps its norm partials in a region of the scratch
- *                        buffer of its own (zero_plan sizes the scratch for it).
- * With overlap, per-kernel event timing (zero_set_timing) brackets launches that may run
- * concurrently; time the whole sequence instead. Errors: BAD_CONTEXT, INVALID_ARG. */
+ *                        stream does its work at once and waits for its predecessor only
+ *                        before it exits: a fused bucket step or a bucket reduction after
+ *                        another bucket of the same step (not the first bucket of a step, not
+ *                        a bucket reduced a second time), a gather after a gather into a
+ *                        disjoint destination. It still completes after its predecessor, so
+ *                        stream order holds for whatever is enqueued later. The library
+ *                        decides this from its own launches; the caller guarantees the rest:
+ *                        the kernel that the caller enqueues on the stream directly before
+ *                        such a call must not write what the call reads (gradient slices;
+ *                        the parameter shards) nor access what it writes. Work ordered by an
+ *                        event wait (cudaStreamWaitEvent) is not affected: that dependency is
+ *                        kept whole.
+ * zero_step_bucket_scheduled always launches ordinary kernels. Under either overlap mode each
+ * bucket reduction keeps its norm partials in a region of the scratch buffer of its own
+ * (zero_plan sizes the scratch for it). With overlap, per-kernel event timing
+ * (zero_set_timing) brackets launches that may run concurrently; time the whole sequence
+ * instead. Errors: BAD_CONTEXT, INVALID_ARG. */
 #define ZERO_OVERLAP_NONE    0
 #define ZERO_OVERLAP_LAUNCH  1
 #define ZERO_OVERLAP_BUCKETS 2
