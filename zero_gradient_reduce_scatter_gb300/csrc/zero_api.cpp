@@ -338,7 +338,9 @@ void note_chain(zero_ctx* c, int kind, cudaStream_t s, uintptr_t lo = 0, uintptr
 
 // out[0 .. count) = parameters of unpadded indices [u0, u0 + count). may_overlap: the
 // launch may overlap a directly preceding gather into a disjoint destination.
-int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStream_t s, bool may_overlap = false) {
+// b_first / b_end: the buckets the indices lie in (b_end 0: any).
+int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStream_t s, bool may_overlap = false,
+                 int64_t b_first = 0, int64_t b_end = 0) {
     const int grid = grid_for(c, zg::kVarGather, count / 8 + 2);
     const uintptr_t lo = reinterpret_cast<uintptr_t>(out), hi = lo + 2 * (uintptr_t)(count > 0 ? count : 0);
     const bool disjoint = hi <= c->chain_lo || lo >= c->chain_hi;
@@ -347,7 +349,7 @@ int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStre
     {
         Timed tm(c, ZERO_K_GATHER, s);
         e = zg::launch_gather((const uint16_t*)c->bufs.param_shards, out, c->dev_buckets, (int64_t)c->buckets.size(),
-                              c->npad, u0, count, c->status, grid, s, pdl);
+                              c->npad, u0, count, c->status, grid, s, pdl, b_first, b_end);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     if (count > 0 && pdl != zg::kPdlNone) note_chain(c, ZERO_K_GATHER, s, lo, hi);
@@ -599,6 +601,8 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     a.vend = e.end / 8;
     a.gbase = e.off;
     a.gext = e.end - e.off;
+    a.b_first = bucket;
+    a.b_end = bucket + 1;
     int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
     double* parts = c->partials;
     int sum_pdl = zg::kPdlNone;
@@ -644,6 +648,8 @@ static int step_one_bucket(zero_ctx* c, int64_t bucket, const void* const* grads
     a.vbeg = e.off / 8;
     a.vend = e.end / 8;
     a.gext = e.end;
+    a.b_first = bucket;
+    a.b_end = bucket + 1;
     if (!sched) a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
     int rc;
     if (sched && c->n_bucket_done == 0 && (rc = launch_step_begin(c, s))) return rc;  // once per step
@@ -659,7 +665,7 @@ static int step_one_bucket(zero_ctx* c, int64_t bucket, const void* const* grads
     if (err != cudaSuccess) return cuda_fail(err);
     if (a.pdl != zg::kPdlNone) note_chain(c, ZERO_K_RS_ADAMW, s);
     if (c->cfg.gather == ZERO_GATHER_SHARDS) {  // the bucket's all-gather
-        rc = gather_range(c, e.uoff, e.n, (uint16_t*)c->bufs.param_full + e.uoff, s);
+        rc = gather_range(c, e.uoff, e.n, (uint16_t*)c->bufs.param_full + e.uoff, s, false, bucket, bucket + 1);
         if (rc) return rc;
     }
     c->bucket_done[(size_t)bucket] = 1;
@@ -952,7 +958,8 @@ int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
         u0 = c->buckets[(size_t)bucket].uoff;
         count = c->buckets[(size_t)bucket].n;
     }
-    return gather_range(c, u0, count, out + u0, (cudaStream_t)stream, true);
+    return gather_range(c, u0, count, out + u0, (cudaStream_t)stream, true, bucket >= 0 ? bucket : 0,
+                        bucket >= 0 ? bucket + 1 : 0);
 }
 
 int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
@@ -963,7 +970,7 @@ int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     const zg::Bucket& e = c->buckets[(size_t)bucket];
-    return gather_range(c, e.uoff, e.n, (uint16_t*)dst, (cudaStream_t)stream, true);
+    return gather_range(c, e.uoff, e.n, (uint16_t*)dst, (cudaStream_t)stream, true, bucket, bucket + 1);
 }
 
 int zero_bucket_info(zero_ctx* c, int64_t bucket, int64_t* uoff, int64_t* n) {

@@ -80,6 +80,8 @@ struct StepArgs {
     double* partials;     // one fp64 partial sum of squares per CTA of the norm pass
     int32_t pdl;          // PdlMode of kernels launched with programmatic stream serialization
     int32_t part_cap;     // partial sums `partials` holds (0: kMaxPartials; bounds checks)
+    int64_t b_first;      // the launch's lanes lie in buckets [b_first, b_end) (b_end 0: all):
+    int64_t b_end;        // its threads search only those for their first bucket
 };
 
 // Programmatic dependent launch of the per-bucket kernels (zero_set_launch_overlap).
@@ -205,10 +207,11 @@ cudaError_t launch_schedule_install(Status* st, int64_t t, int64_t count, cudaSt
 cudaError_t launch_step_begin(Status* st, const ScheduleEntry* table, cudaStream_t s);
 // out[d] = bf16 parameter of unpadded index u0 + d, d < count, from the padded shards
 // (out needs only 2-byte alignment).
-// pdl != kPdlNone: launched with programmatic stream serialization in that mode.
+// pdl != kPdlNone: launched with programmatic stream serialization in that mode. The
+// indices lie in buckets [b_first, b_end) (b_end 0: all buckets).
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb,
                           int64_t npad, int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s,
-                          int pdl = kPdlNone);
+                          int pdl = kPdlNone, int64_t b_first = 0, int64_t b_end = 0);
 // State from unpadded fp32 vectors (m_init / v_init may be null: zeros), plus bf16 copies.
 cudaError_t launch_init(const float* master_init, const float* m_init, const float* v_init,
                         float* master, float* m, float* v, uint16_t* full, uint16_t* shards,

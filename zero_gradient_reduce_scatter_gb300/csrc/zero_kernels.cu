@@ -146,11 +146,14 @@ struct Cursor {
     int64_t b;
     Bucket e;
 
-    // Last bucket whose padded start is <= lane (empty buckets share their successor's start).
-    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t lane) {
+    // Last bucket whose padded start is <= lane (empty buckets share their successor's start),
+    // searched among buckets [first, end) (end <= 0: all); a launch over one bucket passes
+    // just that one, and its threads then need no search of the table.
+    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t lane, int64_t first = 0,
+                                         int64_t end = 0) {
         tab = t;
         nb = n;
-        int64_t lo = 0, hi = n - 1;
+        int64_t lo = first, hi = (end > 0 ? end : n) - 1;
         while (lo < hi) {
             int64_t mid = (lo + hi + 1) >> 1;
             if (tab[mid].off <= lane) lo = mid;
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     int64_t vi = a.vbeg + (int64_t)blockIdx.x * THREADS + threadIdx.x;
     if (vi < a.vend) {
         Cursor c;
-        c.init(a.buckets, a.nb, vi * 8);
+        c.init(a.buckets, a.nb, vi * 8, a.b_first, a.b_end);
         for (; vi < a.vend; vi += stride) {
             const int64_t o = vi * 8;
             c.seek(o);
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
     int64_t vi = a.vbeg + (int64_t)blockIdx.x * kThreadsRsAdamw + threadIdx.x;
     if (vi >= a.vend) return;
     Cursor c;
-    c.init(a.buckets, a.nb, vi * 8);
+    c.init(a.buckets, a.nb, vi * 8, a.b_first, a.b_end);
     for (; vi < a.vend; vi += stride) {
         const int64_t o = vi * 8;
         c.seek(o);
@@ -602,9 +605,11 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
 // indices [u_begin, u_end). Work item: 8 destination elements (one 16-byte store). When
 // its source run is unaligned by k elements, two aligned 16-byte loads are spliced.
 // ---------------------------------------------------------------------------------------
-// Last bucket whose unpadded start is <= u (buckets are never empty for a valid plan).
-__device__ __forceinline__ int64_t bucket_of_unpadded(const Bucket* tab, int64_t nb, int64_t u) {
-    int64_t lo = 0, hi = nb - 1;
+// Last bucket among [first, end) whose unpadded start is <= u (end <= 0: all buckets;
+// buckets are never empty for a valid plan).
+__device__ __forceinline__ int64_t bucket_of_unpadded(const Bucket* tab, int64_t nb, int64_t u, int64_t first,
+                                                      int64_t end) {
+    int64_t lo = first, hi = (end > 0 ? end : nb) - 1;
     while (lo < hi) {
         const int64_t mid = (lo + hi + 1) >> 1;
         if (tab[mid].uoff <= u) lo = mid;
@@ -641,10 +646,10 @@ struct UCursor {
     const Bucket* tab;
     int64_t nb, b;
     Bucket e;
-    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t u) {
+    __device__ __forceinline__ void init(const Bucket* t, int64_t n, int64_t u, int64_t first, int64_t end) {
         tab = t;
         nb = n;
-        b = bucket_of_unpadded(t, n, u);
+        b = bucket_of_unpadded(t, n, u, first, end);
         e = tab[b];
     }
     __device__ __forceinline__ void seek(int64_t u) {
@@ -659,7 +664,7 @@ template <bool PDL>
 __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __restrict__ shards,
                                                      uint16_t* __restrict__ out, const Bucket* tab, int64_t nb,
                                                      int64_t npad, int64_t u0, int64_t count, Status* st,
-                                                     int32_t pdl_mode) {
+                                                     int64_t b_first, int64_t b_end, int32_t pdl_mode) {
     const PdlScope<PDL> pdl(pdl_mode);
     const int64_t a0 = (int64_t)((reinterpret_cast<uintptr_t>(out) >> 1) & 7);
     const int64_t nslots = (count + a0 + 7) >> 3;
@@ -667,7 +672,7 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
     int64_t w = (int64_t)blockIdx.x * kThreadsGather + threadIdx.x;
     if (w >= nslots) return;
     UCursor c;
-    c.init(tab, nb, u0 + (w * 8 - a0 > 0 ? w * 8 - a0 : 0));
+    c.init(tab, nb, u0 + (w * 8 - a0 > 0 ? w * 8 - a0 : 0), b_first, b_end);
     for (; w < nslots; w += stride) {
         const int64_t d0 = w * 8 - a0;  // first output element of the slot (may be < 0)
         if (d0 >= 0 && d0 + 8 <= count) {
@@ -944,12 +949,14 @@ cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int
 }
 
 cudaError_t launch_gather(const uint16_t* shards, uint16_t* out, const Bucket* buckets, int64_t nb, int64_t npad,
-                          int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s, int pdl) {
+                          int64_t u0, int64_t count, Status* st, int grid, cudaStream_t s, int pdl,
+                          int64_t b_first, int64_t b_end) {
     if (count <= 0) return cudaSuccess;
     if (pdl != kPdlNone)
         return launch_pdl(&k_gather<true>, grid, kThreadsGather, s, shards, out, buckets, nb, npad, u0, count, st,
-                          (int32_t)pdl);
-    k_gather<false><<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count, st, (int32_t)kPdlNone);
+                          b_first, b_end, (int32_t)pdl);
+    k_gather<false><<<grid, kThreadsGather, 0, s>>>(shards, out, buckets, nb, npad, u0, count, st, b_first, b_end,
+                                                    (int32_t)kPdlNone);
     return cudaGetLastError();
 }
 
