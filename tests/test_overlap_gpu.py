@@ -330,3 +330,76 @@ def test_overlap_with_tiny_grids(ctas):
             assert opt.sync_status() == 0 and ref.sync_status() == 0
             for a, b_ in ((opt.master, ref.master), (opt.m, ref.m), (opt.v, ref.v), (opt.params(), ref.params())):
                 assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), (clip, k)
+
+
+@pytest.mark.parametrize("clip", [None, 1.0])
+def test_full_size_streamed_step_matches_ordinary_launches(clip):
+    """The GPT-2-small shaped workload at full size (123,570,432 parameters, M=8, 25 MiB
+    buckets), streamed in backward order with overlapped launches as bench.py --mode stream
+    times it: two steps bit-identical to the same steps with ordinary launches (the fused
+    bucket steps without clipping; bucket reductions + one apply with clipping)."""
+    w = W.workload("gpt2s")
+    if clip is not None:
+        w = W.small_variant(w, w.numel, clip=clip, name=w.name)
+    dev = torch.device("cuda")
+    mi = W.master_init(w, dev)
+    ref = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=clip is not None)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, mi, bucket_bytes=w.bucket_bytes, ghat_buffer=clip is not None)
+    opt.set_launch_overlap("buckets")
+    nb = len(opt.buckets)
+    assert nb == 9
+    h, _ = make_hyper(w)
+    sig = W.sigmas(w)
+    stream = torch.cuda.Stream(device=dev)
+    order = list(reversed(range(nb)))
+    for k in range(2):
+        full = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, full[r], opt.tensor_offsets, sig)
+        torch.cuda.synchronize()
+        if clip is None:
+            for b in order:
+                ref.step_bucket(b, _bucket_slices(ref, full, b), h)
+            _ahead(opt, full, order, h, stream)
+        else:
+            for b in order:
+                ref.reduce_bucket(b, _bucket_slices(ref, full, b))
+            ref.apply(h)
+            _reduce_ahead(opt, full, order, stream)
+            opt.apply(h, stream=stream)
+        torch.cuda.synchronize()
+        assert opt.sync_status() == 0 and ref.sync_status() == 0
+        if clip is not None:
+            assert opt.last_norm() == ref.last_norm()
+        for a, b_ in ((opt.master, ref.master), (opt.m, ref.m), (opt.v, ref.v), (opt.params(), ref.params())):
+            assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), (clip, k)
+        del full
+
+
+def test_full_size_prefetched_gather_sweep():
+    """The 4B workload at full size (4,092,982,400 parameters, M=4, ZeRO-3 shards, 25 MiB
+    buckets: 129 buckets) after one step: the overlapped prefetched sweep, as bench.py
+    --mode gather times it, rebuilds every parameter bit for bit."""
+    import dataclasses
+    w = dataclasses.replace(W.workload("4b"), bucket_bytes=25 * 1024 * 1024)
+    dev = torch.device("cuda")
+    opt = zg.ZeroOptimizer(w.numel, w.M, 3, W.master_init(w, dev), bucket_bytes=w.bucket_bytes, gather="shards")
+    opt.set_launch_overlap("buckets")
+    nb = len(opt.buckets)
+    assert nb == 129
+    h, _ = make_hyper(w)
+    grads = opt.new_grad_buffers()
+    sig = W.sigmas(w)
+    for r in range(w.M):
+        W.fill_grads(w, r, 0, grads[r], opt.tensor_offsets, sig)
+    opt.step(grads, h)
+    del grads
+    check = torch.full((opt.sizes["n"],), -1, dtype=torch.int16, device=dev)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    for b, params in opt.prefetched_buckets(list(range(nb)), stream=stream, side_stream=side):
+        u0, n = opt.bucket_range(b)
+        check[u0:u0 + n].copy_(params.view(torch.int16))
+    torch.cuda.synchronize()
+    assert opt.sync_status() == 0
+    assert torch.equal(check, opt.params().view(torch.int16))
