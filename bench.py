@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="step and stream modes: capture one step (scalars from a device schedule) in a CUDA "
-                         "graph and time its replays; the roofline then covers the whole step")
+                         "graph and time its replays; gather mode: capture one prefetched sweep; the roofline "
+                         "then covers the whole step or sweep")
     ap.add_argument("--cpu-procs", type=int, default=0,
                     help="oracle processes for the CPU baseline and the reference arm (0 = one per host core)")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
@@ -796,18 +797,30 @@ def run_gather(args):
 
     overlapped = args.overlap != "none"
     opt.set_launch_overlap(args.overlap)
+    graph = None
+    if args.graph:
+        # one sweep captured in a CUDA graph: the prefetch's cross-stream event waits become
+        # graph edges; each replay gathers the shards as they are then
+        sweep()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap_side = torch.cuda.Stream(device=device)
+        with torch.cuda.graph(graph):
+            for _b, _params in opt.prefetched_buckets(order, stream=torch.cuda.current_stream(), side_stream=cap_side):
+                pass
+        sweep = graph.replay
     for _ in range(args.warmup):
         sweep()
     torch.cuda.synchronize()
     # with overlap, per-launch events would bracket launches that overlap: the region runs
     # untimed and the roofline covers the whole sweep
-    opt.set_timing(not overlapped)
+    opt.set_timing(not overlapped and graph is None)
     opt.kernel_times()
     ms, clk, step_ms = _timed_region(sweep, args.steps, stream, dist, device)
     kt = opt.kernel_times()
     n = w.N
     peak, kind = hbm_peak()
-    if overlapped:
+    if overlapped or graph is not None:
         g_ms, g_cnt = ms, nb * args.steps
     else:
         g_ms, g_cnt = kt["gather"]
@@ -821,8 +834,9 @@ def run_gather(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
                        "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead",
-                       "launch_overlap": args.overlap},
-            "roofline": {"bound": "hbm", "kernel": "gather" + (f" (whole sweep, {args.overlap}-overlapped launches)"
+                       "launch_overlap": args.overlap, "cuda_graph": graph is not None},
+            "roofline": {"bound": "hbm", "kernel": "gather" + (" (whole sweep, CUDA graph replay)" if graph is not None
+                                                               else f" (whole sweep, {args.overlap}-overlapped launches)"
                                                                if overlapped else ""),
                          "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": kind,

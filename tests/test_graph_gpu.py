@@ -18,7 +18,7 @@ import torch
 import oracle as O
 import workloads as W
 import zero_gradient_reduce_scatter_gb300 as zg
-from parity_util import REL_NORM, bf16_ulp_diff, f32, state_errors, u16
+from parity_util import REL_NORM, bf16_ulp_diff, f32, make_hyper, state_errors, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -232,3 +232,36 @@ def test_captured_fused_bucket_steps_match_oracle(gather):
         assert np.array_equal(u16(opt.params()), full)
         for name, buf in (("master", opt.master), ("mom", opt.m), ("var", opt.v)):
             assert np.array_equal(f32(buf).view(np.uint32), O.flat_state(p, st, name).view(np.uint32)), name
+
+
+@pytest.mark.parametrize("overlap", ["none", "buckets"])
+def test_captured_prefetched_gather_sweep(overlap):
+    """ZeRO-3: one prefetched per-bucket gather sweep (side stream, two transient buffers,
+    the consumer copying each bucket out) captured in a CUDA graph; after every step a
+    replay rebuilds the parameters of that step bit for bit."""
+    w = W.small_variant(W.workload("ragged"), W.ragged_numel(40, 200, 9000, 43), bucket_bytes=20000, steps=3)
+    dev = torch.device("cuda")
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev), bucket_bytes=w.bucket_bytes,
+                           gather="shards")
+    opt.set_launch_overlap(overlap)
+    nb = len(opt.buckets)
+    assert nb > 6
+    h, _ = make_hyper(w)
+    check = torch.full((opt.sizes["n"],), -1, dtype=torch.int16, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for b, params in opt.prefetched_buckets(list(range(nb)), stream=torch.cuda.current_stream(), side_stream=side):
+            u0, n = opt.bucket_range(b)
+            check[u0:u0 + n].copy_(params.view(torch.int16))
+    for k in range(w.steps):
+        grads = opt.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, grads[r], opt.tensor_offsets)
+        opt.step(grads, h)
+        check.fill_(-1)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert opt.sync_status() == 0
+        assert torch.equal(check, opt.params().view(torch.int16)), k
