@@ -795,7 +795,6 @@ def run_gather(args):
         for _b, _params in opt.prefetched_buckets(order, stream=stream, side_stream=side):
             pass
 
-    overlapped = args.overlap != "none"
     opt.set_launch_overlap(args.overlap)
     graph = None
     if args.graph:
@@ -812,18 +811,14 @@ def run_gather(args):
     for _ in range(args.warmup):
         sweep()
     torch.cuda.synchronize()
-    # with overlap, per-launch events would bracket launches that overlap: the region runs
-    # untimed and the roofline covers the whole sweep
-    opt.set_timing(not overlapped and graph is None)
-    opt.kernel_times()
+    # the two buffers' gathers run on two side streams and overlap one another (and, with
+    # launch overlap, their launches too): per-launch events would bracket concurrent
+    # launches, so the region runs untimed and the roofline covers the whole sweep
+    opt.set_timing(False)
     ms, clk, step_ms = _timed_region(sweep, args.steps, stream, dist, device)
-    kt = opt.kernel_times()
     n = w.N
     peak, kind = hbm_peak()
-    if overlapped or graph is not None:
-        g_ms, g_cnt = ms, nb * args.steps
-    else:
-        g_ms, g_cnt = kt["gather"]
+    g_ms, g_cnt = ms, nb * args.steps
     achieved = 4 * n * args.steps / (g_ms / 1e3) / 1e9
     if rank == 0:
         print(json.dumps({
@@ -833,11 +828,11 @@ def run_gather(args):
             "ms_per_step_min": step_ms["min"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
-                       "bucket_bytes": w.bucket_bytes, "prefetch": "side stream, one bucket ahead",
+                       "bucket_bytes": w.bucket_bytes,
+                       "prefetch": "one bucket ahead, two transient buffers, a side stream per buffer",
                        "launch_overlap": args.overlap, "cuda_graph": graph is not None},
-            "roofline": {"bound": "hbm", "kernel": "gather" + (" (whole sweep, CUDA graph replay)" if graph is not None
-                                                               else f" (whole sweep, {args.overlap}-overlapped launches)"
-                                                               if overlapped else ""),
+            "roofline": {"bound": "hbm", "kernel": "gather (whole sweep" + (", CUDA graph replay" if graph is not None
+                                                                         else f", {args.overlap} launch overlap") + ")",
                          "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": kind,
                          "alg_bytes_per_param": 4, "avg_launch_ms": round(g_ms / max(g_cnt, 1), 4)},

@@ -392,16 +392,22 @@ class ZeroOptimizer:
         """ZeRO-3 just-in-time parameters with one-bucket-ahead prefetch.
 
         Yields (bucket, params) in `order`; `params` (bf16, the bucket's n_b values) is ready
-        for work queued on `stream` when yielded. The gather of the next bucket runs on
-        `side_stream` meanwhile, into the other of two transient buffers; a buffer is reused
+        for work queued on `stream` when yielded. The gather of the next bucket runs on a
+        side stream meanwhile, into the other of two transient buffers; a buffer is reused
         only after the work the consumer queued on `stream` before asking for the next
-        bucket has finished with it.
+        bucket has finished with it. Each buffer has a side stream of its own (`side_stream`
+        may be one stream or a pair; the second is made when not given), so consecutive
+        gathers do not wait for each other: each waits only for its buffer's last consumer,
+        and one buffer's gather runs while the other's waits.
         """
         order = list(order)
         if not order:
             return
         stream = stream or torch.cuda.current_stream()
-        side = side_stream or torch.cuda.Stream(device=self.device)
+        if isinstance(side_stream, (tuple, list)):
+            sides = list(side_stream)
+        else:
+            sides = [side_stream or torch.cuda.Stream(device=self.device), torch.cuda.Stream(device=self.device)]
         cap = max(self.buckets[b][1] for b in order)
         bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(2)]
         ready = [torch.cuda.Event() for _ in range(2)]
@@ -411,9 +417,9 @@ class ZeroOptimizer:
 
         def issue(i):
             slot = i % 2
-            side.wait_event(free[slot])
-            self.gather_bucket(order[i], bufs[slot], stream=side)
-            ready[slot].record(side)
+            sides[slot].wait_event(free[slot])
+            self.gather_bucket(order[i], bufs[slot], stream=sides[slot])
+            ready[slot].record(sides[slot])
 
         issue(0)
         for i, b in enumerate(order):
