@@ -8,7 +8,6 @@ import subprocess
 import sys
 import time
 
-import pytest
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))

@@ -256,7 +256,7 @@ def test_overlapped_bucket_reductions_match_ordinary_launches(mode, producer, gr
         for a, b_ in ((opt.ghat, ref.ghat), (opt.master, ref.master), (opt.m, ref.m), (opt.v, ref.v),
                       (opt.params(), ref.params())):
             assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), k
-        fullp, norm, _, rc = O.zero_step(p, st, [u16(g) for g in full], oh)
+        _, norm, _, rc = O.zero_step(p, st, [u16(g) for g in full], oh)
         assert rc == 0
         assert np.array_equal(f32(opt.ghat).view(np.uint32), O.flat_state(p, st, "ghat").view(np.uint32)), k
         assert abs(opt.last_norm()[0] - norm) <= REL_NORM * norm
