@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--overlap", default="buckets", choices=["none", "launch", "buckets"],
                     help="--mode stream and gather: programmatic launch overlap of the per-bucket "
                          "kernels (zero_set_launch_overlap); the roofline then covers the whole step or sweep")
+    ap.add_argument("--prefetch-buffers", type=int, default=4,
+                    help="--mode gather: transient buffers of the prefetch (buckets gathered ahead + 1)")
     ap.add_argument("--bucket-mib", type=float, default=25.0,
                     help="bucket size for --mode gather when the workload has none")
     ap.add_argument("--max-params", type=int, default=0,
@@ -791,7 +793,8 @@ def run_gather(args):
     order = list(range(nb))
 
     def sweep():
-        for _b, _params in opt.prefetched_buckets(order, stream=stream, side_stream=side):
+        for _b, _params in opt.prefetched_buckets(order, stream=stream, side_stream=side,
+                                                  buffers=args.prefetch_buffers):
             pass
 
     opt.set_launch_overlap(args.overlap)
@@ -804,7 +807,8 @@ def run_gather(args):
         graph = torch.cuda.CUDAGraph()
         cap_side = torch.cuda.Stream(device=device)
         with torch.cuda.graph(graph):
-            for _b, _params in opt.prefetched_buckets(order, stream=torch.cuda.current_stream(), side_stream=cap_side):
+            for _b, _params in opt.prefetched_buckets(order, stream=torch.cuda.current_stream(), side_stream=cap_side,
+                                                      buffers=args.prefetch_buffers):
                 pass
         sweep = graph.replay
     for _ in range(args.warmup):
@@ -828,7 +832,8 @@ def run_gather(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "params": n, "M": w.M, "stage": 3, "buckets": nb,
                        "bucket_bytes": w.bucket_bytes,
-                       "prefetch": "one bucket ahead, two transient buffers, a side stream per buffer",
+                       "prefetch": f"{args.prefetch_buffers - 1} bucket(s) ahead, {args.prefetch_buffers} transient "
+                                   "buffers, a side stream per buffer",
                        "launch_overlap": args.overlap, "cuda_graph": graph is not None},
             "roofline": {"bound": "hbm", "kernel": "gather (whole sweep" + (", CUDA graph replay" if graph is not None
                                                                          else f", {args.overlap} launch overlap") + ")",

@@ -127,8 +127,8 @@ def test_overlapped_bucket_steps_match_oracle(mode, producer, stage, gather, gro
             assert np.array_equal(f32(buf).view(np.uint32), O.flat_state(p, st, name).view(np.uint32)), (k, name)
 
 
-@pytest.mark.parametrize("order", ["forward", "backward"])
-def test_overlapped_prefetched_gather(order):
+@pytest.mark.parametrize("order,buffers", [("forward", 2), ("backward", 2), ("forward", 3), ("backward", 4)])
+def test_overlapped_prefetched_gather(order, buffers):
     """ZeRO-3 gathers on a side stream, one bucket ahead, into two transient buffers that a
     slow consumer holds: a gather overlaps the previous gather but never overwrites a buffer
     before the consumer's event says it is free. Three sweeps with a step between each."""
@@ -149,7 +149,7 @@ def test_overlapped_prefetched_gather(order):
             W.fill_grads(w, r, k, grads[r], opt.tensor_offsets)
         opt.step(grads, h)
         check = torch.full((opt.sizes["n"],), -1, dtype=torch.int16, device=dev)
-        for b, params in opt.prefetched_buckets(seq, stream=stream, side_stream=side):
+        for b, params in opt.prefetched_buckets(seq, stream=stream, side_stream=side, buffers=buffers):
             torch.cuda._sleep(100_000)  # a slow "module" keeps the buffer busy
             u0, n = opt.bucket_range(b)
             check[u0:u0 + n].copy_(params.view(torch.int16))

@@ -388,44 +388,74 @@ class ZeroOptimizer:
         _check(_lib().zero_bucket_info(self._ctx, bucket, ctypes.byref(u), ctypes.byref(n)), "zero_bucket_info")
         return u.value, n.value
 
-    def prefetched_buckets(self, order, stream=None, side_stream=None):
-        """ZeRO-3 just-in-time parameters with one-bucket-ahead prefetch.
+    def _side_streams(self, count: int, exclude) -> list:
+        """`count` distinct side streams kept by this optimizer (made once, reused by later
+        calls), none of them the same CUDA stream as any in `exclude`."""
+        if count <= 0:
+            return []
+        taken = {int(x.cuda_stream) for x in exclude}
+        pool = getattr(self, "_prefetch_streams", None)
+        if pool is None:
+            pool = self._prefetch_streams = []
+        out = []
+        for x in pool:
+            if len(out) < count and int(x.cuda_stream) not in taken:
+                out.append(x)
+                taken.add(int(x.cuda_stream))
+        for _ in range(64):  # torch hands out pool streams in turn; skip ones already taken
+            if len(out) == count:
+                break
+            x = torch.cuda.Stream(device=self.device)
+            if int(x.cuda_stream) not in taken and all(int(x.cuda_stream) != int(y.cuda_stream) for y in pool):
+                pool.append(x)
+                out.append(x)
+                taken.add(int(x.cuda_stream))
+        if len(out) < count:
+            raise RuntimeError(f"could not find {count} distinct side streams")
+        return out
+
+    def prefetched_buckets(self, order, stream=None, side_stream=None, buffers: int = 2):
+        """ZeRO-3 just-in-time parameters with prefetch.
 
         Yields (bucket, params) in `order`; `params` (bf16, the bucket's n_b values) is ready
-        for work queued on `stream` when yielded. The gather of the next bucket runs on a
-        side stream meanwhile, into the other of two transient buffers; a buffer is reused
-        only after the work the consumer queued on `stream` before asking for the next
-        bucket has finished with it. Each buffer has a side stream of its own (`side_stream`
-        may be one stream or a pair; the second is made when not given), so consecutive
-        gathers do not wait for each other: each waits only for its buffer's last consumer,
-        and one buffer's gather runs while the other's waits.
+        for work queued on `stream` when yielded. The gathers of the next `buffers - 1`
+        buckets run on side streams meanwhile, each into a transient buffer of its own
+        (`buffers` of them, used in turn); a buffer is reused only after the work the consumer
+        queued on `stream` while it held that buffer has finished with it. Each buffer has a
+        side stream of its own (`side_stream` may be one stream or a sequence; missing ones
+        are made), so consecutive gathers do not wait for each other: each waits only for its
+        buffer's last consumer, and another buffer's gather runs while it waits.
         """
         order = list(order)
         if not order:
             return
+        if buffers < 2:
+            raise ValueError("buffers must be at least 2")
         stream = stream or torch.cuda.current_stream()
         if isinstance(side_stream, (tuple, list)):
             sides = list(side_stream)
         else:
-            sides = [side_stream or torch.cuda.Stream(device=self.device), torch.cuda.Stream(device=self.device)]
+            sides = [side_stream] if side_stream is not None else []
+        sides += self._side_streams(buffers - len(sides), exclude=[stream] + sides)
         cap = max(self.buckets[b][1] for b in order)
-        bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(2)]
-        ready = [torch.cuda.Event() for _ in range(2)]
-        free = [torch.cuda.Event() for _ in range(2)]
-        for i in range(2):
+        bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(buffers)]
+        ready = [torch.cuda.Event() for _ in range(buffers)]
+        free = [torch.cuda.Event() for _ in range(buffers)]
+        for i in range(buffers):
             free[i].record(stream)
 
         def issue(i):
-            slot = i % 2
+            slot = i % buffers
             sides[slot].wait_event(free[slot])
             self.gather_bucket(order[i], bufs[slot], stream=sides[slot])
             ready[slot].record(sides[slot])
 
-        issue(0)
+        for i in range(min(buffers - 1, len(order))):
+            issue(i)
         for i, b in enumerate(order):
-            if i + 1 < len(order):
-                issue(i + 1)
-            slot = i % 2
+            if i + buffers - 1 < len(order):
+                issue(i + buffers - 1)
+            slot = i % buffers
             stream.wait_event(ready[slot])
             yield b, bufs[slot][:self.buckets[b][1]]
             free[slot].record(stream)
