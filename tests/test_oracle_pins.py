@@ -633,3 +633,44 @@ def test_hsdp_one_rank_per_group_is_plain_dp():
     full, norm, s, _ = O.zero_step(p, st, [p.pad(g) for g in gs], h)
     full_dp, norm_dp, s_dp, _ = O.naive_dp_step(dp, gs, h)
     assert norm == norm_dp and np.array_equal(full, full_dp)
+
+
+@pytest.mark.parametrize("stage_a,stage_b,clip", [(3, 1, True), (2, 3, False), (1, 2, True)])
+def test_resume_and_reshard_equal_uninterrupted_run(stage_a, stage_b, clip):
+    """Checkpoint, resume and reshard, in the oracle alone: five steps of one job equal two
+    steps, the unpadded state (master, m, v) and the step count handed to a job of another
+    rank count, stage and bucket size, then three steps, bit for bit (norms, scales,
+    parameters, state). Every rank holds the same gradient and both rank counts (4, 2) are
+    powers of two, so the averaged gradient is that gradient exactly in both jobs; the
+    flat real-lane order, and so the norm's summation order, does not depend on the layout."""
+    rng = np.random.default_rng(70 + stage_a * 3 + stage_b)
+    numel = [257, 1, 1000, 63, 130]
+    N = sum(numel)
+    w0 = rng.normal(0, 0.02, N).astype(np.float32)
+    grads = [O.bf16_rne(rng.normal(0, 1e-2, N).astype(np.float32)) for _ in range(5)]
+    h = O.hyper(clip=clip, max_grad_norm=0.05)
+
+    pa = O.plan(numel, 4, 600)
+    sa = O.init_state(pa, stage_a, w0)
+    whole = [O.zero_step(pa, sa, [pa.pad(g)] * 4, h) for g in grads]
+
+    pb = O.plan(numel, 4, 600)
+    sb = O.init_state(pb, stage_a, w0)
+    first = [O.zero_step(pb, sb, [pb.pad(g)] * 4, h) for g in grads[:2]]
+    u = pb.unpadded_index()
+    saved = {k: O.flat_state(pb, sb, k)[u >= 0].copy() for k in ("master", "mom", "var")}
+    pc = O.plan(numel, 2, 0)
+    sc = O.init_state(pc, stage_b, saved["master"], saved["mom"], saved["var"], t=sb.t)
+    second = [O.zero_step(pc, sc, [pc.pad(g)] * 2, h) for g in grads[2:]]
+
+    for (fa, na, sa_, ra), (fb, nb_, sb_, rb) in zip(whole, first + second):
+        assert ra == rb == 0 and na == nb_ and sa_ == sb_
+        assert np.array_equal(fa, fb)
+    if clip:
+        assert any(o[2] < 1.0 for o in whole), "case meant to exercise clipping"
+    ua, uc = pa.unpadded_index(), pc.unpadded_index()
+    for k in ("master", "mom", "var"):
+        a = O.flat_state(pa, sa, k)[ua >= 0]
+        c = O.flat_state(pc, sc, k)[uc >= 0]
+        assert np.array_equal(a.view(np.uint32), c.view(np.uint32)), k
+    assert sa.t == sc.t == 5
