@@ -40,6 +40,10 @@ MUTANTS = [
      "if (in_bucket < b_n[b]) dst[base * 0 + in_bucket + b * 1] = shard_bf16[r][base + j];"),
     ("groups summed flat", "        for (int32_t k = 0; k < K; ++k) part = part + orc_bf16_to_f32(g[grp * K + k][o]);\n        acc = acc + part;",
      "        for (int32_t k = 0; k < K; ++k) acc = acc + orc_bf16_to_f32(g[grp * K + k][o]);\n        part = part + acc;"),
+    ("saved v dropped on resume", "var[r][base + j] = (real && v_init) ? v_init[u] : 0.0f;",
+     "var[r][base + j] = 0.0f;"),
+    ("saved m and v swapped on resume", "mom[r][base + j] = (real && m_init) ? m_init[u] : 0.0f;",
+     "mom[r][base + j] = (real && v_init) ? v_init[u] : 0.0f;"),
     ("nonfinite not skipped", "if (!isfinite(norm)) skipped = 1;\n        else s = orc_clip_scale(norm, h->max_grad_norm);\n    }\n    *scale_out = s;",
      "s = orc_clip_scale(norm, h->max_grad_norm);\n    }\n    *scale_out = s;"),
 ]
