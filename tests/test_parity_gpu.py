@@ -418,3 +418,16 @@ def test_results_do_not_depend_on_the_grid(clip):
                 for a, b in zip(got[:3], ref[:3]):
                     assert state_errors(a, b) <= 1.0, (cap, gather)
                 assert bf16_ulp_diff(got[3], ref[3]) <= 1
+
+
+def test_default_stream_handle_is_the_current_stream():
+    """Calls without a stream argument enqueue on torch's current stream: the binding's fast
+    handle lookup equals torch.cuda.current_stream() outside and inside a stream context,
+    and on a second device index when there is one."""
+    dev = torch.device("cuda")
+    assert zg._stream_handle(None) == torch.cuda.current_stream(dev).cuda_stream
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        assert zg._stream_handle(None) == s.cuda_stream == torch.cuda.current_stream().cuda_stream
+    assert zg._stream_handle(None) == torch.cuda.current_stream(dev).cuda_stream
+    assert zg._stream_handle(s) == s.cuda_stream

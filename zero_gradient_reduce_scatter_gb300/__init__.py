@@ -165,9 +165,19 @@ def _i64_array(vals):
     return arr
 
 
+# The current stream's raw handle without building a torch.cuda.Stream object (the getter
+# torch's own generated code uses; ~0.3 us against ~3 us, which matters for steps of a few
+# microseconds); the public path when this torch lacks it.
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_CUR_DEVICE = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_handle(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return int(s.cuda_stream)
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _RAW_STREAM is not None and _CUR_DEVICE is not None:
+        return int(_RAW_STREAM(_CUR_DEVICE()))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 # ---- host-only planning -----------------------------------------------------------------
