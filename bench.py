@@ -14,6 +14,7 @@ torch.distributed.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -414,6 +415,8 @@ def run_ours(args):
         launches_per_step = int(sum(c for _, c in opt.kernel_times().values()))
         opt.set_timing(False)
         graph = torch.cuda.CUDAGraph()
+        gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+        torch.cuda.synchronize()
         with torch.cuda.graph(graph):
             opt.step_scheduled(grads)
 
@@ -706,6 +709,8 @@ def run_stream(args):
         launches_per_step = int(sum(c for _, c in opt.kernel_times().values()))
         opt.set_timing(False)
         graph = torch.cuda.CUDAGraph()
+        gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+        torch.cuda.synchronize()
         with torch.cuda.graph(graph):
             eager_step(True)
         step = graph.replay
@@ -806,6 +811,8 @@ def run_gather(args):
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         cap_side = torch.cuda.Stream(device=device)
+        gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+        torch.cuda.synchronize()
         with torch.cuda.graph(graph):
             for _b, _params in opt.prefetched_buckets(order, stream=torch.cuda.current_stream(), side_stream=cap_side,
                                                       buffers=args.prefetch_buffers):

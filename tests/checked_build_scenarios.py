@@ -5,6 +5,7 @@ before the binding loads anything. Every scenario also runs its oracle compariso
 each the device must report no failed bounds check. Exits non-zero on the first failure.
 """
 import ctypes
+import gc
 import os
 import sys
 
@@ -76,6 +77,8 @@ def main():
     hq, _ = make_hyper(wq)
     opt.set_schedule([hq, hq])
     graph = torch.cuda.CUDAGraph()
+    gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+    torch.cuda.synchronize()
     with torch.cuda.graph(graph):
         opt.step_scheduled(gq)
     for _ in range(2):

@@ -9,6 +9,7 @@ optimizer runs alongside), and the oracle within the parity tolerances. A replay
 schedule must change no state and raise ZERO_ERR_SCHEDULE. A new schedule continues from
 the last step that ran.
 """
+import gc
 import math
 
 import numpy as np
@@ -100,6 +101,8 @@ def test_captured_step_replays_match_zero_step_and_oracle(case):
     first = schedule(w, 4, 0)
     opt.set_schedule([h for h, _ in first])
     graph = torch.cuda.CUDAGraph()
+    gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+    torch.cuda.synchronize()
     with torch.cuda.graph(graph):
         opt.step_scheduled(grads)
     assert opt.t == 0  # capturing ran nothing
@@ -187,6 +190,8 @@ def test_captured_streaming_step_matches_oracle(overlap):
     sched = schedule(w, 3, 0)
     opt.set_schedule([h for h, _ in sched])
     graph = torch.cuda.CUDAGraph()
+    gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+    torch.cuda.synchronize()
     with torch.cuda.graph(graph):
         for b in reversed(range(nb)):
             opt.reduce_bucket(b, slices[b])
@@ -220,6 +225,8 @@ def test_captured_fused_bucket_steps_match_oracle(gather):
     sched = schedule(w, 3, 0)
     opt.set_schedule([h for h, _ in sched])
     graph = torch.cuda.CUDAGraph()
+    gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+    torch.cuda.synchronize()
     with torch.cuda.graph(graph):
         for b in reversed(range(nb)):
             opt.step_bucket_scheduled(b, slices[b])
@@ -251,6 +258,8 @@ def test_captured_prefetched_gather_sweep(overlap):
     side = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
+    gc.collect()  # collect garbage (CUDA objects) now, not inside the global-mode capture
+    torch.cuda.synchronize()
     with torch.cuda.graph(graph):
         for b, params in opt.prefetched_buckets(list(range(nb)), stream=torch.cuda.current_stream(), side_stream=side):
             u0, n = opt.bucket_range(b)

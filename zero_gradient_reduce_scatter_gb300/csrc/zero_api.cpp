@@ -1146,13 +1146,22 @@ int zero_destroy(zero_ctx* c) {
         g_live.erase(c);
     }
     {
-        DeviceGuard guard(c->device);
-        for (auto& tl : c->events) {
-            cudaEventDestroy(tl.start);
-            cudaEventDestroy(tl.stop);
+        // A context may be released while some stream is being captured into a CUDA graph
+        // in global mode (for example when a garbage collector runs during the capture).
+        // Releasing events is harmless to any capture, so this thread relaxes its capture
+        // mode around the releases and restores it afterwards.
+        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+        const bool exchanged = cudaThreadExchangeStreamCaptureMode(&mode) == cudaSuccess;
+        {
+            DeviceGuard guard(c->device);
+            for (auto& tl : c->events) {
+                cudaEventDestroy(tl.start);
+                cudaEventDestroy(tl.stop);
+            }
+            for (auto& g : c->grad_sets) cudaEventDestroy(g.consumed);
+            if (c->h2d_done) cudaEventDestroy(c->h2d_done);
         }
-        for (auto& g : c->grad_sets) cudaEventDestroy(g.consumed);
-        if (c->h2d_done) cudaEventDestroy(c->h2d_done);
+        if (exchanged) cudaThreadExchangeStreamCaptureMode(&mode);
     }
     delete c;
     return ZERO_OK;
