@@ -127,6 +127,12 @@ typedef struct {
                              device keeps one copy; rank q = grp * K + k. The average sums
                              each group's K gradients in order, then the G group sums in
                              order, then multiplies by (float)(1/M). M % G must be 0.        */
+    int32_t sharded;      /* 0: all M ranks are emulated on this device (the default).
+                             1: process per rank: this context is rank `rank` of a job of M
+                             processes, one per GPU, and holds only that rank's part of the
+                             state; see "Process-per-rank mode" below.                      */
+    int32_t rank;         /* sharded mode: this process's rank, 0..M-1 (owner of shard `rank`
+                             of every bucket); unused otherwise                              */
 } zero_config;
 
 /* Hyper-parameters of one step. */
@@ -254,6 +260,92 @@ int zero_step_host(zero_ctx* ctx, const void* const* host_grads, void* const* de
 int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void* const* dev_grads,
                               int stage, const zero_hyper* hyper, void* host_params, void* stream,
                               void* copy_stream);
+
+/* ---- Process-per-rank mode (zero_config.sharded = 1) ----------------------------------
+ * The same step split across M processes, one per GPU, each holding only its own part
+ * ("CS336 2026 Lecture 8" Slides 8 and 20: reduce-scatter the gradients to their owners,
+ * each owner updates its shard, all-gather the parameters; "并行训练优化、MoE扩展与系统瓶颈"
+ * 1.2.2 reduce_scatter_sum / all_gather and 2.2.1-2.2.6; "并行策略总览：六个维度各切什么、
+ * 怎么通信", the per-card volumes of the reduce-scatter and all-gather; "CS231n Lecture 11"
+ * 4.3-4.4). Rank r = zero_config.rank owns lanes [off_b + r*S_b, off_b + (r+1)*S_b) of every
+ * bucket b of the flat layout above: its "shard", shard_len lanes, the concatenation of these
+ * slices in bucket order (local lane base_b + j is global lane off_b + r*S_b + j, base_b the
+ * sum of S over earlier buckets). The library's kernels read and write this device's buffers
+ * only; the caller moves data between processes with its own collectives (torch.distributed
+ * over NCCL, or gloo through host memory), at three points of a step:
+ *   (1) the exchange that feeds the reduce-scatter. Gradients travel as bf16 bytes and are
+ *       summed at the owner in fp32, rank order 0..M-1 from +0, so the result is the
+ *       emulated step's bit for bit (a collective that reduced in bf16, or in another order,
+ *       would not be). Per bucket, an all-to-all of the bucket's M slices:
+ *         recv[off_b + q*S_b + j] = grad_q[off_b + r*S_b + j],   0 <= q < M, 0 <= j < S_b,
+ *       i.e. all_to_all_single(recv[off_b : off_b + M*S_b], grad[off_b : off_b + M*S_b])
+ *       with equal splits. recv is bf16 [npad] ("the exchange layout").
+ *   (2) with clipping, one fp64 per rank: each rank's sum of squares of its averaged shard
+ *       (zero_rank_sumsq), gathered in rank order into a device array of M doubles on every
+ *       rank (all_gather). Every rank then forms the same norm in the same order.
+ *   (3) the all-gather of the updated bf16 shards: per bucket,
+ *         all_gather(param_full[off_b : off_b + M*S_b], param_shards[base_b : base_b + S_b]).
+ *       With ZeRO-3 the same call into a transient buffer of M*S_b lanes gives bucket b's
+ *       parameters, in tensor order, in its first n_b lanes (the per-module gather).
+ * Hybrid sharding (groups = G > 1, M = G*K processes, rank q = grp*K + k owns shard k of a
+ * layout planned for K owners, replicated across the G groups): (1) runs inside each group
+ * (an all-to-all among its K ranks, source index k' in place of q); zero_rank_partial then
+ * sums the K slices in order into an fp32 group partial; the partials of shard k are
+ * all-gathered across the G groups in group order (among ranks k, K + k, ...) into
+ * parts[G * shard_len]; the step sums them in group order and multiplies by (float)(1/M)
+ * -- the all-reduce across groups, in a fixed order. (2) gathers the K sums of one group.
+ *
+ * Buffers in this mode (zero_plan reports these sizes when cfg->sharded = 1):
+ *   master, m, v  fp32 [shard_len]: this rank's shard of the state (required)
+ *   ghat          fp32 [shard_len]: averaged-gradient workspace (optional, as above)
+ *   param_shards  bf16 [shard_len]: this rank's updated bf16 shard, the all-gather's send
+ *                 buffer (required; the persistent parameters at stage 3)
+ *   param_full    bf16 [npad]: the full parameters in the padded layout, tensor i at lanes
+ *                 [tensor_off[i], tensor_off[i] + numel[i]) like the gradients (the
+ *                 all-gather's receive buffer; required at stages 1 and 2, may be NULL at
+ *                 stage 3, where the caller gathers into its own transient buffers)
+ *   scratch       bytes_scratch
+ * bytes_grad_each is 2 * npad: this rank's gradient, and the exchange buffer recv.
+ * zero_init takes the full unpadded master_init [n] (the same on every rank), initialises
+ * this rank's shard, its bf16 shard and all of param_full (padding 0), with no collective.
+ * The gather field has no effect: the owner always writes param_shards.
+ * Calls of the emulated mode that would touch other ranks' data (zero_step, zero_step_host*,
+ * the per-bucket and scheduled forms, zero_gather*) return INVALID_ARG on such a context.
+ * zero_get_state copies this rank's shard (rank must be cfg->rank, or k with groups);
+ * zero_save_state writes this rank's real lanes of the unpadded vectors and leaves the other
+ * lanes untouched (the ranks' outputs are disjoint; summing zero-filled outputs across
+ * ranks, or across one group, gives the whole state); zero_load_state reads the whole
+ * unpadded vectors. */
+
+/* Without clipping, the whole update of this rank's shard in one fused pass per bucket:
+ * reduce-scatter from the exchanged slices (rank-ordered fp32 sum x (float)(1/M)), AdamW,
+ * the bf16 shard into param_shards. With clipping: zero_rank_sumsq first, then the gathered
+ * sums, then this call. Increments t.
+ *  src        flat mode: bf16 recv [npad] in the exchange layout (read-only, borrowed until
+ *             the stream passes the call); hybrid mode: fp32 parts [G * shard_len], the
+ *             gathered group partials of this shard, group grp at [grp * shard_len]
+ *  sumsq_all  clipping only (else NULL): device fp64 [P], P = M (flat) or K (hybrid), entry i
+ *             = the value zero_rank_sumsq wrote on rank i (of this group); the same on every
+ *             rank, so every rank computes the same norm and clip scale
+ * The materialized / recomputed choice of the clipped form is the one zero_rank_sumsq made.
+ * Errors: BAD_CONTEXT, INVALID_ARG (not a sharded context, missing sumsq_all, clipping
+ * without a preceding zero_rank_sumsq), STAGE, MISALIGNED, SIZE_MISMATCH, CUDA. */
+int zero_rank_step(zero_ctx* ctx, const void* src, const double* sumsq_all, int stage,
+                   const zero_hyper* hyper, void* stream);
+
+/* Clipping, first pass: averages this rank's shard from src (as in zero_rank_step) and writes
+ * the fp64 sum of squares over its real lanes to *sumsq (device, 8-byte aligned). Under
+ * ZERO_GHAT_MATERIALIZE (or AUTO choosing it) the fp32 average also goes to the ghat buffer,
+ * and zero_rank_step reads it instead of src. hyper->clip must be 1.
+ * Errors: BAD_CONTEXT, INVALID_ARG, MISALIGNED, SIZE_MISMATCH, CUDA. */
+int zero_rank_sumsq(zero_ctx* ctx, const void* src, const zero_hyper* hyper, double* sumsq,
+                    void* stream);
+
+/* Hybrid mode only: the group partial of this rank's shard, part[j] = the K exchanged bf16
+ * slices of local lane j summed in fp32 in order from +0 (no scaling; padding lanes 0), from
+ * recv (bf16 [npad], the exchange layout of this rank's group) into part (fp32 [shard_len]).
+ * Errors: BAD_CONTEXT, INVALID_ARG (not a hybrid sharded context), MISALIGNED, CUDA. */
+int zero_rank_partial(zero_ctx* ctx, const void* recv, void* part, void* stream);
 
 /* Steps whose scalars live on the device, for capture in a CUDA graph. The pages define no
  * interface for this. It serves training loops that capture whole steps as CUDA graphs and

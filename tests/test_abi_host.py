@@ -165,3 +165,45 @@ def test_state_ledger_matches_pages(zg):
     assert 100e9 * f(0, 1, 2, 2, 4) / 1e9 == g["fsdp_4x2B_100B_total_GB"][0]
     assert 100e9 * f(3, 80, 2, 2, 4) / 1e9 == g["fsdp_4x2B_100B_per_gpu_80_GB"][0]
     assert f(4, 8, 2, 2, 8) < 0 and f(1, 0, 2, 2, 8) < 0
+
+
+@pytest.mark.parametrize("numel,M,bucket_bytes,groups", [
+    ((1000, 37, 3001), 2, 6100, 1), (W.ragged_numel(40, 100, 6000, 3), 4, 15000, 1),
+    ((5, 7, 4099), 8, 0, 2), ((3,), 16, 0, 1)])
+def test_sharded_sizes(zg, numel, M, bucket_bytes, groups):
+    """Process-per-rank sizes: one rank's shard of the state, the padded full parameters and
+    gradient, the same layout (and npad) as the emulated job planned for the owners."""
+    K = M // groups
+    emu = zg.plan(numel, M, 3, bucket_bytes, groups=groups)
+    p = O.plan(numel, K, bucket_bytes, 64)
+    for r in range(M):
+        s = zg.plan(numel, M, 3, bucket_bytes, groups=groups, rank=r)
+        assert (s["npad"], s["n"], s["n_buckets"], s["shard_len"]) == (p.npad, p.N, p.nb, p.shard_len)
+        assert s["bytes_master"] == s["bytes_m"] == s["bytes_v"] == s["bytes_ghat"] == 4 * p.shard_len
+        assert s["bytes_param_shards"] == 2 * p.shard_len and s["bytes_param_full"] == 2 * p.npad
+        assert s["bytes_grad_each"] == 2 * p.npad
+        # the scratch also holds the rank's own bucket table (32 bytes a bucket, rounded to 256)
+        assert s["bytes_scratch"] == emu["bytes_scratch"] + (32 * p.nb + 255) // 256 * 256
+        assert zg.layout(numel, M, 3, bucket_bytes, groups=groups) == (
+            [int(x) for x in p.t_off], [(int(a), int(b), int(c), int(d)) for a, b, c, d in
+                                        zip(p.b_off, p.b_n, p.b_S, p.b_first[:p.nb])])
+
+
+@pytest.mark.parametrize("sharded,rank,gather,stage,code", [
+    (1, 2, 0, 1, -1), (1, -1, 0, 1, -1), (2, 0, 0, 1, -1), (1, 1, 1, 1, 0), (0, 5, 0, 1, 0)])
+def test_sharded_config_checks(zg, sharded, rank, gather, stage, code):
+    """rank must lie in [0, M) in process-per-rank mode (and is ignored otherwise); the gather
+    mode has no effect there, so the shards mode is accepted at any stage."""
+    c = zg.Config(2, stage, 0, gather, 0, sharded, rank)
+    arr = (ctypes.c_int64 * 1)(100)
+    out = zg.Sizes()
+    assert zg._lib().zero_plan(ctypes.byref(c), ctypes.cast(arr, ctypes.c_void_p), 1, ctypes.byref(out)) == code
+
+
+def test_rank_calls_reject_null_or_unknown_context(zg):
+    lib = zg._lib()
+    h = zg.Hyper(clip=True)
+    for ctx in (None, ctypes.c_void_p(0x1234)):
+        assert lib.zero_rank_step(ctx, None, None, 1, ctypes.byref(h), None) == -7
+        assert lib.zero_rank_sumsq(ctx, None, ctypes.byref(h), None, None) == -7
+        assert lib.zero_rank_partial(ctx, None, None, None) == -7

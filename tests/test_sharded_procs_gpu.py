@@ -1,0 +1,138 @@
+"""Process-per-rank mode with real processes: two ranks on the one GPU, one process each.
+
+NCCL does not run two ranks on one device, so the ranks exchange through gloo with their
+device buffers staged through host memory (ShardedZeroOptimizer(transport="host")). Each
+process runs the library's kernels on its own shard only. Three clipped steps on a ragged
+multi-bucket layout, at ZeRO-1 (full parameters kept) and ZeRO-3 (per-bucket gathers into a
+transient buffer), both forms of the clipped step; every rank checks itself against the
+oracle's two-rank step: its shard of master / m / v (1e-6 relative; bit-identical expected),
+the averaged gradient bit-exact when materialized, the norm within 1e-7 and equal on both
+ranks, the gathered bf16 parameters within 1 ulp; then the assembled checkpoint state equals
+the oracle's bit for bit.
+
+The ranks wait for each other only on the host (gloo), never inside a kernel.
+"""
+import os
+import socket
+import sys
+import traceback
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+pytestmark = pytest.mark.gpu
+
+NUMEL = (3001, 1000, 37, 4099, 1, 64, 777)
+BUCKET_BYTES = 6000
+
+
+def free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _grads_all(p, M, k):
+    """Every rank's bf16 gradient of step k (uint16 patterns; each process can make all)."""
+    import oracle as O
+    rng = np.random.default_rng(4242 + k)
+    out = []
+    for _ in range(M):
+        out.append(O.bf16_rne(rng.standard_normal(p.npad).astype(np.float32) * np.float32(3e-3)))
+    real = p.real_mask()
+    for g in out:
+        g[~real] = 0x3F80  # padding garbage: ignored on both sides
+    return out
+
+
+def _rank_main(rank, world, port, stage, ghat_mode, q):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        import torch
+        import torch.distributed as dist
+
+        import oracle as O
+        import workloads as W
+        import zero_gradient_reduce_scatter_gb300 as zg
+        from parity_util import assert_state_close, bf16_ulp_diff, f32, u16
+        from rank_util import padded_to_unpadded
+
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
+        mi = W.master_init(w, dev)
+        opt = zg.ShardedZeroOptimizer(NUMEL, stage, mi, bucket_bytes=BUCKET_BYTES, transport="host",
+                                      ghat_buffer=True)
+        assert opt.M == world and opt.rank == rank and len(opt.buckets) >= 2
+        p = O.plan(NUMEL, world, BUCKET_BYTES)
+        st = O.init_state(p, stage, f32(mi))
+        h = zg.Hyper(clip=True, max_grad_norm=0.05, ghat_mode=ghat_mode)
+        oh = O.hyper(clip=True, max_grad_norm=0.05)
+        scratch = torch.empty(world * max(b[2] for b in opt.buckets), dtype=torch.bfloat16, device=dev)
+        for k in range(3):
+            G = _grads_all(p, world, k)
+            mine = torch.from_numpy(G[rank].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+            opt.step(mine, h)
+            full, norm, scale, rc = O.zero_step(p, st, G, oh)
+            assert rc == 0 and scale < 1.0
+            assert opt.sync_status() == 0
+            gn, gs = opt.last_norm()
+            assert abs(gn - norm) <= 1e-7 * norm
+            both = torch.tensor([gn, gs], dtype=torch.float64)
+            seen = [torch.zeros(2, dtype=torch.float64) for _ in range(world)]
+            dist.all_gather(seen, both)
+            assert all(torch.equal(x, seen[0]) for x in seen), "both ranks form the same norm and scale"
+            assert_state_close(f32(opt.get_state("master")), st.master[rank][:p.shard_len], f"step {k} master")
+            assert_state_close(f32(opt.get_state("m")), st.mom[rank][:p.shard_len], f"step {k} m")
+            assert_state_close(f32(opt.get_state("v")), st.var[rank][:p.shard_len], f"step {k} v")
+            if ghat_mode == "materialize":
+                assert np.array_equal(f32(opt.get_state("ghat")).view(np.uint32),
+                                      st.ghat[rank][:p.shard_len].view(np.uint32))
+            if stage == 3:
+                assert opt.params() is None  # ZeRO-3: no persistent full parameters
+                assert bf16_ulp_diff(u16(opt.param_shards), st.param[rank][:p.shard_len]) <= 1
+                uoff = 0
+                for b, (_off, n_b, _S, _) in enumerate(opt.buckets):  # per-module gathers
+                    got = opt.gather_bucket(b, scratch)
+                    assert bf16_ulp_diff(u16(got), full[uoff:uoff + n_b]) <= 1
+                    uoff += n_b
+            else:
+                assert bf16_ulp_diff(padded_to_unpadded(p, u16(opt.params())), full) <= 1
+        state = opt.save_state()
+        u = p.unpadded_index()
+        real = u >= 0
+        for name, attr in (("master", "master"), ("m", "mom"), ("v", "var")):
+            flat = O.flat_state(p, st, attr)
+            want = np.empty(p.N, dtype=np.float32)
+            want[u[real]] = flat[real]
+            assert np.array_equal(f32(state[name]).view(np.uint32), want.view(np.uint32)), name
+        assert state["t"] == 3
+        opt.close()
+        dist.destroy_process_group()
+        q.put((rank, "ok"))
+    except BaseException:
+        q.put((rank, traceback.format_exc()))
+
+
+@pytest.mark.parametrize("stage,ghat_mode", [(1, "materialize"), (3, "recompute"), (3, "materialize")])
+def test_two_processes_on_one_gpu(stage, ghat_mode):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, stage, ghat_mode, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=600) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+    bad = {r: v for r, v in got.items() if v != "ok"}
+    assert not bad, "\n".join(f"rank {r}:\n{v}" for r, v in bad.items())
+    assert all(p.exitcode == 0 for p in procs)

@@ -60,7 +60,8 @@ class ZeroError(RuntimeError):
 # ---- ctypes mirrors of the ABI structs --------------------------------------------------
 class Config(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int32), ("stage", ctypes.c_int32), ("bucket_bytes", ctypes.c_int64),
-                ("gather", ctypes.c_int32), ("groups", ctypes.c_int32)]
+                ("gather", ctypes.c_int32), ("groups", ctypes.c_int32), ("sharded", ctypes.c_int32),
+                ("rank", ctypes.c_int32)]
 
 
 class Hyper(ctypes.Structure):
@@ -130,6 +131,9 @@ SIGNATURES = {
     "zero_state_bytes_per_param": (ctypes.c_double, [ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                      ctypes.c_double, ctypes.c_double]),
     "zero_grad_norm_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, ctypes.c_double, _P, _P, _P]),
+    "zero_rank_step": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
+    "zero_rank_sumsq": (ctypes.c_int, [_P, _P, ctypes.POINTER(Hyper), _P, _P]),
+    "zero_rank_partial": (ctypes.c_int, [_P, _P, _P, _P]),
 }
 
 
@@ -181,9 +185,12 @@ def _stream_handle(stream) -> int:
 
 
 # ---- host-only planning -----------------------------------------------------------------
-def plan(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused", groups: int = 1) -> dict:
-    """Layout sizes of the ZeRO step (host only, no CUDA)."""
-    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups if groups > 1 else 0)
+def plan(numel, M: int, stage: int, bucket_bytes: int = 0, gather: str = "fused", groups: int = 1,
+         rank: int | None = None) -> dict:
+    """Layout sizes of the ZeRO step (host only, no CUDA). rank: the sizes of one rank of the
+    process-per-rank mode (its shard of the state) instead of the emulated job's."""
+    cfg = Config(M, stage, bucket_bytes, GATHER[gather], groups if groups > 1 else 0,
+                 0 if rank is None else 1, rank or 0)
     arr = _i64_array(numel)
     out = Sizes()
     _check(_lib().zero_plan(ctypes.byref(cfg), ctypes.cast(arr, _P), len(numel), ctypes.byref(out)), "zero_plan")
@@ -591,3 +598,7 @@ class ZeroOptimizer:
             self.close()
         except Exception:
             pass
+
+
+# process-per-rank mode (one process per GPU); imported last: it builds on the names above
+from .sharded import ShardedZeroOptimizer  # noqa: E402

@@ -80,6 +80,15 @@ struct zero_ctx {
     cudaStream_t chain_stream = nullptr;
     int chain_kind = -1;
     uintptr_t chain_lo = 0, chain_hi = 0;
+    // process-per-rank mode (cfg.sharded): this rank owns shard `owner` of every bucket; its
+    // shard is a layout of its own (`local`: per bucket {base_b, real lanes of the slice,
+    // base_b + S_b, unpadded index of the slice's first lane}, on the device at dev_local);
+    // npad / buckets / dev_buckets stay the global layout
+    int owner = 0;
+    std::vector<zg::Bucket> local;
+    zg::Bucket* dev_local = nullptr;
+    bool rank_reduced = false;          // zero_rank_sumsq ran and zero_rank_step has not
+    int rank_mode = ZERO_GHAT_RECOMPUTE;  // the clipped form zero_rank_sumsq chose
 };
 
 namespace {
@@ -140,7 +149,10 @@ int check_config(const zero_config* cfg) {
     if (cfg->M < 1 || cfg->M > ZERO_MAX_RANKS) return ZERO_ERR_INVALID_ARG;
     if (cfg->bucket_bytes < 0 || cfg->groups < 0) return ZERO_ERR_INVALID_ARG;
     if (cfg->groups > 1 && cfg->M % cfg->groups != 0) return ZERO_ERR_INVALID_ARG;
+    if (cfg->sharded != 0 && cfg->sharded != 1) return ZERO_ERR_INVALID_ARG;
+    if (cfg->sharded && (cfg->rank < 0 || cfg->rank >= cfg->M)) return ZERO_ERR_INVALID_ARG;
     if (cfg->gather != ZERO_GATHER_FUSED && cfg->gather != ZERO_GATHER_SHARDS) return ZERO_ERR_INVALID_ARG;
+    if (cfg->sharded) return ZERO_OK;  // the gather mode has no effect in process-per-rank mode
     if (cfg->gather == ZERO_GATHER_SHARDS && cfg->stage != 3) return ZERO_ERR_STAGE;
     return ZERO_OK;
 }
@@ -193,17 +205,49 @@ int make_layout(const zero_config* cfg, const int64_t* numel, int64_t n_tensors,
     return ZERO_OK;
 }
 
+// Process-per-rank mode: the rank's own bucket table follows the regular scratch parts.
+int64_t local_table_offset(int64_t n_buckets) { return zg::scratch_bytes(n_buckets); }
+
+int64_t scratch_size(const zero_config* cfg, int64_t n_buckets) {
+    const int64_t base = zg::scratch_bytes(n_buckets);
+    return cfg->sharded ? base + (32 * n_buckets + 255) / 256 * 256 : base;
+}
+
 void fill_sizes(const zero_config* cfg, const Layout& L, zero_sizes* s) {
     s->npad = L.npad;
     s->n = L.n;
     s->n_buckets = (int64_t)L.buckets.size();
     s->shard_len = L.shard_len;
+    s->bytes_grad_each = 2 * L.npad;
+    s->bytes_scratch = scratch_size(cfg, (int64_t)L.buckets.size());
+    if (cfg->sharded) {  // one rank's shard of the state; the full parameters padded
+        s->bytes_master = s->bytes_m = s->bytes_v = 4 * L.shard_len;
+        s->bytes_ghat = 4 * L.shard_len;
+        s->bytes_param_full = 2 * L.npad;
+        s->bytes_param_shards = 2 * L.shard_len;
+        return;
+    }
     s->bytes_master = s->bytes_m = s->bytes_v = 4 * L.npad;
     s->bytes_ghat = 4 * L.npad;
     s->bytes_param_full = 2 * L.n;
     s->bytes_param_shards = (cfg->gather == ZERO_GATHER_SHARDS) ? 2 * L.npad : 0;
-    s->bytes_grad_each = 2 * L.npad;
-    s->bytes_scratch = zg::scratch_bytes((int64_t)L.buckets.size());
+}
+
+// Process-per-rank mode: owner k's slice of every bucket as a layout of its own. Slice b
+// starts at local lane base_b (its position in the shard), holds S_b lanes of which the
+// first min(max(n_b - k * S_b, 0), S_b) are real, and its lane j is unpadded index
+// uoff_b + k * S_b + j (clamped to the bucket's end for a slice of padding only).
+std::vector<zg::Bucket> local_table(const std::vector<zg::Bucket>& global, int K, int k) {
+    std::vector<zg::Bucket> out;
+    int64_t base = 0;
+    for (const zg::Bucket& e : global) {
+        const int64_t S = (e.end - e.off) / K;
+        const int64_t first = std::min((int64_t)k * S, e.n);
+        const int64_t real = std::min(std::max(e.n - (int64_t)k * S, (int64_t)0), S);
+        out.push_back(zg::Bucket{base, real, base + S, e.uoff + first});
+        base += S;
+    }
+    return out;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -356,6 +400,35 @@ int gather_range(zero_ctx* c, int64_t u0, int64_t count, uint16_t* out, cudaStre
     return ZERO_OK;
 }
 
+// State from unpadded fp32 vectors (m_init / v_init may be null: zeros) and the bf16
+// parameters: init and checkpoint load. Emulated mode: one kernel over the whole layout.
+// Process-per-rank mode: one over this rank's shard (state and bf16 shard), then one over the
+// global layout that writes only the padded full parameters (padding 0), if there are any.
+cudaError_t launch_state_in(zero_ctx* c, const float* master, const float* m, const float* v, cudaStream_t s) {
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (!c->cfg.sharded) {
+        const int grid = grid_for(c, zg::kVarInit, c->npad);
+        Timed tm(c, ZERO_K_INIT, s);
+        return zg::launch_init(master, m, v, (float*)c->bufs.master, (float*)c->bufs.m, (float*)c->bufs.v,
+                               (uint16_t*)c->bufs.param_full, (uint16_t*)c->bufs.param_shards, c->dev_buckets, nb,
+                               c->npad, c->n, c->status, grid, s);
+    }
+    cudaError_t e;
+    {
+        const int grid = grid_for(c, zg::kVarInit, c->shard_len);
+        Timed tm(c, ZERO_K_INIT, s);
+        e = zg::launch_init(master, m, v, (float*)c->bufs.master, (float*)c->bufs.m, (float*)c->bufs.v, nullptr,
+                            (uint16_t*)c->bufs.param_shards, c->dev_local, nb, c->shard_len, c->n, c->status, grid, s);
+    }
+    if (e == cudaSuccess && c->bufs.param_full) {
+        const int grid = grid_for(c, zg::kVarInit, c->npad);
+        Timed tm(c, ZERO_K_INIT, s);
+        e = zg::launch_init(master, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                            (uint16_t*)c->bufs.param_full, c->dev_buckets, nb, c->npad, c->n, c->status, grid, s);
+    }
+    return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -396,8 +469,14 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     int rc = make_layout(cfg, numel, n_tensors, &L);
     if (rc) return rc;
     if (!bufs || !master_init) return ZERO_ERR_INVALID_ARG;
-    if (!bufs->master || !bufs->m || !bufs->v || !bufs->param_full || !bufs->scratch) return ZERO_ERR_SIZE_MISMATCH;
-    if (cfg->gather == ZERO_GATHER_SHARDS && !bufs->param_shards) return ZERO_ERR_SIZE_MISMATCH;
+    if (!bufs->master || !bufs->m || !bufs->v || !bufs->scratch) return ZERO_ERR_SIZE_MISMATCH;
+    if (cfg->sharded) {
+        // the rank's bf16 shard always; the full parameters unless ZeRO-3 gathers on demand
+        if (!bufs->param_shards || (cfg->stage < 3 && !bufs->param_full)) return ZERO_ERR_SIZE_MISMATCH;
+    } else {
+        if (!bufs->param_full) return ZERO_ERR_SIZE_MISMATCH;
+        if (cfg->gather == ZERO_GATHER_SHARDS && !bufs->param_shards) return ZERO_ERR_SIZE_MISMATCH;
+    }
     const void* must_align[] = {bufs->master, bufs->m, bufs->v, bufs->ghat, bufs->param_full, bufs->param_shards,
                                 bufs->scratch, master_init};
     for (const void* p : must_align)
@@ -427,8 +506,14 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     c->n = L.n;
     c->shard_len = L.shard_len;
     c->bufs = *bufs;
-    if (cfg->gather != ZERO_GATHER_SHARDS) c->bufs.param_shards = nullptr;
+    if (cfg->gather != ZERO_GATHER_SHARDS && !cfg->sharded) c->bufs.param_shards = nullptr;
     char* scratch = (char*)bufs->scratch;
+    if (cfg->sharded) {
+        const int K = shard_count(cfg);
+        c->owner = cfg->rank % K;
+        c->local = local_table(L.buckets, K, c->owner);
+        c->dev_local = (zg::Bucket*)(scratch + local_table_offset((int64_t)L.buckets.size()));
+    }
     c->status = (zg::Status*)(scratch + zg::kScratchStatus);
     c->partials = (double*)(scratch + zg::kScratchPartials);
     c->dev_buckets = (zg::Bucket*)(scratch + zg::kScratchBuckets);
@@ -455,13 +540,10 @@ int zero_init(zero_ctx** out, const zero_config* cfg, const int64_t* numel, int6
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(c->dev_buckets, c->buckets.data(), sizeof(zg::Bucket) * c->buckets.size(),
                             cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) {
-        const int grid = grid_for(c, zg::kVarInit, c->npad);
-        Timed tm(c, ZERO_K_INIT, s);
-        e = zg::launch_init((const float*)master_init, nullptr, nullptr, (float*)c->bufs.master, (float*)c->bufs.m,
-                            (float*)c->bufs.v, (uint16_t*)c->bufs.param_full, (uint16_t*)c->bufs.param_shards,
-                            c->dev_buckets, (int64_t)c->buckets.size(), c->npad, c->n, c->status, grid, s);
-    }
+    if (e == cudaSuccess && cfg->sharded)
+        e = cudaMemcpyAsync(c->dev_local, c->local.data(), sizeof(zg::Bucket) * c->local.size(),
+                            cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = launch_state_in(c, (const float*)master_init, nullptr, nullptr, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // host tables above must outlive the copies
     if (e != cudaSuccess) {
         delete c;
@@ -546,6 +628,7 @@ static int launch_step_begin(zero_ctx* c, cudaStream_t s) {
 
 int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper* h, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (c->n_reduced || c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
@@ -567,6 +650,7 @@ int zero_step(zero_ctx* c, const void* const* grads, int stage, const zero_hyper
 
 int zero_step_scheduled(zero_ctx* c, const void* const* grads, int stage, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (!c->sched_active) return ZERO_ERR_SCHEDULE;
     if (c->n_reduced || c->n_bucket_done) return ZERO_ERR_INVALID_ARG;
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
@@ -583,6 +667,7 @@ int zero_step_scheduled(zero_ctx* c, const void* const* grads, int stage, void* 
 
 int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     const int64_t nb = (int64_t)c->buckets.size();
     if (bucket < 0 || bucket >= nb || !grads_b) return ZERO_ERR_INVALID_ARG;
     if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
@@ -694,6 +779,7 @@ static int check_step_bucket(const zero_ctx* c, int64_t bucket, const void* cons
 int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, const zero_hyper* h,
                      void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     int rc = check_hyper(h);
     if (rc) return rc;
@@ -707,6 +793,7 @@ int zero_step_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, in
 
 int zero_step_bucket_scheduled(zero_ctx* c, int64_t bucket, const void* const* grads_b, int stage, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (!c->sched_active) return ZERO_ERR_SCHEDULE;
     if (c->sched_clip) return ZERO_ERR_INVALID_ARG;
     int rc = check_step_bucket(c, bucket, grads_b, stage);
@@ -751,6 +838,7 @@ static int check_apply(const zero_ctx* c, int stage) {
 
 int zero_apply(zero_ctx* c, int stage, const zero_hyper* h, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     int rc = check_hyper(h);
     if (rc) return rc;
@@ -766,6 +854,7 @@ int zero_apply(zero_ctx* c, int stage, const zero_hyper* h, void* stream) {
 
 int zero_apply_scheduled(zero_ctx* c, int stage, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (!c->sched_active) return ZERO_ERR_SCHEDULE;
     int rc = check_apply(c, stage);
     if (rc) return rc;
@@ -789,6 +878,7 @@ static int read_device_step(zero_ctx* c, int64_t* t) {
 
 int zero_set_schedule(zero_ctx* c, const zero_hyper* h, int64_t count, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (count < 0 || (count > 0 && !h)) return ZERO_ERR_INVALID_ARG;
     if (count > ZERO_MAX_SCHEDULE) return ZERO_ERR_TOO_LARGE;
     int mode = ZERO_GHAT_RECOMPUTE;
@@ -835,6 +925,7 @@ int zero_set_schedule(zero_ctx* c, const zero_hyper* h, int64_t count, void* str
 int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
                    const zero_hyper* h, void* host_params, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!host_grads || !dev_grads || !host_params) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r)
@@ -864,10 +955,13 @@ int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
     ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
-    const int grid = grid_for(c, zg::kVarInit, c->npad);
+    // process-per-rank mode: this rank's real lanes only, through its own table
+    const int64_t lanes = c->cfg.sharded ? c->shard_len : c->npad;
+    const int grid = grid_for(c, zg::kVarInit, lanes);
     cudaError_t e = zg::launch_save((const float*)c->bufs.master, (const float*)c->bufs.m, (const float*)c->bufs.v,
-                                    (float*)master, (float*)m, (float*)v, c->dev_buckets,
-                                    (int64_t)c->buckets.size(), c->npad, c->n, c->status, grid, s);
+                                    (float*)master, (float*)m, (float*)v,
+                                    c->cfg.sharded ? c->dev_local : c->dev_buckets, (int64_t)c->buckets.size(),
+                                    lanes, c->n, c->status, grid, s);
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
@@ -878,20 +972,17 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
-    const int grid = grid_for(c, zg::kVarInit, c->npad);
-    Timed tm(c, ZERO_K_INIT, s);
-    cudaError_t e = zg::launch_init((const float*)master, (const float*)m, (const float*)v, (float*)c->bufs.master,
-                                    (float*)c->bufs.m, (float*)c->bufs.v, (uint16_t*)c->bufs.param_full,
-                                    (uint16_t*)c->bufs.param_shards, c->dev_buckets, (int64_t)c->buckets.size(),
-                                    c->npad, c->n, c->status, grid, s);
+    const cudaError_t e = launch_state_in(c, (const float*)master, (const float*)m, (const float*)v, s);
     if (e != cudaSuccess) return cuda_fail(e);
     c->t = t;
+    c->rank_reduced = false;
     return ZERO_OK;
 }
 
 int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* const* dev_grads, int stage,
                               const zero_hyper* h, void* host_params, void* stream, void* copy_stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!host_grads || !dev_grads || !host_params || copy_stream == stream) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r)
@@ -937,6 +1028,201 @@ int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* 
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
 }
 
+// ---------------------------------------------------------------------------------------
+// Process-per-rank mode. The kernels are the emulated mode's, run over this rank's shard
+// (the local table) with the exchanged slices as their M sources.
+// ---------------------------------------------------------------------------------------
+static bool hybrid(const zero_ctx* c) { return c->cfg.groups > 1; }
+
+// Arguments of a kernel over this rank's shard; the caller sets the sources.
+static zg::StepArgs rank_args(zero_ctx* c) {
+    zg::StepArgs a = base_args(c);
+    a.out = (uint16_t*)c->bufs.param_shards;  // the owner's bf16 shard, the all-gather's send buffer
+    a.out_shards = 1;
+    a.buckets = c->dev_local;
+    a.nvec = c->shard_len / 8;
+    a.vbeg = 0;
+    a.vend = a.nvec;
+    a.gbase = 0;
+    a.gext = c->shard_len;
+    a.npad = c->shard_len;
+    a.groups = 1;
+    return a;
+}
+
+// Bucket b's sources in the exchange layout: the slice that source q (of `count`) sent for
+// this shard starts at lane off_b + q * S_b of recv. rebase: shift each pointer back by the
+// slice's local start base_b, for the fused kernel, which addresses its sources by local
+// lane (address arithmetic only; it reads lanes [base_b, base_b + S_b) alone); otherwise
+// each pointer is the slice start and the norm pass subtracts gbase = base_b.
+static void slice_sources(const zero_ctx* c, zg::StepArgs& a, const void* recv, int64_t b, int count, bool rebase) {
+    const zg::Bucket& G = c->buckets[(size_t)b];
+    const zg::Bucket& L = c->local[(size_t)b];
+    const int64_t S = L.end - L.off;
+    for (int q = 0; q < count; ++q) {
+        const uintptr_t start = (uintptr_t)recv + 2 * (uintptr_t)(G.off + (int64_t)q * S);
+        a.grads[q] = (const uint16_t*)(rebase ? start - 2 * (uintptr_t)L.off : start);
+    }
+    a.M = count;
+    a.vbeg = L.off / 8;
+    a.vend = L.end / 8;
+    a.b_first = b;
+    a.b_end = b + 1;
+    if (rebase) {
+        a.gext = L.end;
+    } else {
+        a.gbase = L.off;
+        a.gext = S;
+    }
+}
+
+// Hybrid mode: the G gathered fp32 group partials of this shard, group grp at [grp * shard_len].
+static void part_sources(const zero_ctx* c, zg::StepArgs& a, const void* parts) {
+    for (int grp = 0; grp < c->cfg.groups; ++grp)
+        a.grads[grp] = (const uint16_t*)((const float*)parts + (size_t)grp * (size_t)c->shard_len);
+    a.M = c->cfg.groups;
+}
+
+static int check_rank_ctx(const zero_ctx* c) {
+    if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (!c->cfg.sharded) return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
+}
+
+int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
+    int rc = check_rank_ctx(c);
+    if (rc) return rc;
+    if (!hybrid(c) || !recv || !part) return ZERO_ERR_INVALID_ARG;
+    if (!aligned16(recv) || !aligned16(part)) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int K = shard_count(&c->cfg);
+    cudaError_t e = cudaSuccess;
+    for (int64_t b = 0; b < (int64_t)c->buckets.size() && e == cudaSuccess; ++b) {
+        // the group's K slices summed in order from +0, unscaled (x 1 is exact), into `part`;
+        // the pass's partial sums of squares are not used
+        zg::StepArgs a = rank_args(c);
+        slice_sources(c, a, recv, b, K, false);
+        a.inv_M = 1.0f;
+        a.ghat = (float*)part;
+        const int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
+        Timed tm(c, ZERO_K_RS_NORM, s);
+        e = zg::launch_rs_norm(a, true, g1, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->last_stream = s;
+    return ZERO_OK;
+}
+
+int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* sumsq, void* stream) {
+    int rc = check_rank_ctx(c);
+    if (rc) return rc;
+    if ((rc = check_hyper(h))) return rc;
+    if (!h->clip || !src || !sumsq) return ZERO_ERR_INVALID_ARG;
+    if (!aligned16(src) || (reinterpret_cast<uintptr_t>(sumsq) & 7u)) return ZERO_ERR_MISALIGNED;
+    int mode;
+    if ((rc = resolve_ghat_mode(c, h, &mode))) return rc;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool write = mode == ZERO_GHAT_MATERIALIZE;
+    const int variant = write ? zg::kVarRsNormWrite : zg::kVarRsNormOnly;
+    const int64_t nb = (int64_t)c->buckets.size();
+    cudaError_t e = cudaSuccess;
+    if (hybrid(c)) {  // one pass over the whole shard from the gathered group partials
+        zg::StepArgs a = rank_args(c);
+        part_sources(c, a, src);
+        const int g1 = grid_for(c, variant, a.nvec);
+        {
+            Timed tm(c, ZERO_K_RS_NORM, s);
+            e = zg::launch_rs_norm_f32src(a, write, g1, s);
+        }
+        if (e == cudaSuccess) {
+            Timed tm(c, ZERO_K_NORM_FINAL, s);
+            e = zg::launch_sum_partials(c->partials, g1, sumsq, s);
+        }
+    } else {  // per bucket (the slices of a bucket are contiguous in the exchange buffer)
+        for (int64_t b = 0; b < nb && e == cudaSuccess; ++b) {
+            zg::StepArgs a = rank_args(c);
+            slice_sources(c, a, src, b, c->cfg.M, false);
+            const int g1 = grid_for(c, variant, a.vend - a.vbeg);
+            {
+                Timed tm(c, ZERO_K_RS_NORM, s);
+                e = zg::launch_rs_norm(a, write, g1, s);
+            }
+            if (e == cudaSuccess) {  // one bucket: straight to the output
+                Timed tm(c, ZERO_K_NORM_FINAL, s);
+                e = zg::launch_sum_partials(c->partials, g1, nb == 1 ? sumsq : c->bucket_sums + b, s);
+            }
+        }
+        if (e == cudaSuccess && nb > 1) {
+            Timed tm(c, ZERO_K_NORM_FINAL, s);
+            e = zg::launch_sum_partials(c->bucket_sums, (int)nb, sumsq, s);
+        }
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->rank_reduced = true;
+    c->rank_mode = mode;
+    c->last_stream = s;
+    return ZERO_OK;
+}
+
+int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int stage, const zero_hyper* h,
+                   void* stream) {
+    int rc = check_rank_ctx(c);
+    if (rc) return rc;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    if ((rc = check_hyper(h))) return rc;
+    const int clip = h->clip;
+    if (clip && (!sumsq_all || !c->rank_reduced)) return ZERO_ERR_INVALID_ARG;
+    const int mode = clip ? c->rank_mode : ZERO_GHAT_RECOMPUTE;
+    const bool from_ghat = clip && mode == ZERO_GHAT_MATERIALIZE;  // the sources are not read again
+    if (!from_ghat && !src) return ZERO_ERR_INVALID_ARG;
+    if (src && !aligned16(src)) return ZERO_ERR_MISALIGNED;
+    if (clip && (reinterpret_cast<uintptr_t>(sumsq_all) & 7u)) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    c->t += 1;
+    const zg::AdamConsts k = adam_consts(h, c->t);
+    cudaError_t e = cudaSuccess;
+    if (clip) {  // every rank sums the same P values in the same order: the same norm and scale
+        const int P = hybrid(c) ? shard_count(&c->cfg) : c->cfg.M;
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        e = zg::launch_norm_final(c->status, sumsq_all, P, h->max_grad_norm, 1, false, s);
+    }
+    if (e == cudaSuccess && from_ghat) {
+        zg::StepArgs a = rank_args(c);
+        a.k = k;
+        const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
+        Timed tm(c, ZERO_K_ADAMW, s);
+        e = zg::launch_adamw(a, false, g3, s);
+    } else if (e == cudaSuccess && hybrid(c)) {
+        zg::StepArgs a = rank_args(c);
+        part_sources(c, a, src);
+        a.k = k;
+        const int g4 = grid_for(c, clip ? zg::kVarRsAdamwScaled : zg::kVarRsAdamwPlain, a.nvec);
+        Timed tm(c, ZERO_K_RS_ADAMW, s);
+        e = zg::launch_rs_adamw_f32src(a, clip != 0, g4, s);
+    } else if (e == cudaSuccess) {
+        for (int64_t b = 0; b < (int64_t)c->buckets.size() && e == cudaSuccess; ++b) {
+            zg::StepArgs a = rank_args(c);
+            slice_sources(c, a, src, b, c->cfg.M, true);
+            a.k = k;
+            const int g4 = grid_for(c, clip ? zg::kVarRsAdamwScaled : zg::kVarRsAdamwPlain, a.vend - a.vbeg);
+            Timed tm(c, ZERO_K_RS_ADAMW, s);
+            e = zg::launch_rs_adamw(a, clip != 0, false, g4, s);
+        }
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->rank_reduced = false;
+    c->last_clip = clip;
+    c->last_stream = s;
+    c->stepped = 1;
+    return ZERO_OK;
+}
+
 int zero_params(zero_ctx* c, void** full_bf16) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!full_bf16) return ZERO_ERR_INVALID_ARG;
@@ -946,6 +1232,7 @@ int zero_params(zero_ctx* c, void** full_bf16) {
 
 int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->cfg.gather != ZERO_GATHER_SHARDS) return ZERO_ERR_INVALID_ARG;
     const int64_t nb = (int64_t)c->buckets.size();
     if (bucket < -1 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
@@ -964,6 +1251,7 @@ int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
 
 int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
+    if (c->cfg.sharded) return ZERO_ERR_INVALID_ARG;  // emulated mode only
     if (c->cfg.gather != ZERO_GATHER_SHARDS || !dst) return ZERO_ERR_INVALID_ARG;
     if (bucket < 0 || bucket >= (int64_t)c->buckets.size()) return ZERO_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dst) & 1u) return ZERO_ERR_MISALIGNED;
@@ -998,6 +1286,12 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     float* d = (float*)dst;
+    if (c->cfg.sharded) {  // the shard is contiguous on this rank
+        if (rank != c->owner) return ZERO_ERR_INVALID_ARG;
+        const cudaError_t ce =
+            cudaMemcpyAsync(d, src, sizeof(float) * (size_t)c->shard_len, cudaMemcpyDeviceToDevice, s);
+        return ce == cudaSuccess ? ZERO_OK : cuda_fail(ce);
+    }
     for (const zg::Bucket& e : c->buckets) {
         const int64_t S = (e.end - e.off) / shard_count(&c->cfg);
         cudaError_t ce = cudaMemcpyAsync(d, src + e.off + rank * S, sizeof(float) * (size_t)S,

@@ -197,6 +197,11 @@ cudaError_t launch_sum_partials(const double* partials, int nparts, double* out,
                                 int pdl = kPdlNone);
 // sched: the AdamW scalars are the running scheduled step's (st->cur), not a.k.
 cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s);
+// The norm pass and the fused step over fp32 sources: a.M fp32 buffers a.grads[r] (cast),
+// summed in order (process-per-rank hybrid sharding, the group partials). Launch shapes as
+// the bf16 variants of the generic rank count.
+cudaError_t launch_rs_norm_f32src(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
+cudaError_t launch_rs_adamw_f32src(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
 // a.pdl != kPdlNone (plain, unscheduled form only): launched with programmatic stream
 // serialization in that mode.
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int grid, cudaStream_t s);

@@ -256,13 +256,34 @@ __device__ __forceinline__ void rank_sum_grouped_fixed(const StepArgs& a, int64_
     }
 }
 
+// fp32 sources (process-per-rank hybrid sharding: the G group partials of this rank's
+// shard, gathered across groups): a.M sources, each read as fp32 at lane g, added in source
+// order -- the all-reduce across groups in a fixed order.
+__device__ __forceinline__ void rank_sum_f32(const StepArgs& a, int64_t g, float acc[8]) {
+    for (int r = 0; r < a.M; ++r) {
+        const float* p = reinterpret_cast<const float*>(a.grads[r]) + g;
+        const float4 x0 = __ldg(reinterpret_cast<const float4*>(p)), x1 = __ldg(reinterpret_cast<const float4*>(p + 4));
+        acc[0] = __fadd_rn(acc[0], x0.x);
+        acc[1] = __fadd_rn(acc[1], x0.y);
+        acc[2] = __fadd_rn(acc[2], x0.z);
+        acc[3] = __fadd_rn(acc[3], x0.w);
+        acc[4] = __fadd_rn(acc[4], x1.x);
+        acc[5] = __fadd_rn(acc[5], x1.y);
+        acc[6] = __fadd_rn(acc[6], x1.z);
+        acc[7] = __fadd_rn(acc[7], x1.w);
+    }
+}
+
 // GROUPED selects the hybrid-sharding order at compile time, so the plain kernels carry no
 // branch that would keep the compiler from issuing the state loads beside the gradient loads.
-template <int MT, int PATH, bool GROUPED>
+// F32SRC: the sources are fp32 (rank_sum_f32), not bf16.
+template <int MT, int PATH, bool GROUPED, bool F32SRC = false>
 __device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t g, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
-    if constexpr (GROUPED && MT > 0) {
+    if constexpr (F32SRC) {
+        rank_sum_f32(a, g, acc);
+    } else if constexpr (GROUPED && MT > 0) {
         rank_sum_grouped_fixed<MT, PATH>(a, g, acc);
     } else if constexpr (GROUPED) {
         rank_sum_grouped<PATH>(a, g, acc);
@@ -434,7 +455,7 @@ __device__ __forceinline__ double block_sum(double x) {
 // K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
 // ---------------------------------------------------------------------------------------
 template <int MT, bool WRITE, bool GROUPED = false, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly,
-          bool PDL = false>
+          bool PDL = false, bool F32SRC = false>
 __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     const PdlScope<PDL> pdl(a.pdl);
     SumSq acc;
@@ -448,7 +469,7 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
             c.seek(o);
             float sum[8], gh[8];
             if (!ZG_OK(a.status, o - a.gbase >= 0 && o - a.gbase + 8 <= a.gext, kSiteGradNorm, o)) continue;
-            rank_sum<MT, kGradLoadRsNorm, GROUPED>(a, o - a.gbase, sum);
+            rank_sum<MT, kGradLoadRsNorm, GROUPED, F32SRC>(a, o - a.gbase, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
             if (WRITE && ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatWrite, o)) {
                 st_f4<kGhatStoreRsNorm>(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
@@ -565,7 +586,7 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
 // leaves registers. SCALE applies the clip scale computed by K2 (recompute form). Runs over
 // vecs [vbeg, vend): the whole layout, or one bucket (ZeRO-2 per-bucket steps).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false, bool PDL = false>
+template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false, bool PDL = false, bool F32SRC = false>
 __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
     const PdlScope<PDL> pdl(a.pdl);
     float s = 1.0f;
@@ -591,7 +612,7 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
         // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
         load_state<kStateLoadRsAdamw>(a, o, p, m, v);
-        rank_sum<MT, kGradLoadRsAdamw, GROUPED>(a, o, sum);  // grads[r] is addressed by absolute lane
+        rank_sum<MT, kGradLoadRsAdamw, GROUPED, F32SRC>(a, o, sum);  // grads[r] is addressed by absolute lane
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
         adam_vec<SCALE>(gh, s, p, m, v, k);
@@ -708,7 +729,8 @@ __global__ void __launch_bounds__(kThreadsGather) k_gather(const uint16_t* __res
 // ---------------------------------------------------------------------------------------
 // State in: master (and optionally m, v; zeros when null) from unpadded vectors scattered
 // into the padded layout (padding 0), plus the bf16 copies of the parameters. One lane per
-// thread (not a hot kernel). Serves initialisation and checkpoint loading.
+// thread (not a hot kernel). Serves initialisation and checkpoint loading. Any output may be
+// null (the padded full parameters of the process-per-rank mode are written alone).
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__ init, const float* __restrict__ m_init,
                                                    const float* __restrict__ v_init, float* master, float* m,
@@ -725,9 +747,9 @@ __global__ void __launch_bounds__(kThreadsInit) k_init(const float* __restrict__
         const int64_t u = o - c.e.off + c.e.uoff;
         if (!ZG_OK(st, !real || (u >= 0 && u < n), kSiteInit, u)) continue;
         const float x = real ? init[u] : 0.0f;
-        master[o] = x;
-        m[o] = (real && m_init) ? m_init[u] : 0.0f;
-        v[o] = (real && v_init) ? v_init[u] : 0.0f;
+        if (master) master[o] = x;
+        if (m) m[o] = (real && m_init) ? m_init[u] : 0.0f;
+        if (v) v[o] = (real && v_init) ? v_init[u] : 0.0f;
         const uint16_t h = to_bf16(x);
         if (shards) shards[o] = h;
         if (real && full) full[u] = h;
@@ -903,6 +925,18 @@ cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStr
         return launch_pdl(ByM<RsNormWritePdl>::get(a.M, a.groups), grid, kThreadsRsNormWrite, s, a);
     if (write_ghat) ByM<RsNormWrite>::get(a.M, a.groups)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
     else ByM<RsNormOnly>::get(a.M, a.groups)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_norm_f32src(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
+    if (write_ghat) k_rs_norm<0, true, false, kThreadsRsNormWrite, false, true><<<grid, kThreadsRsNormWrite, 0, s>>>(a);
+    else k_rs_norm<0, false, false, kThreadsRsNormOnly, false, true><<<grid, kThreadsRsNormOnly, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_adamw_f32src(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
+    if (apply_scale) k_rs_adamw<0, true, false, false, false, true><<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    else k_rs_adamw<0, false, false, false, false, true><<<grid, kThreadsRsAdamw, 0, s>>>(a);
     return cudaGetLastError();
 }
 
