@@ -528,20 +528,28 @@ int zero_last_cuda_error(void);
  * sums, bucket table: 98,560 bytes) is a fixed array inside the library image, which every
  * GPU that loads the library holds until the process exits. It calls no cudaMalloc,
  * cudaFree or other allocating routine.
- *  grads         M device pointers, bf16 [npad] each in the padded layout, 16-byte aligned
+ *  grads         M device pointers, bf16 [npad] each in the padded layout, 16-byte aligned,
+ *                all on one device (the device of grads[0] runs the call)
  *  M             1..ZERO_MAX_RANKS
  *  bucket_table  host array, 4 int64 per bucket {off_b, n_b, S_b, unused} as written by
  *                zero_plan_layout; buckets must tile [0, npad) from lane 0
  *  n_buckets     1..ZERO_NOALLOC_MAX_BUCKETS; more returns ZERO_ERR_TOO_LARGE
- *  norm_out      device double (8-byte aligned), receives the norm
- *  scale_out     device float (4-byte aligned), receives the clip scale
+ *  norm_out      device double (8-byte aligned) on that device, receives the norm
+ *  scale_out     device float (4-byte aligned) on that device, receives the clip scale
+ *  stream        NULL or a stream of that device
+ * A gradient or output that is not device memory of that device, or a stream of another
+ * device, returns INVALID_ARG before anything is enqueued.
  * Asynchronous on `stream`. The first call on a device also does that device's set-up
- * (looks up the fixed array's device address and the launch shape); make that first call
- * before any stream capture. All calls share the one array, which keeps the last call's
- * contents; nothing in it has to start at zero (every value a call reads is written
- * earlier in the same call). Calls whose work overlaps on the GPU -- on different streams,
- * or from different threads -- race on the array and must be serialised by the caller.
- * Errors: INVALID_ARG, MISALIGNED, TOO_LARGE, CUDA. */
+ * (looks up the fixed array's device address and the launch shapes of every M); make that
+ * first call before any stream capture. The set-up is kept for the life of the process:
+ * after cudaDeviceReset of a device the entry point must not be used on it again. All calls
+ * share the one array, which keeps the last call's contents; nothing in it has to start at
+ * zero (every value a call reads is written earlier in the same call). Calls whose work
+ * overlaps on the GPU -- on different streams, or from different threads -- race on the
+ * array and must be serialised by the caller. In the bounds-checked build
+ * (zero_checked_build() == 1) the call clears the array's status word first, waits for its
+ * stream at the end and returns ZERO_ERR_DEVICE if a bounds check failed.
+ * Errors: INVALID_ARG, MISALIGNED, TOO_LARGE, CUDA, DEVICE (checked build). */
 int zero_grad_norm_noalloc(const void* const* grads, int M, const int64_t* bucket_table,
                            int64_t n_buckets, double max_grad_norm, double* norm_out,
                            float* scale_out, void* stream);

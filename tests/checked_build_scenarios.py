@@ -6,6 +6,7 @@ each the device must report no failed bounds check. Exits non-zero on the first 
 """
 import ctypes
 import gc
+import math
 import os
 import sys
 
@@ -187,9 +188,27 @@ def main():
     ptrs = (ctypes.c_void_p * ws.M)(*[x.data_ptr() for x in g])
     no = torch.empty(1, dtype=torch.float64, device=dev)
     so = torch.empty(1, dtype=torch.float32, device=dev)
+    # in the checked build the call waits and returns ZERO_ERR_DEVICE if a check failed
     rc = zg._lib().zero_grad_norm_noalloc(ctypes.cast(ptrs, ctypes.c_void_p), ws.M, ctypes.cast(table, ctypes.c_void_p),
                                           len(opt.buckets), 1.0, no.data_ptr(), so.data_ptr(), None)
-    assert rc == 0 and float(no.item()) > 0
+    assert rc == 0, f"allocation-free norm: status {rc}"
+    pn = O.plan(ws.numel, ws.M, ws.bucket_bytes)
+    want = math.sqrt(O.global_sumsq(pn, O.reduce_scatter(pn, [u16(x) for x in g])))
+    assert abs(float(no.item()) - want) <= 1e-7 * want, "allocation-free norm vs the oracle"
+
+    # process-per-rank mode: flat (multi-bucket, both clipped forms, unclipped) and hybrid
+    import test_sharded_gpu as TS
+    for kw in ({"M": 4, "stage": 3, "clip": True, "ghat_mode": "materialize"},
+               {"M": 3, "stage": 1, "clip": True, "ghat_mode": "recompute"},
+               {"M": 4, "stage": 2, "clip": False},
+               {"M": 4, "stage": 1, "clip": True, "groups": 2},
+               {"M": 8, "stage": 3, "clip": False, "groups": 2}):
+        ranks, _, _ = TS._run(TS.RAGGED, bucket_bytes=6000, steps=2, **kw)
+        for rc_ in ranks:
+            site, idx = ctypes.c_int64(), ctypes.c_int64()
+            assert zg._lib().zero_check_report(rc_.ctx, ctypes.byref(site), ctypes.byref(idx)) == 0
+            assert site.value == 0, f"rank {rc_.rank} {kw}: bounds check {site.value} failed at {idx.value}"
+            rc_.close()
     print("checked build: all scenarios clean")
 
 

@@ -9,6 +9,7 @@
 // is part of the library image instead: every GPU that loads the library holds it until
 // the process exits.
 
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -46,26 +47,41 @@ struct DeviceGuard {
 int fail(cudaError_t e) { return zg::record_cuda_error(e); }
 
 // Set-up, once per device, with that device current: the scratch array's device address
-// and the launch grid (same rule as the regular path, so both sum in the same order).
+// and the launch grid for every rank count 1..ZERO_MAX_RANKS (same rule as the regular path,
+// so both sum in the same order). All of it happens in the device's first call, so no later
+// call, whatever its M, queries the runtime.
 int setup(int dev, int M, void** addr, int* grid_cap) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_addr[dev]) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return fail(e);
-        g_addr[dev] = p;
-    }
-    if (!g_grid[dev][M]) {
-        int per_sm = 0, sms = 0;
-        cudaError_t e = zg::variant_blocks_per_sm(zg::kVarRsNormOnly, M, 1, &per_sm);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail(e);
-        int g = (per_sm < 1 ? 1 : per_sm) * sms;
-        g_grid[dev][M] = g > zg::kMaxPartials ? zg::kMaxPartials : g;
+        for (int m = 1; m <= ZERO_MAX_RANKS; ++m) {
+            int per_sm = 0;
+            e = zg::variant_blocks_per_sm(zg::kVarRsNormOnly, m, 1, &per_sm);
+            if (e != cudaSuccess) return fail(e);
+            const int g = (per_sm < 1 ? 1 : per_sm) * sms;
+            g_grid[dev][m] = g > zg::kMaxPartials ? zg::kMaxPartials : g;
+        }
+        g_addr[dev] = p;  // last: set-up is complete once the address is published
     }
     *addr = g_addr[dev];
     *grid_cap = g_grid[dev][M];
     return ZERO_OK;
+}
+
+// A pointer the call may hand to its kernels: device (or managed) memory on device `dev`.
+bool on_device(const void* p, int dev) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error of an unknown pointer
+        return false;
+    }
+    if (attr.type == cudaMemoryTypeManaged) return true;
+    return attr.type == cudaMemoryTypeDevice && attr.device == dev;
 }
 
 // Up to 64 bucket-table rows, passed by value, written into the fixed scratch.
@@ -99,23 +115,42 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
         if (!grads[r]) return ZERO_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(grads[r]) & 15u) return ZERO_ERR_MISALIGNED;
     }
-    // The table must tile the padded layout contiguously from lane 0, in vecs of 8 lanes.
+    // The table must tile the padded layout contiguously from lane 0, in vecs of 8 lanes
+    // (S is bounded before any product is formed, so no sum or product overflows).
     int64_t off = 0;
     for (int64_t b = 0; b < n_buckets; ++b) {
         const int64_t o = bucket_table[4 * b], n = bucket_table[4 * b + 1], S = bucket_table[4 * b + 2];
-        if (o != off || S < 0 || n < 0 || n > M * S || (M * S) % 8 != 0) return ZERO_ERR_INVALID_ARG;
+        if (o != off || S < 0 || n < 0 || S > (INT64_MAX - off) / M) return ZERO_ERR_INVALID_ARG;
+        if (n > M * S || (M * S) % 8 != 0) return ZERO_ERR_INVALID_ARG;
         off += M * S;
     }
     const int64_t npad = off;
 
+    // The device is the one that holds the gradients: every gradient and both outputs must
+    // be device memory there (a pointer to another GPU's memory, or to host memory, is
+    // refused rather than read across devices), and so must the stream, if one is given.
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, grads[0]);
-    if (e != cudaSuccess) return fail(e);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ZERO_ERR_INVALID_ARG;
+    }
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return ZERO_ERR_INVALID_ARG;
-    const int dev = attr.device;
+    int dev = attr.device;
+    if (attr.type == cudaMemoryTypeManaged && cudaGetDevice(&dev) != cudaSuccess) return ZERO_ERR_INVALID_ARG;
     if (dev < 0 || dev >= kMaxDevices) return ZERO_ERR_INVALID_ARG;
+    for (int r = 1; r < M; ++r)
+        if (!on_device(grads[r], dev)) return ZERO_ERR_INVALID_ARG;
+    if (!on_device(norm_out, dev) || !on_device(scale_out, dev)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(dev);
     if (!guard.ok) return fail(cudaErrorInvalidDevice);
+    if (stream) {  // with `dev` current, so that the special stream handles resolve to it
+        int sdev = -1;
+        if (cudaStreamGetDevice((cudaStream_t)stream, &sdev) != cudaSuccess || sdev != dev) {
+            cudaGetLastError();
+            return ZERO_ERR_INVALID_ARG;
+        }
+    }
     void* base = nullptr;
     int grid_cap = 0;
     int rc = setup(dev, M, &base, &grid_cap);
@@ -164,12 +199,27 @@ extern "C" int zero_grad_norm_noalloc(const void* const* grads, int M, const int
     if (need < 1) need = 1;
     const int grid = (int)(need < grid_cap ? need : grid_cap);
     // Every partial the finalise kernel reads is written by this call's norm pass, and the
-    // status word is written whole, so nothing in the scratch has to be cleared first.
+    // status word is written whole, so nothing in the scratch has to be cleared first. The
+    // bounds-checked build is the exception: its failed-check record is sticky, so each
+    // call starts from a cleared status word (a memset of the fixed array, no allocation).
+#ifdef ZERO_CHECKED
+    e = cudaMemsetAsync(status, 0, sizeof(zg::Status), s);
+    if (e != cudaSuccess) return fail(e);
+#endif
     e = zg::launch_rs_norm(a, false, grid, s);
     if (e == cudaSuccess) e = zg::launch_norm_final(status, partials, grid, max_grad_norm, 1, false, s);
     if (e == cudaSuccess) {
         k_copy_result<<<1, 1, 0, s>>>(status, norm_out, scale_out);
         e = cudaGetLastError();
     }
-    return e == cudaSuccess ? ZERO_OK : fail(e);
+    if (e != cudaSuccess) return fail(e);
+#ifdef ZERO_CHECKED
+    // checked build only: wait, and report a failed bounds check of this call
+    zg::Status st;
+    e = cudaMemcpyAsync(&st, status, sizeof st, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(e);
+    if (st.flags & zg::kFlagBounds) return ZERO_ERR_DEVICE;
+#endif
+    return ZERO_OK;
 }
