@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
                     help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
                          "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+    ap.add_argument("--shard", action="store_true",
+                    help="process-per-rank mode: the job's M ranks are the N processes (one per GPU, NCCL), "
+                         "each holding only its shard; the workload's tensors, stage, clipping and buckets "
+                         "with M = N. Strong scaling: the whole job steps the workload's parameters once")
     ap.add_argument("--stream-form", default="auto", choices=["auto", "fused", "reduce-apply"],
                     help="--mode stream: one fused pass per bucket (no clipping) or reduce-scatter of every "
                          "bucket then one update (auto: fused when the workload does not clip)")
@@ -447,7 +451,8 @@ def run_ours(args):
     clk = clocks.stop()
     barrier(dist, device)
     ms_total = ev[0].elapsed_time(ev[-1])
-    step_ms = step_stats([ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)], dist, device)
+    per_step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    step_ms = step_stats(per_step_ms, dist, device)
     ktimes = opt.kernel_times()
     opt.set_timing(False)
     ms_total_max = max_over_ranks(dist, ms_total, device)
@@ -527,14 +532,17 @@ def run_ours(args):
         e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3, device)
         e2e_step_ms = [round(marks[i].elapsed_time(marks[i + 1]), 2) for i in range(args.e2e_steps)]
         h2d_after = copy_rate([(sets[0][r], host_grads[r]) for r in range(w.M)], copy_stream)
+        h2d_bytes = sum(g.numel() * 2 for g in host_grads)
         e2e = {"value": world * n * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
-               "ms_per_step": e2e_ms / args.e2e_steps, "call": "zero_step_host_overlapped",
+               "ms_per_step": e2e_ms / args.e2e_steps, "ms_per_step_median": statistics.median(e2e_step_ms),
+               "call": "zero_step_host_overlapped",
                "h2d_bytes_per_step": sum(g.numel() * 2 for g in host_grads), "d2h_bytes_per_step": n * 2,
                "host_gradients": (f"{w.M} pinned replicas" if distinct else
                                   f"one pinned replica copied to all {w.M} device buffers (host memory)"),
                "h2d_copy_gbs": round(h2d_gbs, 1), "d2h_copy_gbs": round(d2h_gbs, 1),
                "h2d_copy_gbs_after": round(h2d_after, 1), "step_ms": e2e_step_ms,
-               "copy_floor_ms": round(sum(g.numel() * 2 for g in host_grads) / h2d_gbs / 1e6, 2)}
+               "copy_floor_ms": round(h2d_bytes / h2d_gbs / 1e6, 2),
+               "copy_floor_ms_after": round(h2d_bytes / h2d_after / 1e6, 2)}
         del host_grads, host_params, sets, srcs
 
     cpu = None
@@ -556,6 +564,7 @@ def run_ours(args):
                        "parallelism": f"{world} independent emulated jobs (one per GPU)"},
             "gbs_alg": round(gbs_alg, 1), "alg_bytes_per_param": alg_bytes_per_param(w.M),
             "frac_of_peak_alg": round(gbs_alg / peak, 4),
+            **target_stats(per_step_ms, alg_b, peak, dist, device),
             "real_bytes_per_param": real_bytes_per_param(w.M, clip, ghat_mode),
             "gbs_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9, 1),
             "frac_of_peak_real": round(real_bytes_per_param(w.M, clip, ghat_mode) * n / (ms_per_step / 1e3) / 1e9
@@ -563,7 +572,7 @@ def run_ours(args):
             "frac_of_vendor_hbm_alg": round(gbs_alg / VENDOR_HBM_GBS, 4),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         }
-        print(json.dumps(line), flush=True)
+        print_line(line)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -590,7 +599,7 @@ def run_reference(args):
         "cpu_baseline": {"value": rate, "unit": "params/s", "cores": procs, "kind": "oracle", "sample": sample},
         "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    print_line(line)
 
 
 def _timed_region(fn, steps, stream, dist, device):
@@ -628,6 +637,22 @@ def l2_note(input_bytes):
         return f"inputs {input_bytes / 1e9:.2f} GB > L2 {L2_BYTES / 1e6:.0f} MB; no flush"
     return (f"inputs {input_bytes / 1e6:.3f} MB fit in L2 {L2_BYTES / 1e6:.0f} MB and are not flushed: "
             f"a latency figure for a launch-bound step, not a bandwidth one")
+
+
+TARGET_FRAC_ALG = 0.80  # the step's bandwidth target: this fraction of the measured HBM peak
+
+
+def target_stats(per_step_ms, alg_bytes, peak, dist, device):
+    """How the individual timed steps stand against the bandwidth target: each step's fraction
+    of the peak under the algorithmic bytes (a rank's step counts at its own time; with several
+    ranks the count is the smallest over ranks), and how many steps reach the target."""
+    fr = [alg_bytes / (t / 1e3) / 1e9 / peak for t in per_step_ms]
+    hits = sum(f >= TARGET_FRAC_ALG for f in fr)
+    if dist is not None:
+        hits = int(-max_over_ranks(dist, -float(hits), device))
+    return {"target_frac_alg": TARGET_FRAC_ALG, "steps_at_or_above_target": int(hits),
+            "step_frac_alg": {"min": round(min(fr), 4), "median": round(statistics.median(fr), 4),
+                              "max": round(max(fr), 4)}}
 
 
 def step_stats(ms, dist, device):
@@ -751,7 +776,7 @@ def run_stream(args):
         dom_name = "adamw" if dom == "adamw" else "rs_norm_write (all buckets)"
         dom_bytes, dom_ms = (30 * lanes, up_ms) if dom == "adamw" else ((2 * w.M + 4) * lanes, rs_ms)
     if rank == 0:
-        print(json.dumps({
+        print_line({
             "metric": METRIC + " (ZeRO-2 per-bucket streaming)", "mode": "stream", "value": world * n * args.steps / (ms / 1e3),
             "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "ms_per_step_median": step_ms["median"], "ms_per_step_min": step_ms["min"],
@@ -768,7 +793,7 @@ def run_stream(args):
                          "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4), "traffic": None,
                          "peak_source": kind, "kernel_share": {k: round(v[0] / ms, 4) for k, v in kt.items() if v[1]}},
-            "gpu_launches": int(sum(c for _, c in kt.values())), "clocks": clk}), flush=True)
+            "gpu_launches": int(sum(c for _, c in kt.values())), "clocks": clk})
     if dist is not None:
         dist.destroy_process_group()
 
@@ -831,7 +856,7 @@ def run_gather(args):
     g_ms, g_cnt = ms, nb * args.steps
     achieved = 4 * n * args.steps / (g_ms / 1e3) / 1e9
     if rank == 0:
-        print(json.dumps({
+        print_line({
             "metric": "params/s and achieved HBM GB/s of the ZeRO-3 per-bucket parameter all-gather", "mode": "gather",
             "value": world * n * args.steps / (ms / 1e3), "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "ms_per_step_median": step_ms["median"],
@@ -847,15 +872,147 @@ def run_gather(args):
                          "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None, "peak_source": kind,
                          "alg_bytes_per_param": 4, "avg_launch_ms": round(g_ms / max(g_cnt, 1), 4)},
-            "gpu_launches": int(g_cnt), "clocks": clk}), flush=True)
+            "gpu_launches": int(g_cnt), "clocks": clk})
     if dist is not None:
         dist.destroy_process_group()
+
+
+def print_line(line: dict):
+    """The one JSON line. C-level stdout of the libraries (NCCL prints its version there) is
+    flushed first, so that the line is the last one the process writes."""
+    import ctypes
+    try:
+        ctypes.CDLL(None).fflush(None)
+    except (OSError, AttributeError):
+        pass
+    sys.stdout.write(json.dumps(line) + "\n")
+    sys.stdout.flush()
+
+
+def run_shard(args):
+    """Process-per-rank ZeRO step: N processes (torchrun, one per GPU, NCCL; N = 1 runs a job of
+    one rank) form one job of M = N ranks over the workload's tensors. Per step every rank
+    exchanges its gradient's bucket slices with the others (all-to-all), sums its shard's
+    slices in rank order and updates it (the library's kernels), and all-gathers the bf16
+    parameters; with clipping one fp64 per rank is all-gathered in between. The timed region
+    holds the collectives and the kernels: the job steps w.N parameters per step."""
+    import datetime
+    import socket
+
+    import torch
+    import torch.distributed as tdist
+
+    import workloads as W
+    import zero_gradient_reduce_scatter_gb300 as zg
+    from zero_gradient_reduce_scatter_gb300 import _build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if world == 1 and "MASTER_PORT" not in os.environ:
+        s = socket.socket()
+        s.bind(("127.0.0.1", 0))
+        os.environ["MASTER_PORT"] = str(s.getsockname()[1])
+        s.close()
+    tdist.init_process_group("nccl", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=600),
+                             device_id=device)
+    dist = tdist if world > 1 else None
+    if not os.path.exists(_build.LIB_PATH):
+        if rank == 0:
+            _build.build()
+        tdist.barrier(device_ids=[local])
+    w0 = workload(args)
+    w = W.small_variant(w0, w0.numel, name=w0.name, M=world)
+    opt = zg.ShardedZeroOptimizer(w.numel, w.stage, W.master_init(w, device), bucket_bytes=w.bucket_bytes,
+                                  full_params=True)
+    grad = opt.new_grad_buffer()
+    W.fill_grads(w, rank, 0, grad, opt.tensor_offsets)
+    clip = w.clip is not None
+    h = zg.Hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip=clip,
+                 max_grad_norm=w.clip or 1.0, ghat_mode=args.ghat_mode)
+    ghat_mode = args.ghat_mode
+    if ghat_mode == "auto":
+        ghat_mode = ("materialize" if (w.M > 4 and opt.ghat is not None) else "recompute") if clip else "none"
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        opt.step(grad, h)
+    torch.cuda.synchronize()
+    if opt.sync_status() != 0:
+        raise SystemExit("warm-up step saw a non-finite gradient norm")
+    opt.set_timing(True)
+    opt.kernel_times()
+    ms_total, clk, step_ms = _timed_region(lambda: opt.step(grad, h), args.steps, stream, dist, device)
+    kt = opt.kernel_times()
+    opt.set_timing(False)
+    n, L = w.N, opt.sizes["shard_len"]
+    ms_per_step = ms_total / args.steps
+    peak, peak_kind = hbm_peak()
+    # each kernel kind covers the rank's shard once per step (in one launch per bucket where
+    # it reads the exchanged slices): the dominant kernel's algorithmic bytes per step over
+    # its time per step
+    dom = max((k for k in kt if kt[k][1] > 0), key=lambda k: kt[k][0])
+    dom_step_bytes = kernel_alg_bytes_per_lane(dom, w.M, ghat_mode == "materialize") * L
+    dom_ms = kt[dom][0] / args.steps
+    dom_launches = kt[dom][1] / args.steps
+    achieved = dom_step_bytes / (dom_ms / 1e3) / 1e9
+    kernel_ms = sum(v[0] for v in kt.values()) / args.steps
+
+    e2e = None
+    if not args.no_e2e:  # the rank's gradient from pinned host memory in, the parameters out
+        host_g = torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
+        host_g.copy_(grad)
+        host_p = torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
+
+        def e2e_step():
+            grad.copy_(host_g, non_blocking=True)
+            opt.step(grad, h)
+            host_p.copy_(opt.params(), non_blocking=True)
+
+        e2e_step()
+        e_ms, _, e_stats = _timed_region(e2e_step, args.e2e_steps, stream, dist, device)
+        e2e = {"value": n / (e_ms / args.e2e_steps / 1e3), "unit": "params/s", "ms_per_step": e_ms / args.e2e_steps,
+               "ms_per_step_median": e_stats["median"], "call": "ShardedZeroOptimizer.step",
+               "h2d_bytes_per_step": 2 * opt.sizes["npad"] * world, "d2h_bytes_per_step": 2 * opt.sizes["npad"] * world}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_procs)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": n / (ms_per_step / 1e3), "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "ms_per_step_median": step_ms["median"], "ms_per_step_min": step_ms["min"], "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w0.name + f"; process per rank: M = {world}", "params": n, "M": world,
+                       "stage": w.stage, "clip": w.clip, "bucket_bytes": w.bucket_bytes, "ghat_mode": ghat_mode,
+                       "padded_lanes": opt.sizes["npad"], "shard_lanes": L,
+                       "l2": l2_note(opt.sizes["bytes_grad_each"] * 2 + 12 * L),
+                       "parallelism": f"zero-dp{world}: one process per GPU, state sharded over {world} ranks "
+                                      f"(NCCL all-to-all of bf16 bucket slices, rank-ordered fp32 sum at the owner, "
+                                      f"bf16 all-gather)"},
+            "kernel_ms_per_step": round(kernel_ms, 4),
+            "collective_ms_per_step": round(ms_per_step - kernel_ms, 4),
+            "frac_of_peak_alg_kernels": round(alg_bytes_per_param(w.M) * L / (kernel_ms / 1e3) / 1e9 / peak, 4),
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                         "alg_bytes_per_launch": dom_step_bytes / max(dom_launches, 1),
+                         "avg_launch_ms": round(dom_ms / max(dom_launches, 1), 4),
+                         "launches_per_step": dom_launches},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(sum(v[1] for v in kt.values())), "clocks": clk,
+        }
+        print_line(line)
+    opt.close()
+    tdist.destroy_process_group()
 
 
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.shard:
+        run_shard(args)
     elif args.mode == "stream":
         run_stream(args)
     elif args.mode == "gather":

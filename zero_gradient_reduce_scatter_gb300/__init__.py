@@ -431,7 +431,7 @@ class ZeroOptimizer:
             raise RuntimeError(f"could not find {count} distinct side streams")
         return out
 
-    def prefetched_buckets(self, order, stream=None, side_stream=None, buffers: int = 2):
+    def prefetched_buckets(self, order, stream=None, side_stream=None, buffers: int = 4):
         """ZeRO-3 just-in-time parameters with prefetch.
 
         Yields (bucket, params) in `order`; `params` (bf16, the bucket's n_b values) is ready
@@ -442,6 +442,10 @@ class ZeroOptimizer:
         side stream of its own (`side_stream` may be one stream or a sequence; missing ones
         are made), so consecutive gathers do not wait for each other: each waits only for its
         buffer's last consumer, and another buffer's gather runs while it waits.
+        The default of four buffers is the measured best on GB300: a 129-bucket sweep of the
+        4B layout took 2.39 ms with four (101.5% of the copy peak, the gather kernels' own
+        time) against 2.58 ms with two and 2.54 with three; six gave no more. The transient
+        memory is `buffers` times the largest bucket.
         """
         order = list(order)
         if not order:
