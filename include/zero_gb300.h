@@ -333,6 +333,19 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
 int zero_rank_step(zero_ctx* ctx, const void* src, const double* sumsq_all, int stage,
                    const zero_hyper* hyper, void* stream);
 
+/* Per-bucket form of zero_rank_step without clipping (flat mode): the update of bucket
+ * `bucket`'s slice of this rank's shard, from src (the exchange buffer; only the bucket's
+ * region, lanes [off_b, off_b + M*S_b), is read, so the call may follow that bucket's
+ * all-to-all while later buckets are still in flight: the ZeRO-2 pattern of reducing each
+ * bucket as soon as its gradients exist, "CS336 2026 Lecture 8" Slide 23, "并行训练优化、
+ * MoE扩展与系统瓶颈" 2.2.4). Every bucket takes step t + 1; the step is complete, and t
+ * advances, once every bucket has been stepped, in any order. Until then zero_rank_step,
+ * zero_rank_sumsq and a second call for the same bucket return INVALID_ARG.
+ * Errors: BAD_CONTEXT, INVALID_ARG (not a flat sharded context, clipping, bad bucket),
+ * STAGE, MISALIGNED, CUDA. */
+int zero_rank_step_bucket(zero_ctx* ctx, int64_t bucket, const void* src, int stage,
+                          const zero_hyper* hyper, void* stream);
+
 /* Clipping, first pass: averages this rank's shard from src (as in zero_rank_step) and writes
  * the fp64 sum of squares over its real lanes to *sumsq (device, 8-byte aligned). Under
  * ZERO_GHAT_MATERIALIZE (or AUTO choosing it) the fp32 average also goes to the ghat buffer,
@@ -503,6 +516,9 @@ int zero_set_max_ctas(zero_ctx* ctx, int ctas);
  *                        the parameter shards) nor access what it writes. Work ordered by an
  *                        event wait (cudaStreamWaitEvent) is not affected: that dependency is
  *                        kept whole.
+ * In process-per-rank mode, either overlap mode also lets the per-bucket launches of one
+ * unclipped zero_rank_step overlap each other (safe by construction: the call's first
+ * launch waits for everything before it). zero_rank_step_bucket launches ordinary kernels.
  * zero_step_bucket_scheduled always launches ordinary kernels. Under either overlap mode each
  * bucket reduction keeps its norm partials in a region of the scratch buffer of its own
  * (zero_plan sizes the scratch for it). With overlap, per-kernel event timing

@@ -125,6 +125,13 @@ def _flat_rank(rank, M, case):
             want = G[src][off + rank * S: off + (rank + 1) * S]
             assert np.array_equal(got[off + src * S: off + (src + 1) * S], want), (b, src)
 
+    # (1b) bucket by bucket, in backward order, asynchronously: the same bytes
+    recv2 = torch.zeros(p.npad, dtype=torch.int16).view(torch.bfloat16)
+    works = exchange_gradients(mine, recv2, buckets, M, which=list(reversed(range(p.nb))), async_op=True)
+    for wk in works:
+        wk.wait()
+    assert torch.equal(recv2.view(torch.int16), recv.view(torch.int16))
+
     # (2) the oracle's reduce-scatter needs nothing else: rebuild the M gradients from the
     # received bytes only (NaN on every lane that did not arrive here) and average
     virt = [np.full(p.npad, BF16_NAN, dtype=np.uint16) for _ in range(M)]

@@ -44,13 +44,15 @@ def _grads(p, M, k, dev, sig_seed=5):
 
 
 def _run(numel, M, stage, clip, ghat_mode="auto", bucket_bytes=0, groups=1, steps=3, max_norm=0.05,
-         ghat_buffer=True, full=True):
+         ghat_buffer=True, full=True, overlap="none"):
     dev = torch.device("cuda")
     K = M // groups
     p = O.plan(numel, K, bucket_bytes)
     w = W.small_variant(W.workload("tiny"), tuple(numel), steps=steps)
     mi = W.master_init(w, dev)
     ranks = [RankCtx(numel, M, r, stage, mi, bucket_bytes, groups, ghat=ghat_buffer, full=full) for r in range(M)]
+    for rc in ranks:
+        assert zg._lib().zero_set_launch_overlap(rc.ctx, zg.OVERLAP[overlap]) == 0
     # the clipped form each rank takes: the average materialized when asked, or by default
     # with more than 4 ranks and a buffer for it
     materialized = clip and ghat_buffer and (ghat_mode == "materialize" or (ghat_mode == "auto" and M > 4))
@@ -114,6 +116,13 @@ def test_sharded_stages_and_clip_forms(stage, ghat_mode):
 @pytest.mark.parametrize("bucket_bytes", [0, 4096])
 def test_sharded_unclipped(bucket_bytes):
     for rc in _run(RAGGED, 4, 2, False, bucket_bytes=bucket_bytes)[0]:
+        rc.close()
+
+
+@pytest.mark.parametrize("overlap", ["launch", "buckets"])
+def test_sharded_unclipped_overlapped_bucket_launches(overlap):
+    # the per-bucket launches of one step overlap each other: results unchanged
+    for rc in _run(RAGGED, 4, 2, False, bucket_bytes=2048, overlap=overlap)[0]:
         rc.close()
 
 
@@ -205,3 +214,45 @@ def test_sharded_argument_errors():
                                1, ctypes.byref(zg.Sizes())) == -1
     rc.close()
     emu.close()
+
+
+def test_sharded_per_bucket_steps_in_any_order():
+    """zero_rank_step_bucket: buckets updated one at a time (reverse order, each right after its
+    own exchange) equal the oracle's step; the step counter advances once all are done."""
+    dev = torch.device("cuda")
+    numel, M, stage = RAGGED, 4, 2
+    p = O.plan(numel, M, 4096)
+    assert p.nb > 3
+    w = W.small_variant(W.workload("tiny"), tuple(numel), steps=2)
+    mi = W.master_init(w, dev)
+    ranks = [RankCtx(numel, M, r, stage, mi, 4096) for r in range(M)]
+    st = O.init_state(p, stage, f32(mi))
+    h = zg.Hyper()
+    lib, s = zg._lib(), zg._stream_handle(None)
+    from rank_util import loopback_exchange, loopback_gather
+    for k in range(2):
+        grads = _grads(p, M, k, dev)
+        loopback_exchange(ranks, grads)
+        for b in reversed(range(p.nb)):
+            for rc in ranks:
+                assert lib.zero_rank_step_bucket(rc.ctx, b, rc.recv.data_ptr(), stage, ctypes.byref(h), s) == 0
+            if b == p.nb - 1:  # a step in progress: no second call for the bucket, no whole step
+                rc = ranks[0]
+                assert lib.zero_rank_step_bucket(rc.ctx, b, rc.recv.data_ptr(), stage, ctypes.byref(h), s) == -1
+                assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr(), None, stage, ctypes.byref(h), s) == -1
+                t = ctypes.c_int64()
+                assert lib.zero_get_step(rc.ctx, ctypes.byref(t)) == 0 and t.value == k
+        loopback_gather(ranks)
+        full, _, _, _ = O.zero_step(p, st, [u16(g) for g in grads], O.hyper())
+        torch.cuda.synchronize()
+        for rc in ranks:
+            assert np.array_equal(f32(rc.master).view(np.uint32), st.master[rc.rank][:p.shard_len].view(np.uint32))
+            assert np.array_equal(f32(rc.v).view(np.uint32), st.var[rc.rank][:p.shard_len].view(np.uint32))
+            assert bf16_ulp_diff(padded_to_unpadded(p, u16(rc.full)), full) == 0
+            t = ctypes.c_int64()
+            assert lib.zero_get_step(rc.ctx, ctypes.byref(t)) == 0 and t.value == k + 1
+    rc = ranks[0]
+    assert lib.zero_rank_step_bucket(rc.ctx, 0, rc.recv.data_ptr(), stage, ctypes.byref(zg.Hyper(clip=True)), s) == -1
+    assert lib.zero_rank_step_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), stage, ctypes.byref(h), s) == -1
+    for rc in ranks:
+        rc.close()

@@ -4,7 +4,8 @@ NCCL does not run two ranks on one device, so the ranks exchange through gloo wi
 device buffers staged through host memory (ShardedZeroOptimizer(transport="host")). Each
 process runs the library's kernels on its own shard only. Three clipped steps on a ragged
 multi-bucket layout, at ZeRO-1 (full parameters kept) and ZeRO-3 (per-bucket gathers into a
-transient buffer), both forms of the clipped step; every rank checks itself against the
+transient buffer), both forms of the clipped step, and three unclipped ZeRO-2 steps streamed
+bucket by bucket in backward order (step_streamed); every rank checks itself against the
 oracle's two-rank step: its shard of master / m / v (1e-6 relative; bit-identical expected),
 the averaged gradient bit-exact when materialized, the norm within 1e-7 and equal on both
 ranks, the gathered bf16 parameters within 1 ulp; then the assembled checkpoint state equals
@@ -52,7 +53,7 @@ def _grads_all(p, M, k):
     return out
 
 
-def _rank_main(rank, world, port, stage, ghat_mode, q):
+def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
         import torch
@@ -74,22 +75,27 @@ def _rank_main(rank, world, port, stage, ghat_mode, q):
         assert opt.M == world and opt.rank == rank and len(opt.buckets) >= 2
         p = O.plan(NUMEL, world, BUCKET_BYTES)
         st = O.init_state(p, stage, f32(mi))
-        h = zg.Hyper(clip=True, max_grad_norm=0.05, ghat_mode=ghat_mode)
-        oh = O.hyper(clip=True, max_grad_norm=0.05)
+        clip = not streamed  # the streamed form does not clip
+        h = zg.Hyper(clip=clip, max_grad_norm=0.05, ghat_mode=ghat_mode)
+        oh = O.hyper(clip=clip, max_grad_norm=0.05)
         scratch = torch.empty(world * max(b[2] for b in opt.buckets), dtype=torch.bfloat16, device=dev)
         for k in range(3):
             G = _grads_all(p, world, k)
             mine = torch.from_numpy(G[rank].view(np.int16).copy()).to(dev).view(torch.bfloat16)
-            opt.step(mine, h)
+            if streamed:  # ZeRO-2 bucket streaming, buckets in backward order
+                opt.step_streamed(mine, h, order=reversed(range(len(opt.buckets))))
+            else:
+                opt.step(mine, h)
             full, norm, scale, rc = O.zero_step(p, st, G, oh)
-            assert rc == 0 and scale < 1.0
+            assert rc == 0 and (scale < 1.0 or streamed)
             assert opt.sync_status() == 0
-            gn, gs = opt.last_norm()
-            assert abs(gn - norm) <= 1e-7 * norm
-            both = torch.tensor([gn, gs], dtype=torch.float64)
-            seen = [torch.zeros(2, dtype=torch.float64) for _ in range(world)]
-            dist.all_gather(seen, both)
-            assert all(torch.equal(x, seen[0]) for x in seen), "both ranks form the same norm and scale"
+            if clip:
+                gn, gs = opt.last_norm()
+                assert abs(gn - norm) <= 1e-7 * norm
+                both = torch.tensor([gn, gs], dtype=torch.float64)
+                seen = [torch.zeros(2, dtype=torch.float64) for _ in range(world)]
+                dist.all_gather(seen, both)
+                assert all(torch.equal(x, seen[0]) for x in seen), "both ranks form the same norm and scale"
             assert_state_close(f32(opt.get_state("master")), st.master[rank][:p.shard_len], f"step {k} master")
             assert_state_close(f32(opt.get_state("m")), st.mom[rank][:p.shard_len], f"step {k} m")
             assert_state_close(f32(opt.get_state("v")), st.var[rank][:p.shard_len], f"step {k} v")
@@ -122,12 +128,13 @@ def _rank_main(rank, world, port, stage, ghat_mode, q):
         q.put((rank, traceback.format_exc()))
 
 
-@pytest.mark.parametrize("stage,ghat_mode", [(1, "materialize"), (3, "recompute"), (3, "materialize")])
-def test_two_processes_on_one_gpu(stage, ghat_mode):
+@pytest.mark.parametrize("stage,ghat_mode,streamed", [(1, "materialize", False), (3, "recompute", False),
+                                                      (3, "materialize", False), (2, "auto", True)])
+def test_two_processes_on_one_gpu(stage, ghat_mode, streamed):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, stage, ghat_mode, q)) for r in range(2)]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, stage, ghat_mode, q, streamed)) for r in range(2)]
     for p in procs:
         p.start()
     got = dict(q.get(timeout=600) for _ in procs)

@@ -1118,6 +1118,7 @@ int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
 int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* sumsq, void* stream) {
     int rc = check_rank_ctx(c);
     if (rc) return rc;
+    if (c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if ((rc = check_hyper(h))) return rc;
     if (!h->clip || !src || !sumsq) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src) || (reinterpret_cast<uintptr_t>(sumsq) & 7u)) return ZERO_ERR_MISALIGNED;
@@ -1172,6 +1173,7 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
                    void* stream) {
     int rc = check_rank_ctx(c);
     if (rc) return rc;
+    if (c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     if ((rc = check_hyper(h))) return rc;
     const int clip = h->clip;
@@ -1206,10 +1208,18 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
         Timed tm(c, ZERO_K_RS_ADAMW, s);
         e = zg::launch_rs_adamw_f32src(a, clip != 0, g4, s);
     } else if (e == cudaSuccess) {
-        for (int64_t b = 0; b < (int64_t)c->buckets.size() && e == cudaSuccess; ++b) {
+        // one fused launch per bucket. Without clipping, under launch overlap (any mode but
+        // ZERO_OVERLAP_NONE) the buckets' launches overlap: they touch disjoint lanes and read
+        // only sources complete before the call's first launch (which waits for everything
+        // before it), and each still completes after the one before it, so stream order
+        // holds for later work
+        const int64_t nb = (int64_t)c->buckets.size();
+        const bool overlap = !clip && nb > 1 && c->overlap != ZERO_OVERLAP_NONE;
+        for (int64_t b = 0; b < nb && e == cudaSuccess; ++b) {
             zg::StepArgs a = rank_args(c);
             slice_sources(c, a, src, b, c->cfg.M, true);
             a.k = k;
+            if (overlap) a.pdl = b == 0 ? zg::kPdlWaitFirst : zg::kPdlWaitLast;
             const int g4 = grid_for(c, clip ? zg::kVarRsAdamwScaled : zg::kVarRsAdamwPlain, a.vend - a.vbeg);
             Timed tm(c, ZERO_K_RS_ADAMW, s);
             e = zg::launch_rs_adamw(a, clip != 0, false, g4, s);
@@ -1220,6 +1230,41 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
     c->last_clip = clip;
     c->last_stream = s;
     c->stepped = 1;
+    return ZERO_OK;
+}
+
+int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stage, const zero_hyper* h,
+                          void* stream) {
+    int rc = check_rank_ctx(c);
+    if (rc) return rc;
+    if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
+    if ((rc = check_hyper(h))) return rc;
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (h->clip || hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
+    if (c->rank_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
+    if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    zg::StepArgs a = rank_args(c);
+    slice_sources(c, a, src, bucket, c->cfg.M, true);
+    a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
+    const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_RS_ADAMW, s);
+        e = zg::launch_rs_adamw(a, false, false, g4, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->bucket_done[(size_t)bucket] = 1;
+    c->last_stream = s;
+    if (++c->n_bucket_done == nb) {  // the step is complete
+        std::fill(c->bucket_done.begin(), c->bucket_done.end(), 0);
+        c->n_bucket_done = 0;
+        c->t += 1;
+        c->last_clip = 0;
+        c->stepped = 1;
+    }
     return ZERO_OK;
 }
 

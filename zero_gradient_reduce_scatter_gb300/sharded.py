@@ -43,26 +43,39 @@ def _bytes(t: torch.Tensor) -> torch.Tensor:
 
 
 # ---- the collectives of a step, on any device (plain torch.distributed calls) ---------------
-def exchange_gradients(grad: torch.Tensor, recv: torch.Tensor, buckets, count: int, group=None):
-    """The exchange that feeds the reduce-scatter: for every bucket (off, n, S, _), the
-    all-to-all of its `count` slices, recv[off + q*S : off + (q+1)*S] = source q's
-    grad[off + me*S : off + (me+1)*S], with `me` this process's index in `group`.
-    grad and recv: bf16 [npad] in the padded layout (the same layout on every rank)."""
+def exchange_gradients(grad: torch.Tensor, recv: torch.Tensor, buckets, count: int, group=None,
+                       which=None, async_op: bool = False):
+    """The exchange that feeds the reduce-scatter: for every bucket (off, n, S, _) (or the
+    buckets listed in `which`), the all-to-all of its `count` slices,
+    recv[off + q*S : off + (q+1)*S] = source q's grad[off + me*S : off + (me+1)*S], with `me`
+    this process's index in `group`. grad and recv: bf16 [npad] in the padded layout (the
+    same layout on every rank). Returns the collectives' work handles when async_op."""
     import torch.distributed as dist
-    for off, _n, S, _ in buckets:
+    works = []
+    for b in (range(len(buckets)) if which is None else which):
+        off, _n, S, _ = buckets[b]
         lanes = count * S
-        dist.all_to_all_single(_bytes(recv[off:off + lanes]), _bytes(grad[off:off + lanes]), group=group)
+        works.append(dist.all_to_all_single(_bytes(recv[off:off + lanes]), _bytes(grad[off:off + lanes]),
+                                            group=group, async_op=async_op))
+    return works
 
 
-def gather_params(shards: torch.Tensor, full: torch.Tensor, buckets, count: int, group=None):
-    """The all-gather: for every bucket, full[off : off + count*S] = the `count` owners' bf16
-    slices of it in owner order, from each owner's shards[base : base + S] (base = the sum of
-    S over earlier buckets)."""
+def gather_params(shards: torch.Tensor, full: torch.Tensor, buckets, count: int, group=None, which=None,
+                  async_op: bool = False):
+    """The all-gather: for every bucket (or those in `which`), full[off : off + count*S] = the
+    `count` owners' bf16 slices of it in owner order, from each owner's shards[base : base + S]
+    (base = the sum of S over earlier buckets). Returns the work handles when async_op."""
     import torch.distributed as dist
-    base = 0
-    for off, _n, S, _ in buckets:
-        dist.all_gather_into_tensor(_bytes(full[off:off + count * S]), _bytes(shards[base:base + S]), group=group)
-        base += S
+    bases = [0]
+    for b in buckets:
+        bases.append(bases[-1] + b[2])
+    works = []
+    for b in (range(len(buckets)) if which is None else which):
+        off, _n, S, _ = buckets[b]
+        works.append(dist.all_gather_into_tensor(_bytes(full[off:off + count * S]),
+                                                 _bytes(shards[bases[b]:bases[b] + S]), group=group,
+                                                 async_op=async_op))
+    return works
 
 
 def gather_bucket_params(shards: torch.Tensor, dst: torch.Tensor, buckets, bucket: int, count: int, group=None):
@@ -241,6 +254,62 @@ class ShardedZeroOptimizer:
                          [self.param_shards], [dst[:self.K * S]])
         return dst[:n]
 
+    # -- ZeRO-2 bucket streaming ------------------------------------------------------------
+    def exchange_bucket(self, bucket: int, grad: torch.Tensor, async_op: bool = False):
+        """Bucket `bucket`'s exchange (as soon as its gradients exist). With the direct
+        transport and async_op, returns the collective's work handle: wait() on it makes the
+        current stream wait for the exchange."""
+        if async_op and not self._stage_io.host:
+            return exchange_gradients(grad, self.recv, self.buckets, self.K, self.intra, [bucket], True)[0]
+        off, _n, S, _ = self.buckets[bucket]
+        lanes = self.K * S
+        self._collective(f"exchange{bucket}",
+                         lambda g, r: exchange_gradients(g, r, [(0, 0, S, 0)], self.K, self.intra),
+                         [grad[off:off + lanes]], [self.recv[off:off + lanes]])
+        return None
+
+    def step_bucket(self, bucket: int, hyper: Hyper):
+        """Bucket `bucket`'s update from its exchanged slices (no clipping): zero_rank_step_bucket.
+        The step completes once every bucket has been stepped."""
+        _check(_lib().zero_rank_step_bucket(self._ctx, bucket, self.recv.data_ptr(), self.stage, ctypes.byref(hyper),
+                                            _stream_handle(None)), "zero_rank_step_bucket")
+
+    def gather_bucket_into_full(self, bucket: int, async_op: bool = False):
+        """Bucket `bucket`'s all-gather into the full parameter buffer."""
+        if async_op and not self._stage_io.host:
+            return gather_params(self.param_shards, self.param_full, self.buckets, self.K, self.intra, [bucket],
+                                 True)[0]
+        off, _n, S, _ = self.buckets[bucket]
+        base = sum(b[2] for b in self.buckets[:bucket])
+        self._collective(f"gather{bucket}",
+                         lambda sh, f: gather_params(sh, f, [(0, 0, S, 0)], self.K, self.intra),
+                         [self.param_shards[base:base + S]], [self.param_full[off:off + self.K * S]])
+        return None
+
+    def step_streamed(self, grad: torch.Tensor, hyper: Hyper, order=None, gather: bool = True):
+        """One step without clipping, bucket by bucket (ZeRO-2 streaming, "CS336 2026 Lecture 8"
+        Slide 23; "并行训练优化、MoE扩展与系统瓶颈" 2.2.4): every bucket's exchange is issued at once
+        (asynchronous over NCCL), each bucket is updated as soon as its own exchange has
+        landed while later ones are still in flight, and its all-gather follows its update.
+        order: the buckets' order (default: layout order; backward passes produce them in
+        reverse). Results equal step()'s bit for bit."""
+        if hyper.clip:
+            raise ValueError("step_streamed does not clip: the norm needs every bucket first (use step)")
+        if self.groups > 1:
+            raise ValueError("step_streamed is the flat mode's form")
+        order = list(range(len(self.buckets))) if order is None else list(order)
+        works = [self.exchange_bucket(b, grad, async_op=True) for b in order]
+        gathers = []
+        for b, wk in zip(order, works):
+            if wk is not None:
+                wk.wait()
+            self.step_bucket(b, hyper)
+            if gather and self.param_full is not None:
+                gathers.append(self.gather_bucket_into_full(b, async_op=True))
+        for wk in gathers:
+            if wk is not None:
+                wk.wait()
+
     def _gather_sums(self):
         import torch.distributed as dist
         self._collective("sums", lambda x, o: dist.all_gather_into_tensor(o, x, group=self.intra), [self.sumsq],
@@ -340,6 +409,12 @@ class ShardedZeroOptimizer:
         t = ctypes.c_int64()
         _check(_lib().zero_get_step(self._ctx, ctypes.byref(t)), "zero_get_step")
         return t.value
+
+    def set_launch_overlap(self, mode: str):
+        """"none" (default) or "launch" / "buckets": the per-bucket launches of one unclipped
+        step overlap each other (programmatic dependent launch; zero_set_launch_overlap)."""
+        from . import OVERLAP
+        _check(_lib().zero_set_launch_overlap(self._ctx, OVERLAP[mode]), "zero_set_launch_overlap")
 
     def set_timing(self, on: bool):
         _check(_lib().zero_set_timing(self._ctx, 1 if on else 0), "zero_set_timing")
