@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
                     help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
                          "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+    ap.add_argument("--emulate-ranks", action="store_true",
+                    help="with --shard on one GPU: the workload's M ranks as M rank contexts in this one process, "
+                         "each holding only its shard, with device copies in place of the collectives (timed "
+                         "apart); all ranks' kernels run one after another and move the emulated step's bytes")
     ap.add_argument("--shard", action="store_true",
                     help="process-per-rank mode: the job's M ranks are the N processes (one per GPU, NCCL), "
                          "each holding only its shard; the workload's tensors, stage, clipping and buckets "
@@ -69,11 +73,9 @@ def parse():
     ap.add_argument("--groups", type=int, default=1,
                     help="hybrid sharding: split the workload's M ranks into this many groups (state "
                          "sharded over M / groups ranks, replicated across groups)")
-    ap.add_argument("--overlap", default=None, choices=["none", "launch", "buckets"],
-                    help="--mode stream and gather (default buckets), and --shard (default none): programmatic "
-                         "launch overlap of the per-bucket kernels (zero_set_launch_overlap); the roofline then "
-                         "covers the whole step or sweep. Measured best per mode: overlapped launches for the "
-                         "emulated streams and gathers, ordinary ones beside NCCL's kernels in --shard")
+    ap.add_argument("--overlap", default="buckets", choices=["none", "launch", "buckets"],
+                    help="--mode stream and gather: programmatic launch overlap of the per-bucket "
+                         "kernels (zero_set_launch_overlap); the roofline then covers the whole step or sweep")
     ap.add_argument("--prefetch-buffers", type=int, default=4,
                     help="--mode gather: transient buffers of the prefetch (buckets gathered ahead + 1)")
     ap.add_argument("--bucket-mib", type=float, default=25.0,
@@ -937,22 +939,19 @@ def run_shard(args):
     if ghat_mode == "auto":
         ghat_mode = ("materialize" if (w.M > 4 and opt.ghat is not None) else "recompute") if clip else "none"
     stream = torch.cuda.current_stream()
-    opt.set_launch_overlap(args.overlap)
     for _ in range(args.warmup):
         opt.step(grad, h)
     torch.cuda.synchronize()
     if opt.sync_status() != 0:
         raise SystemExit("warm-up step saw a non-finite gradient norm")
-    # the step itself, with no per-launch events (they would split overlapped launches)
+    # the step itself, with no per-launch events
     ms_total, clk, step_ms = _timed_region(lambda: opt.step(grad, h), args.steps, stream, dist, device)
-    # then the kernels one by one: ordinary launches, each bracketed by events
-    opt.set_launch_overlap("none")
+    # then the same steps with every kernel launch bracketed by events
     opt.set_timing(True)
     opt.kernel_times()
     _timed_region(lambda: opt.step(grad, h), args.steps, stream, dist, device)
     kt = opt.kernel_times()
     opt.set_timing(False)
-    opt.set_launch_overlap(args.overlap)
     n, L = w.N, opt.sizes["shard_len"]
     ms_per_step = ms_total / args.steps
     peak, peak_kind = hbm_peak()
@@ -1000,8 +999,7 @@ def run_shard(args):
                                       f"bf16 all-gather)"},
             "kernel_ms_per_step": round(kernel_ms, 4),
             "collective_ms_per_step": round(ms_per_step - kernel_ms, 4),
-            "kernel_timing": "a second pass of the same steps with ordinary launches, each bracketed by events",
-            "launch_overlap": args.overlap,
+            "kernel_timing": "a second pass of the same steps, each kernel launch bracketed by events",
             "frac_of_peak_alg_kernels": round(alg_bytes_per_param(w.M) * L / (kernel_ms / 1e3) / 1e9 / peak, 4),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
@@ -1017,12 +1015,176 @@ def run_shard(args):
     tdist.destroy_process_group()
 
 
+def run_shard_emulated(args):
+    """The process-per-rank step of the workload's M ranks on one GPU, measured: M rank contexts
+    (zero_config.sharded) in this process, each with only its shard of the state, its own
+    exchange buffer and full-parameter buffer. The collectives are device copies in the
+    exchange layout (all-to-all of every bucket's slices, the sums in rank order, the all-gather
+    of bf16 shards), timed apart from the kernels. One step runs every rank's library calls one
+    after another: the kernels' time per step is the sum over ranks, and their bytes are the
+    emulated step's, (2M+26) per lane plus the clipped forms' extra pass."""
+    import ctypes
+
+    import torch
+
+    import workloads as W
+    import zero_gradient_reduce_scatter_gb300 as zg
+    from zero_gradient_reduce_scatter_gb300 import _build
+
+    world, rank, local = dist_env()
+    if world != 1:
+        raise SystemExit("--emulate-ranks runs on one GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if not os.path.exists(_build.LIB_PATH):
+        _build.build()
+    w = workload(args)
+    M, lib, sh = w.M, zg._lib(), zg._stream_handle(None)
+    _, buckets = zg.layout(w.numel, M, w.stage, w.bucket_bytes)
+    sz = zg.plan(w.numel, M, w.stage, w.bucket_bytes, rank=0)
+    L, npad = sz["shard_len"], sz["npad"]
+    clip = w.clip is not None
+    h = zg.Hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip=clip,
+                 max_grad_norm=w.clip or 1.0, ghat_mode=args.ghat_mode)
+    ghat = M > 4
+    mi = W.master_init(w, device)
+    ranks = []
+    for r in range(M):
+        b = {k: torch.empty(L, dtype=torch.float32, device=device) for k in ("master", "m", "v")}
+        b["ghat"] = torch.empty(L, dtype=torch.float32, device=device) if ghat else None
+        b["shards"] = torch.empty(L, dtype=torch.bfloat16, device=device)
+        b["full"] = torch.empty(npad, dtype=torch.bfloat16, device=device)
+        b["scratch"] = torch.empty(sz["bytes_scratch"], dtype=torch.uint8, device=device)
+        b["recv"] = torch.empty(npad, dtype=torch.bfloat16, device=device)
+        b["sumsq"] = torch.zeros(1, dtype=torch.float64, device=device)
+        b["sums"] = torch.zeros(M, dtype=torch.float64, device=device)
+        bufs = zg.Buffers(b["master"].data_ptr(), b["m"].data_ptr(), b["v"].data_ptr(),
+                          b["ghat"].data_ptr() if ghat else None, b["full"].data_ptr(), b["shards"].data_ptr(),
+                          b["scratch"].data_ptr())
+        ctx = ctypes.c_void_p()
+        cfg = zg.Config(M, w.stage, w.bucket_bytes, 0, 0, 1, r)
+        zg._check(lib.zero_init(ctypes.byref(ctx), ctypes.byref(cfg), ctypes.cast(zg._i64_array(w.numel), ctypes.c_void_p),
+                                len(w.numel), ctypes.byref(bufs), mi.data_ptr(), sh), "zero_init")
+        b["ctx"] = ctx
+        ranks.append(b)
+    del mi
+    toff, _ = zg.layout(w.numel, M, w.stage, w.bucket_bytes)
+    grads = [torch.zeros(npad, dtype=torch.bfloat16, device=device) for _ in range(M)]
+    sig = W.sigmas(w)
+    for r in range(M):
+        W.fill_grads(w, r, 0, grads[r], toff, sig)
+    bases = [0]
+    for bk in buckets:
+        bases.append(bases[-1] + bk[2])
+
+    def exchange():
+        for r, b in enumerate(ranks):
+            for off, _n, S, _ in buckets:
+                for q in range(M):
+                    b["recv"][off + q * S: off + (q + 1) * S].copy_(grads[q][off + r * S: off + (r + 1) * S])
+
+    def gather():
+        for b in ranks:
+            for i, (off, _n, S, _) in enumerate(buckets):
+                for q in range(M):
+                    b["full"][off + q * S: off + (q + 1) * S].copy_(ranks[q]["shards"][bases[i]:bases[i] + S])
+
+    def kernels():
+        if clip:
+            for b in ranks:
+                zg._check(lib.zero_rank_sumsq(b["ctx"], b["recv"].data_ptr(), ctypes.byref(h), b["sumsq"].data_ptr(), sh),
+                          "zero_rank_sumsq")
+            allsums = torch.cat([b["sumsq"] for b in ranks])
+            for b in ranks:
+                b["sums"].copy_(allsums)
+        for b in ranks:
+            zg._check(lib.zero_rank_step(b["ctx"], b["recv"].data_ptr(), b["sums"].data_ptr() if clip else None,
+                                         w.stage, ctypes.byref(h), sh), "zero_rank_step")
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        exchange()
+        kernels()
+        gather()
+    torch.cuda.synchronize()
+    for b in ranks:
+        if lib.zero_sync_status(b["ctx"]) != 0:
+            raise SystemExit("warm-up step saw a non-finite gradient norm")
+    # every step: the exchange copies, the ranks' kernels (events around them), the all-gather
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        exchange()
+        ev[i][0].record(stream)
+        kernels()
+        ev[i][1].record(stream)
+        gather()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    kms = [a.elapsed_time(b) for a, b in ev]
+    k_ms = sum(kms) / args.steps
+    total_ms = t0.elapsed_time(t1) / args.steps
+    # per-kernel times in a second pass (each launch bracketed by events)
+    for b in ranks:
+        lib.zero_set_timing(b["ctx"], 1)
+        lib.zero_kernel_times(b["ctx"], None, None)
+    for _ in range(args.steps):
+        kernels()
+    torch.cuda.synchronize()
+    tot = {}
+    for b in ranks:
+        ms = (ctypes.c_double * len(zg.KERNELS))()
+        cnt = (ctypes.c_int64 * len(zg.KERNELS))()
+        lib.zero_kernel_times(b["ctx"], ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p))
+        for i, k in enumerate(zg.KERNELS):
+            t = tot.setdefault(k, [0.0, 0])
+            t[0] += ms[i]
+            t[1] += cnt[i]
+        lib.zero_set_timing(b["ctx"], 0)
+    ghat_mode = args.ghat_mode
+    if ghat_mode == "auto":
+        ghat_mode = ("materialize" if ghat else "recompute") if clip else "none"
+    dom = max((k for k in tot if tot[k][1] > 0), key=lambda k: tot[k][0])
+    dom_bytes = kernel_alg_bytes_per_lane(dom, M, ghat_mode == "materialize") * L  # per rank launch
+    dom_ms = tot[dom][0] / tot[dom][1]
+    peak, peak_kind = hbm_peak()
+    n = w.N
+    line = {
+        "metric": METRIC, "value": n / (k_ms / 1e3), "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": k_ms, "ms_per_step_median": round(statistics.median(kms), 4),
+        "ms_per_step_min": round(min(kms), 4), "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + f"; process-per-rank kernels of all {M} ranks, one process",
+                   "params": n, "M": M, "stage": w.stage, "clip": w.clip, "bucket_bytes": w.bucket_bytes,
+                   "ghat_mode": ghat_mode, "shard_lanes": L, "padded_lanes": npad,
+                   "l2": l2_note(2 * npad * M),
+                   "parallelism": f"zero-dp{M} emulated: {M} rank contexts on one GPU, collectives as device copies"},
+        "value_counts": "the ranks' kernels only (the step's library calls, all ranks one after another)",
+        "ms_per_step_with_copies": round(total_ms, 4),
+        "frac_of_peak_alg": round(alg_bytes_per_param(M) * n / (k_ms / 1e3) / 1e9 / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": dom + " (exchange-layout sources)", "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4),
+                     "traffic": None, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
+                     "kernel_share": {k: round(v[0] / max(sum(x[0] for x in tot.values()), 1e-9), 4)
+                                      for k, v in tot.items() if v[1]}},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": int(sum(v[1] for v in tot.values())), "clocks": clk,
+    }
+    for b in ranks:
+        lib.zero_destroy(b["ctx"])
+    print_line(line)
+
+
 def main():
     args = parse()
-    if args.overlap is None:
-        args.overlap = "none" if args.shard else "buckets"
     if args.impl == "reference":
         run_reference(args)
+    elif args.shard and args.emulate_ranks:
+        run_shard_emulated(args)
     elif args.shard:
         run_shard(args)
     elif args.mode == "stream":

@@ -317,7 +317,8 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * ranks, or across one group, gives the whole state); zero_load_state reads the whole
  * unpadded vectors. */
 
-/* Without clipping, the whole update of this rank's shard in one fused pass per bucket:
+/* Without clipping, the whole update of this rank's shard in one fused pass (one launch over
+ * every bucket of the shard):
  * reduce-scatter from the exchanged slices (rank-ordered fp32 sum x (float)(1/M)), AdamW,
  * the bf16 shard into param_shards. With clipping: zero_rank_sumsq first, then the gathered
  * sums, then this call. Increments t.
@@ -516,9 +517,6 @@ int zero_set_max_ctas(zero_ctx* ctx, int ctas);
  *                        the parameter shards) nor access what it writes. Work ordered by an
  *                        event wait (cudaStreamWaitEvent) is not affected: that dependency is
  *                        kept whole.
- * In process-per-rank mode, either overlap mode also lets the per-bucket launches of one
- * unclipped zero_rank_step overlap each other (safe by construction: the call's first
- * launch waits for everything before it). zero_rank_step_bucket launches ordinary kernels.
  * zero_step_bucket_scheduled always launches ordinary kernels. Under either overlap mode each
  * bucket reduction keeps its norm partials in a region of the scratch buffer of its own
  * (zero_plan sizes the scratch for it). With overlap, per-kernel event timing

@@ -285,7 +285,10 @@ int check_hyper(const zero_hyper* h) {
 int grid_for(zero_ctx* c, int variant, int64_t work_items) {
     if (c->grid[variant] == 0) {
         int per_sm = 0;
-        if (zg::variant_blocks_per_sm(variant, c->cfg.M, c->cfg.groups > 1 ? c->cfg.groups : 1, &per_sm) !=
+        // the exchange-layout kernels of a hybrid context read the K slices of its group
+        const bool group_sources = c->cfg.groups > 1 && variant >= zg::kVarRsNormWriteX && variant <= zg::kVarRsAdamwPlainX;
+        const int m = group_sources ? shard_count(&c->cfg) : c->cfg.M;
+        if (zg::variant_blocks_per_sm(variant, m, c->cfg.groups > 1 ? c->cfg.groups : 1, &per_sm) !=
                 cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
@@ -1050,30 +1053,31 @@ static zg::StepArgs rank_args(zero_ctx* c) {
     return a;
 }
 
-// Bucket b's sources in the exchange layout: the slice that source q (of `count`) sent for
-// this shard starts at lane off_b + q * S_b of recv. rebase: shift each pointer back by the
-// slice's local start base_b, for the fused kernel, which addresses its sources by local
-// lane (address arithmetic only; it reads lanes [base_b, base_b + S_b) alone); otherwise
-// each pointer is the slice start and the norm pass subtracts gbase = base_b.
-static void slice_sources(const zero_ctx* c, zg::StepArgs& a, const void* recv, int64_t b, int count, bool rebase) {
+// One bucket's sources for the fused kernel (zero_rank_step_bucket): the slice that source q
+// (of `count`) sent for this shard starts at lane off_b + q * S_b of recv; each pointer is
+// shifted back by the slice's local start base_b, since the fused kernel addresses its
+// sources by local lane (address arithmetic only: it reads lanes [base_b, base_b + S_b)).
+static void slice_sources(const zero_ctx* c, zg::StepArgs& a, const void* recv, int64_t b, int count) {
     const zg::Bucket& G = c->buckets[(size_t)b];
     const zg::Bucket& L = c->local[(size_t)b];
     const int64_t S = L.end - L.off;
-    for (int q = 0; q < count; ++q) {
-        const uintptr_t start = (uintptr_t)recv + 2 * (uintptr_t)(G.off + (int64_t)q * S);
-        a.grads[q] = (const uint16_t*)(rebase ? start - 2 * (uintptr_t)L.off : start);
-    }
+    for (int q = 0; q < count; ++q)
+        a.grads[q] = (const uint16_t*)((uintptr_t)recv + 2 * (uintptr_t)(G.off + (int64_t)q * S) - 2 * (uintptr_t)L.off);
     a.M = count;
     a.vbeg = L.off / 8;
     a.vend = L.end / 8;
     a.b_first = b;
     a.b_end = b + 1;
-    if (rebase) {
-        a.gext = L.end;
-    } else {
-        a.gbase = L.off;
-        a.gext = S;
-    }
+    a.gext = L.end;
+}
+
+// The exchange buffer as the sources of one launch over the whole shard: `count` sources,
+// bucket b's slice of source q at lanes [count * base_b + q * S_b, +S_b) (the kernels find it
+// from the rank's own table).
+static void exchange_sources(const zero_ctx* c, zg::StepArgs& a, const void* recv, int count) {
+    a.grads[0] = (const uint16_t*)recv;
+    a.M = count;
+    a.gext = c->npad;  // lanes of the exchange buffer
 }
 
 // Hybrid mode: the G gathered fp32 group partials of this shard, group grp at [grp * shard_len].
@@ -1097,18 +1101,17 @@ int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
-    const int K = shard_count(&c->cfg);
-    cudaError_t e = cudaSuccess;
-    for (int64_t b = 0; b < (int64_t)c->buckets.size() && e == cudaSuccess; ++b) {
-        // the group's K slices summed in order from +0, unscaled (x 1 is exact), into `part`;
-        // the pass's partial sums of squares are not used
-        zg::StepArgs a = rank_args(c);
-        slice_sources(c, a, recv, b, K, false);
-        a.inv_M = 1.0f;
-        a.ghat = (float*)part;
-        const int g1 = grid_for(c, zg::kVarRsNormWrite, a.vend - a.vbeg);
+    // the group's K slices summed in order from +0, unscaled (x 1 is exact), into `part`; the
+    // pass's partial sums of squares are not used
+    zg::StepArgs a = rank_args(c);
+    exchange_sources(c, a, recv, shard_count(&c->cfg));
+    a.inv_M = 1.0f;
+    a.ghat = (float*)part;
+    const int g1 = grid_for(c, zg::kVarRsNormWriteX, a.nvec);
+    cudaError_t e;
+    {
         Timed tm(c, ZERO_K_RS_NORM, s);
-        e = zg::launch_rs_norm(a, true, g1, s);
+        e = zg::launch_rs_norm_exchange(a, true, g1, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     c->last_stream = s;
@@ -1128,39 +1131,22 @@ int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* s
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     const bool write = mode == ZERO_GHAT_MATERIALIZE;
-    const int variant = write ? zg::kVarRsNormWrite : zg::kVarRsNormOnly;
-    const int64_t nb = (int64_t)c->buckets.size();
-    cudaError_t e = cudaSuccess;
-    if (hybrid(c)) {  // one pass over the whole shard from the gathered group partials
-        zg::StepArgs a = rank_args(c);
-        part_sources(c, a, src);
-        const int g1 = grid_for(c, variant, a.nvec);
-        {
-            Timed tm(c, ZERO_K_RS_NORM, s);
-            e = zg::launch_rs_norm_f32src(a, write, g1, s);
-        }
-        if (e == cudaSuccess) {
-            Timed tm(c, ZERO_K_NORM_FINAL, s);
-            e = zg::launch_sum_partials(c->partials, g1, sumsq, s);
-        }
-    } else {  // per bucket (the slices of a bucket are contiguous in the exchange buffer)
-        for (int64_t b = 0; b < nb && e == cudaSuccess; ++b) {
-            zg::StepArgs a = rank_args(c);
-            slice_sources(c, a, src, b, c->cfg.M, false);
-            const int g1 = grid_for(c, variant, a.vend - a.vbeg);
-            {
-                Timed tm(c, ZERO_K_RS_NORM, s);
-                e = zg::launch_rs_norm(a, write, g1, s);
-            }
-            if (e == cudaSuccess) {  // one bucket: straight to the output
-                Timed tm(c, ZERO_K_NORM_FINAL, s);
-                e = zg::launch_sum_partials(c->partials, g1, nb == 1 ? sumsq : c->bucket_sums + b, s);
-            }
-        }
-        if (e == cudaSuccess && nb > 1) {
-            Timed tm(c, ZERO_K_NORM_FINAL, s);
-            e = zg::launch_sum_partials(c->bucket_sums, (int)nb, sumsq, s);
-        }
+    // one pass over the whole shard: from the gathered group partials (hybrid) or from the
+    // exchange buffer (flat)
+    zg::StepArgs a = rank_args(c);
+    if (hybrid(c)) part_sources(c, a, src);
+    else exchange_sources(c, a, src, c->cfg.M);
+    const int g1 = grid_for(c, hybrid(c) ? (write ? zg::kVarRsNormWriteF : zg::kVarRsNormOnlyF)
+                                         : (write ? zg::kVarRsNormWriteX : zg::kVarRsNormOnlyX),
+                            a.nvec);
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_RS_NORM, s);
+        e = hybrid(c) ? zg::launch_rs_norm_f32src(a, write, g1, s) : zg::launch_rs_norm_exchange(a, write, g1, s);
+    }
+    if (e == cudaSuccess) {
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        e = zg::launch_sum_partials(c->partials, g1, sumsq, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     c->rank_reduced = true;
@@ -1200,30 +1186,17 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
         const int g3 = grid_for(c, zg::kVarAdamw, a.nvec);
         Timed tm(c, ZERO_K_ADAMW, s);
         e = zg::launch_adamw(a, false, g3, s);
-    } else if (e == cudaSuccess && hybrid(c)) {
+    } else if (e == cudaSuccess) {  // the fused pass, one launch over the whole shard
         zg::StepArgs a = rank_args(c);
-        part_sources(c, a, src);
+        if (hybrid(c)) part_sources(c, a, src);
+        else exchange_sources(c, a, src, c->cfg.M);
         a.k = k;
-        const int g4 = grid_for(c, clip ? zg::kVarRsAdamwScaled : zg::kVarRsAdamwPlain, a.nvec);
+        const int g4 = grid_for(c, hybrid(c) ? (clip ? zg::kVarRsAdamwScaledF : zg::kVarRsAdamwPlainF)
+                                             : (clip ? zg::kVarRsAdamwScaledX : zg::kVarRsAdamwPlainX),
+                                a.nvec);
         Timed tm(c, ZERO_K_RS_ADAMW, s);
-        e = zg::launch_rs_adamw_f32src(a, clip != 0, g4, s);
-    } else if (e == cudaSuccess) {
-        // one fused launch per bucket. Without clipping, under launch overlap (any mode but
-        // ZERO_OVERLAP_NONE) the buckets' launches overlap: they touch disjoint lanes and read
-        // only sources complete before the call's first launch (which waits for everything
-        // before it), and each still completes after the one before it, so stream order
-        // holds for later work
-        const int64_t nb = (int64_t)c->buckets.size();
-        const bool overlap = !clip && nb > 1 && c->overlap != ZERO_OVERLAP_NONE;
-        for (int64_t b = 0; b < nb && e == cudaSuccess; ++b) {
-            zg::StepArgs a = rank_args(c);
-            slice_sources(c, a, src, b, c->cfg.M, true);
-            a.k = k;
-            if (overlap) a.pdl = b == 0 ? zg::kPdlWaitFirst : zg::kPdlWaitLast;
-            const int g4 = grid_for(c, clip ? zg::kVarRsAdamwScaled : zg::kVarRsAdamwPlain, a.vend - a.vbeg);
-            Timed tm(c, ZERO_K_RS_ADAMW, s);
-            e = zg::launch_rs_adamw(a, clip != 0, false, g4, s);
-        }
+        e = hybrid(c) ? zg::launch_rs_adamw_f32src(a, clip != 0, g4, s)
+                      : zg::launch_rs_adamw_exchange(a, clip != 0, g4, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     c->rank_reduced = false;
@@ -1247,7 +1220,7 @@ int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stag
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     zg::StepArgs a = rank_args(c);
-    slice_sources(c, a, src, bucket, c->cfg.M, true);
+    slice_sources(c, a, src, bucket, c->cfg.M);
     a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
     const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
     cudaError_t e;

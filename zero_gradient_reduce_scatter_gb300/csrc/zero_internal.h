@@ -172,6 +172,16 @@ enum KernelVariant : int {
     kVarRsAdamwPlain,     // fused, no clipping
     kVarGather,
     kVarInit,
+    // process-per-rank mode: sources in the exchange layout (X) or fp32 group partials (F);
+    // their register use differs from the plain kernels', so their grids are their own
+    kVarRsNormWriteX,
+    kVarRsNormOnlyX,
+    kVarRsAdamwScaledX,
+    kVarRsAdamwPlainX,
+    kVarRsNormWriteF,
+    kVarRsNormOnlyF,
+    kVarRsAdamwScaledF,
+    kVarRsAdamwPlainF,
     kNumVariants
 };
 
@@ -202,6 +212,11 @@ cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s
 // the bf16 variants of the generic rank count.
 cudaError_t launch_rs_norm_f32src(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
 cudaError_t launch_rs_adamw_f32src(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
+// The same over sources in the exchange layout of the process-per-rank mode: a.grads[0] is
+// the exchange buffer (gext lanes), a.M sources, a.buckets the rank's own table; one launch
+// covers every bucket of the shard.
+cudaError_t launch_rs_norm_exchange(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s);
+cudaError_t launch_rs_adamw_exchange(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s);
 // a.pdl != kPdlNone (plain, unscheduled form only): launched with programmatic stream
 // serialization in that mode.
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int grid, cudaStream_t s);

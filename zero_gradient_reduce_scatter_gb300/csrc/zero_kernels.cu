@@ -274,15 +274,59 @@ __device__ __forceinline__ void rank_sum_f32(const StepArgs& a, int64_t g, float
     }
 }
 
+// Exchange-layout sources (process-per-rank mode): a.grads[0] is the exchange buffer, in
+// which source q's slice of local bucket e sits at lanes [M*e.off + q*S, +S), S = e.end - e.off
+// (the bucket's global start is M times its local start). So local lane g of bucket e reads
+// source q at g + (M-1)*e.off + q*S, and one launch covers every bucket of the shard.
+template <int MT, int PATH>
+__device__ __forceinline__ void rank_sum_exchange(const StepArgs& a, const Bucket& e, int64_t g, float acc[8]) {
+    const int M = MT > 0 ? MT : a.M;
+    const int64_t S = e.end - e.off;
+    const uint16_t* p = a.grads[0] + g + (int64_t)(M - 1) * e.off;
+    if constexpr (MT > 0) {
+        uint4 q[MT];
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_grad<PATH>(p + r * S);
+#pragma unroll
+        for (int r = 0; r < MT; ++r) add8(acc, q[r]);
+    } else {
+        int r = 0;
+        for (; r + 4 <= M; r += 4) {
+            uint4 q0 = ld_grad<PATH>(p + r * S), q1 = ld_grad<PATH>(p + (r + 1) * S);
+            uint4 q2 = ld_grad<PATH>(p + (r + 2) * S), q3 = ld_grad<PATH>(p + (r + 3) * S);
+            add8(acc, q0);
+            add8(acc, q1);
+            add8(acc, q2);
+            add8(acc, q3);
+        }
+        for (; r < M; ++r) add8(acc, ld_grad<PATH>(p + r * S));
+    }
+}
+
+// Where the sources of a kernel live (a compile-time choice, so the plain kernels are
+// unchanged): M bf16 buffers addressed by lane, M fp32 buffers addressed by lane, or the
+// exchange buffer of the process-per-rank mode.
+enum SrcMode : int { kSrcRanks = 0, kSrcF32 = 1, kSrcExchange = 2 };
+
+// Checked builds: lane g's eight sources lie inside the source buffers (exchange layout: the
+// farthest source lane of bucket e is below M * e.end).
+template <int SRC>
+__device__ __forceinline__ bool src_in_range(const StepArgs& a, const Bucket& e, int64_t g) {
+    if constexpr (SRC == kSrcExchange) return g >= e.off && g + 8 <= e.end && (int64_t)a.M * e.end <= a.gext;
+    else return g >= 0 && g + 8 <= a.gext;
+}
+
 // GROUPED selects the hybrid-sharding order at compile time, so the plain kernels carry no
 // branch that would keep the compiler from issuing the state loads beside the gradient loads.
-// F32SRC: the sources are fp32 (rank_sum_f32), not bf16.
-template <int MT, int PATH, bool GROUPED, bool F32SRC = false>
-__device__ __forceinline__ void rank_sum(const StepArgs& a, int64_t g, float acc[8]) {
+// SRC: the sources (SrcMode); e is the bucket of lane g (used by the exchange layout).
+template <int MT, int PATH, bool GROUPED, int SRC = kSrcRanks>
+__device__ __forceinline__ void rank_sum(const StepArgs& a, const Bucket& e, int64_t g, float acc[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;  // +0: a sum of -0 replicas is +0
-    if constexpr (F32SRC) {
+    if constexpr (SRC == kSrcF32) {
         rank_sum_f32(a, g, acc);
+    } else if constexpr (SRC == kSrcExchange) {
+        rank_sum_exchange<MT, PATH>(a, e, g, acc);
     } else if constexpr (GROUPED && MT > 0) {
         rank_sum_grouped_fixed<MT, PATH>(a, g, acc);
     } else if constexpr (GROUPED) {
@@ -455,7 +499,7 @@ __device__ __forceinline__ double block_sum(double x) {
 // K1: reduce-scatter + per-CTA partial sums of squares (+ write of the fp32 average).
 // ---------------------------------------------------------------------------------------
 template <int MT, bool WRITE, bool GROUPED = false, int THREADS = WRITE ? kThreadsRsNormWrite : kThreadsRsNormOnly,
-          bool PDL = false, bool F32SRC = false>
+          bool PDL = false, int SRC = kSrcRanks>
 __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
     const PdlScope<PDL> pdl(a.pdl);
     SumSq acc;
@@ -468,8 +512,8 @@ __global__ void __launch_bounds__(THREADS) k_rs_norm(const StepArgs a) {
             const int64_t o = vi * 8;
             c.seek(o);
             float sum[8], gh[8];
-            if (!ZG_OK(a.status, o - a.gbase >= 0 && o - a.gbase + 8 <= a.gext, kSiteGradNorm, o)) continue;
-            rank_sum<MT, kGradLoadRsNorm, GROUPED, F32SRC>(a, o - a.gbase, sum);
+            if (!ZG_OK(a.status, src_in_range<SRC>(a, c.e, o - a.gbase), kSiteGradNorm, o)) continue;
+            rank_sum<MT, kGradLoadRsNorm, GROUPED, SRC>(a, c.e, o - a.gbase, sum);
             average8(sum, a.inv_M, c.nreal(o), gh);
             if (WRITE && ZG_OK(a.status, o + 8 <= a.npad, kSiteGhatWrite, o)) {
                 st_f4<kGhatStoreRsNorm>(a.ghat + o, make_float4(gh[0], gh[1], gh[2], gh[3]));
@@ -586,7 +630,7 @@ __global__ void __launch_bounds__(kThreadsAdamw) k_adamw(const StepArgs a) {
 // leaves registers. SCALE applies the clip scale computed by K2 (recompute form). Runs over
 // vecs [vbeg, vend): the whole layout, or one bucket (ZeRO-2 per-bucket steps).
 // ---------------------------------------------------------------------------------------
-template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false, bool PDL = false, bool F32SRC = false>
+template <int MT, bool SCALE, bool GROUPED = false, bool SCHED = false, bool PDL = false, int SRC = kSrcRanks>
 __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) {
     const PdlScope<PDL> pdl(a.pdl);
     float s = 1.0f;
@@ -609,10 +653,10 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
-        if (!ZG_OK(a.status, o + 8 <= a.npad && o + 8 <= a.gext, kSiteStepLanes, o)) continue;
+        if (!ZG_OK(a.status, o + 8 <= a.npad && src_in_range<SRC>(a, c.e, o), kSiteStepLanes, o)) continue;
         // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
         load_state<kStateLoadRsAdamw>(a, o, p, m, v);
-        rank_sum<MT, kGradLoadRsAdamw, GROUPED, F32SRC>(a, o, sum);  // grads[r] is addressed by absolute lane
+        rank_sum<MT, kGradLoadRsAdamw, GROUPED, SRC>(a, c.e, o, sum);  // grads[r] is addressed by absolute lane
         const int nr = c.nreal(o);
         average8(sum, a.inv_M, nr, gh);
         adam_vec<SCALE>(gh, s, p, m, v, k);
@@ -856,6 +900,20 @@ template <int MT> struct RsAdamwPlainSched {
     }
 };
 
+// Process-per-rank mode, sources in the exchange layout (flat mode; no grouped variants).
+template <int MT> struct RsNormWriteX {
+    static auto fn() { return &k_rs_norm<MT < 0 ? 0 : MT, true, false, kThreadsRsNormWrite, false, kSrcExchange>; }
+};
+template <int MT> struct RsNormOnlyX {
+    static auto fn() { return &k_rs_norm<MT < 0 ? 0 : MT, false, false, kThreadsRsNormOnly, false, kSrcExchange>; }
+};
+template <int MT> struct RsAdamwScaledX {
+    static auto fn() { return &k_rs_adamw<MT < 0 ? 0 : MT, true, false, false, false, kSrcExchange>; }
+};
+template <int MT> struct RsAdamwPlainX {
+    static auto fn() { return &k_rs_adamw<MT < 0 ? 0 : MT, false, false, false, false, kSrcExchange>; }
+};
+
 const void* variant_fn(int variant, int M, int groups) {
     switch (variant) {
         case kVarRsNormWrite: return (const void*)ByM<RsNormWrite>::get(M, groups);
@@ -865,6 +923,14 @@ const void* variant_fn(int variant, int M, int groups) {
         case kVarRsAdamwPlain: return (const void*)ByM<RsAdamwPlain>::get(M, groups);
         case kVarGather: return (const void*)&k_gather<false>;
         case kVarInit: return (const void*)&k_init;
+        case kVarRsNormWriteX: return (const void*)ByM<RsNormWriteX>::get(M);
+        case kVarRsNormOnlyX: return (const void*)ByM<RsNormOnlyX>::get(M);
+        case kVarRsAdamwScaledX: return (const void*)ByM<RsAdamwScaledX>::get(M);
+        case kVarRsAdamwPlainX: return (const void*)ByM<RsAdamwPlainX>::get(M);
+        case kVarRsNormWriteF: return (const void*)&k_rs_norm<0, true, false, kThreadsRsNormWrite, false, kSrcF32>;
+        case kVarRsNormOnlyF: return (const void*)&k_rs_norm<0, false, false, kThreadsRsNormOnly, false, kSrcF32>;
+        case kVarRsAdamwScaledF: return (const void*)&k_rs_adamw<0, true, false, false, false, kSrcF32>;
+        case kVarRsAdamwPlainF: return (const void*)&k_rs_adamw<0, false, false, false, false, kSrcF32>;
         default: return nullptr;
     }
 }
@@ -889,11 +955,19 @@ cudaError_t launch_pdl(void (*fn)(P...), int grid, int threads, cudaStream_t s, 
 
 int variant_threads(int variant) {
     switch (variant) {
-        case kVarRsNormWrite: return kThreadsRsNormWrite;
-        case kVarRsNormOnly: return kThreadsRsNormOnly;
+        case kVarRsNormWrite:
+        case kVarRsNormWriteX:
+        case kVarRsNormWriteF: return kThreadsRsNormWrite;
+        case kVarRsNormOnly:
+        case kVarRsNormOnlyX:
+        case kVarRsNormOnlyF: return kThreadsRsNormOnly;
         case kVarAdamw: return kThreadsAdamw;
         case kVarRsAdamwScaled:
-        case kVarRsAdamwPlain: return kThreadsRsAdamw;
+        case kVarRsAdamwPlain:
+        case kVarRsAdamwScaledX:
+        case kVarRsAdamwPlainX:
+        case kVarRsAdamwScaledF:
+        case kVarRsAdamwPlainF: return kThreadsRsAdamw;
         case kVarGather: return kThreadsGather;
         case kVarInit: return kThreadsInit;
         default: return kThreads;
@@ -902,11 +976,19 @@ int variant_threads(int variant) {
 
 int variant_ctas_per_sm_cap(int variant) {
     switch (variant) {
-        case kVarRsNormWrite: return kCtasPerSmRsNormWrite;
-        case kVarRsNormOnly: return kCtasPerSmRsNormOnly;
+        case kVarRsNormWrite:
+        case kVarRsNormWriteX:
+        case kVarRsNormWriteF: return kCtasPerSmRsNormWrite;
+        case kVarRsNormOnly:
+        case kVarRsNormOnlyX:
+        case kVarRsNormOnlyF: return kCtasPerSmRsNormOnly;
         case kVarAdamw: return kCtasPerSmAdamw;
         case kVarRsAdamwScaled:
-        case kVarRsAdamwPlain: return kCtasPerSmRsAdamw;
+        case kVarRsAdamwPlain:
+        case kVarRsAdamwScaledX:
+        case kVarRsAdamwPlainX:
+        case kVarRsAdamwScaledF:
+        case kVarRsAdamwPlainF: return kCtasPerSmRsAdamw;
         default: return 0;
     }
 }
@@ -929,14 +1011,26 @@ cudaError_t launch_rs_norm(const StepArgs& a, bool write_ghat, int grid, cudaStr
 }
 
 cudaError_t launch_rs_norm_f32src(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
-    if (write_ghat) k_rs_norm<0, true, false, kThreadsRsNormWrite, false, true><<<grid, kThreadsRsNormWrite, 0, s>>>(a);
-    else k_rs_norm<0, false, false, kThreadsRsNormOnly, false, true><<<grid, kThreadsRsNormOnly, 0, s>>>(a);
+    if (write_ghat) k_rs_norm<0, true, false, kThreadsRsNormWrite, false, kSrcF32><<<grid, kThreadsRsNormWrite, 0, s>>>(a);
+    else k_rs_norm<0, false, false, kThreadsRsNormOnly, false, kSrcF32><<<grid, kThreadsRsNormOnly, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rs_adamw_f32src(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
-    if (apply_scale) k_rs_adamw<0, true, false, false, false, true><<<grid, kThreadsRsAdamw, 0, s>>>(a);
-    else k_rs_adamw<0, false, false, false, false, true><<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    if (apply_scale) k_rs_adamw<0, true, false, false, false, kSrcF32><<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    else k_rs_adamw<0, false, false, false, false, kSrcF32><<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_norm_exchange(const StepArgs& a, bool write_ghat, int grid, cudaStream_t s) {
+    if (write_ghat) ByM<RsNormWriteX>::get(a.M)<<<grid, kThreadsRsNormWrite, 0, s>>>(a);
+    else ByM<RsNormOnlyX>::get(a.M)<<<grid, kThreadsRsNormOnly, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_adamw_exchange(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
+    if (apply_scale) ByM<RsAdamwScaledX>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    else ByM<RsAdamwPlainX>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -410,12 +410,6 @@ class ShardedZeroOptimizer:
         _check(_lib().zero_get_step(self._ctx, ctypes.byref(t)), "zero_get_step")
         return t.value
 
-    def set_launch_overlap(self, mode: str):
-        """"none" (default) or "launch" / "buckets": the per-bucket launches of one unclipped
-        step overlap each other (programmatic dependent launch; zero_set_launch_overlap)."""
-        from . import OVERLAP
-        _check(_lib().zero_set_launch_overlap(self._ctx, OVERLAP[mode]), "zero_set_launch_overlap")
-
     def set_timing(self, on: bool):
         _check(_lib().zero_set_timing(self._ctx, 1 if on else 0), "zero_set_timing")
 
