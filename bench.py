@@ -63,6 +63,8 @@ def parse():
                     help="with --shard on one GPU: the workload's M ranks as M rank contexts in this one process, "
                          "each holding only its shard, with device copies in place of the collectives (timed "
                          "apart); all ranks' kernels run one after another and move the emulated step's bytes")
+    ap.add_argument("--ranks", type=int, default=0,
+                    help="with --shard --emulate-ranks: this many ranks instead of the workload's M")
     ap.add_argument("--shard", action="store_true",
                     help="process-per-rank mode: the job's M ranks are the N processes (one per GPU, NCCL), "
                          "each holding only its shard; the workload's tensors, stage, clipping and buckets "
@@ -1039,6 +1041,8 @@ def run_shard_emulated(args):
     if not os.path.exists(_build.LIB_PATH):
         _build.build()
     w = workload(args)
+    if args.ranks:
+        w = W.small_variant(w, w.numel, name=w.name + f" (as {args.ranks} ranks)", M=args.ranks)
     M, lib, sh = w.M, zg._lib(), zg._stream_handle(None)
     _, buckets = zg.layout(w.numel, M, w.stage, w.bucket_bytes)
     sz = zg.plan(w.numel, M, w.stage, w.bucket_bytes, rank=0)
