@@ -143,3 +143,60 @@ def test_two_processes_on_one_gpu(stage, ghat_mode, streamed):
     bad = {r: v for r, v in got.items() if v != "ok"}
     assert not bad, "\n".join(f"rank {r}:\n{v}" for r, v in bad.items())
     assert all(p.exitcode == 0 for p in procs)
+
+
+def _nccl_one_rank(q, coalesce):
+    """A job of one rank over NCCL (the only NCCL job one GPU can hold): the collectives run
+    through NCCL, grouped per step or one call per bucket; three clipped steps and three
+    streamed ones against the oracle's one-rank step."""
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(free_port()))
+        import torch
+        import torch.distributed as dist
+
+        import oracle as O
+        import workloads as W
+        import zero_gradient_reduce_scatter_gb300 as zg
+        from parity_util import assert_state_close, bf16_ulp_diff, f32, u16
+        from rank_util import padded_to_unpadded
+
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+        w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
+        mi = W.master_init(w, dev)
+        opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce)
+        assert opt.M == 1 and len(opt.buckets) >= 2
+        p = O.plan(NUMEL, 1, BUCKET_BYTES)
+        st = O.init_state(p, 2, f32(mi))
+        for k in range(6):
+            clip = k < 3
+            G = _grads_all(p, 1, k)
+            mine = torch.from_numpy(G[0].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+            h = zg.Hyper(clip=clip, max_grad_norm=0.05)
+            if clip:
+                opt.step(mine, h)
+            else:
+                opt.step_streamed(mine, h, order=reversed(range(len(opt.buckets))))
+            full, norm, scale, rc = O.zero_step(p, st, G, O.hyper(clip=clip, max_grad_norm=0.05))
+            assert rc == 0
+            assert_state_close(f32(opt.get_state("master")), st.master[0][:p.shard_len], f"step {k} master")
+            assert_state_close(f32(opt.get_state("v")), st.var[0][:p.shard_len], f"step {k} v")
+            assert bf16_ulp_diff(padded_to_unpadded(p, u16(opt.params())), full) <= 1
+        opt.close()
+        dist.destroy_process_group()
+        q.put("ok")
+    except BaseException:
+        q.put(traceback.format_exc())
+
+
+@pytest.mark.parametrize("coalesce", [True, False])
+def test_nccl_one_rank_job(coalesce):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    proc = ctx.Process(target=_nccl_one_rank, args=(q, coalesce))
+    proc.start()
+    got = q.get(timeout=600)
+    proc.join(timeout=120)
+    assert got == "ok", got
+    assert proc.exitcode == 0

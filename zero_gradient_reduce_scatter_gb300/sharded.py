@@ -131,13 +131,15 @@ class ShardedZeroOptimizer:
     groups       hybrid sharding: G groups of K = M / G ranks (state sharded over K)
     transport    "direct" (collectives on device tensors: NCCL) or "host" (staged through
                  host memory: a backend such as gloo)
+    coalesce     direct transport: issue a step's per-bucket all-to-alls, and its per-bucket
+                 all-gathers, each as one group of collectives (one NCCL group call)
     full_params  keep the full parameters (default: stages 1 and 2; ZeRO-3 gathers per
                  bucket with gather_bucket, or into the full buffer with gather_all)
     """
 
     def __init__(self, numel, stage: int, master_init: torch.Tensor, group=None, bucket_bytes: int = 0,
                  groups: int = 1, ghat_buffer: bool | None = None, transport: str = "direct",
-                 full_params: bool | None = None, stream=None):
+                 full_params: bool | None = None, stream=None, coalesce: bool = True):
         import torch.distributed as dist
         if not (isinstance(master_init, torch.Tensor) and master_init.is_cuda and master_init.dtype == torch.float32):
             raise TypeError("master_init must be a CUDA float32 tensor of the unpadded parameters")
@@ -145,6 +147,7 @@ class ShardedZeroOptimizer:
             raise ValueError("transport must be 'direct' or 'host'")
         self.numel = [int(x) for x in numel]
         self.group = group
+        self.coalesce = bool(coalesce)
         self.M = dist.get_world_size(group)
         self.rank = dist.get_rank(group)
         self.stage, self.bucket_bytes = int(stage), int(bucket_bytes)
@@ -229,10 +232,20 @@ class ShardedZeroOptimizer:
         for d, h in zip(outs, hout):
             st.back(d, h)
 
+    def _grouped(self, fn):
+        """fn() with its per-bucket collectives issued as one group (one NCCL group call instead
+        of one call per bucket) where the transport is direct and torch can group them."""
+        import torch.distributed as dist
+        cm = getattr(dist, "_coalescing_manager", None)
+        if self._stage_io.host or cm is None or len(self.buckets) < 2 or not self.coalesce:
+            return fn()
+        with cm(self.intra, device=self.device):
+            return fn()
+
     def exchange(self, grad: torch.Tensor):
         """Step 1's collective: this rank's gradient out, its shard's slices in (self.recv)."""
-        self._collective("exchange", lambda g, r: exchange_gradients(g, r, self.buckets, self.K, self.intra),
-                         [grad], [self.recv])
+        self._grouped(lambda: self._collective(
+            "exchange", lambda g, r: exchange_gradients(g, r, self.buckets, self.K, self.intra), [grad], [self.recv]))
 
     def gather_all(self, dst: torch.Tensor | None = None):
         """The all-gather of every bucket into dst (bf16 [npad], padded; default the full
@@ -240,8 +253,8 @@ class ShardedZeroOptimizer:
         dst = self.param_full if dst is None else dst
         if dst is None:
             raise ValueError("no full parameter buffer: pass dst")
-        self._collective("gather", lambda s, f: gather_params(s, f, self.buckets, self.K, self.intra),
-                         [self.param_shards], [dst])
+        self._grouped(lambda: self._collective(
+            "gather", lambda s, f: gather_params(s, f, self.buckets, self.K, self.intra), [self.param_shards], [dst]))
 
     def gather_bucket(self, bucket: int, dst: torch.Tensor) -> torch.Tensor:
         """ZeRO-3: bucket `bucket`'s parameters into dst (bf16, at least K * S_b lanes); returns
