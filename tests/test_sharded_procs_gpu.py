@@ -105,11 +105,14 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
             if stage == 3:
                 assert opt.params() is None  # ZeRO-3: no persistent full parameters
                 assert bf16_ulp_diff(u16(opt.param_shards), st.param[rank][:p.shard_len]) <= 1
-                uoff = 0
+                uoffs = np.cumsum([0] + [b[1] for b in opt.buckets])
                 for b, (_off, n_b, _S, _) in enumerate(opt.buckets):  # per-module gathers
                     got = opt.gather_bucket(b, scratch)
-                    assert bf16_ulp_diff(u16(got), full[uoff:uoff + n_b]) <= 1
-                    uoff += n_b
+                    assert bf16_ulp_diff(u16(got), full[uoffs[b]:uoffs[b] + n_b]) <= 1
+                seq = list(range(len(opt.buckets)))
+                for order in (seq, seq[::-1]):  # forward and backward sweeps with prefetch
+                    for b, got in opt.prefetched_buckets(order, buffers=2 + k):
+                        assert bf16_ulp_diff(u16(got), full[uoffs[b]:uoffs[b] + opt.buckets[b][1]]) <= 1
             else:
                 assert bf16_ulp_diff(padded_to_unpadded(p, u16(opt.params())), full) <= 1
         state = opt.save_state()
@@ -148,7 +151,8 @@ def test_two_processes_on_one_gpu(stage, ghat_mode, streamed):
 def _nccl_one_rank(q, coalesce):
     """A job of one rank over NCCL (the only NCCL job one GPU can hold): the collectives run
     through NCCL, grouped per step or one call per bucket; three clipped steps and three
-    streamed ones against the oracle's one-rank step."""
+    streamed ones, and prefetched per-bucket gathers after each, against the oracle's
+    one-rank step."""
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(free_port()))
         import torch
@@ -165,7 +169,7 @@ def _nccl_one_rank(q, coalesce):
         dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
         w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
         mi = W.master_init(w, dev)
-        opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce)
+        opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce, full_params=True)
         assert opt.M == 1 and len(opt.buckets) >= 2
         p = O.plan(NUMEL, 1, BUCKET_BYTES)
         st = O.init_state(p, 2, f32(mi))
@@ -183,6 +187,9 @@ def _nccl_one_rank(q, coalesce):
             assert_state_close(f32(opt.get_state("master")), st.master[0][:p.shard_len], f"step {k} master")
             assert_state_close(f32(opt.get_state("v")), st.var[0][:p.shard_len], f"step {k} v")
             assert bf16_ulp_diff(padded_to_unpadded(p, u16(opt.params())), full) <= 1
+            uoffs = np.cumsum([0] + [b[1] for b in opt.buckets])
+            for b, got in opt.prefetched_buckets(reversed(range(len(opt.buckets))), buffers=3):
+                assert bf16_ulp_diff(u16(got), full[uoffs[b]:uoffs[b] + opt.buckets[b][1]]) <= 1
         opt.close()
         dist.destroy_process_group()
         q.put("ok")

@@ -78,13 +78,16 @@ def gather_params(shards: torch.Tensor, full: torch.Tensor, buckets, count: int,
     return works
 
 
-def gather_bucket_params(shards: torch.Tensor, dst: torch.Tensor, buckets, bucket: int, count: int, group=None):
+def gather_bucket_params(shards: torch.Tensor, dst: torch.Tensor, buckets, bucket: int, count: int, group=None,
+                         async_op: bool = False):
     """ZeRO-3 per-module gather: bucket `bucket`'s parameters, in tensor order, into
-    dst[:n_b] (dst holds count * S_b lanes; the lanes after n_b are the bucket's padding)."""
+    dst[:n_b] (dst holds count * S_b lanes; the lanes after n_b are the bucket's padding).
+    Returns the work handle when async_op."""
     import torch.distributed as dist
     base = sum(b[2] for b in buckets[:bucket])
     _off, _n, S, _ = buckets[bucket]
-    dist.all_gather_into_tensor(_bytes(dst[:count * S]), _bytes(shards[base:base + S]), group=group)
+    return dist.all_gather_into_tensor(_bytes(dst[:count * S]), _bytes(shards[base:base + S]), group=group,
+                                       async_op=async_op)
 
 
 def hybrid_groups(M: int, G: int):
@@ -322,6 +325,47 @@ class ShardedZeroOptimizer:
         for wk in gathers:
             if wk is not None:
                 wk.wait()
+
+    def prefetched_buckets(self, order, buffers: int = 2):
+        """ZeRO-3 just-in-time parameters ("CS336 2026 Lecture 8" Slides 24-26; "CS231n Lecture
+        11" 4.3: the next block's weights are gathered while the current one computes).
+
+        Yields (bucket, params) in `order`; `params` (bf16, the bucket's n_b values in tensor
+        order) is ready for work queued on the current stream when yielded. The all-gathers of
+        the next `buffers - 1` buckets are in flight meanwhile (asynchronous over the direct
+        transport), each into one of `buffers` transient buffers used in turn. A buffer is
+        reused only by a gather issued after the consumer's work on the previous bucket in it
+        was queued, and the collective waits for the work queued on the current stream before
+        it starts, so no gather overwrites a buffer still being read."""
+        order = list(order)
+        if not order:
+            return
+        if buffers < 2:
+            raise ValueError("buffers must be at least 2")
+        cap = self.K * max(self.buckets[b][2] for b in order)
+        bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(buffers)]
+        works = {}
+
+        def issue(i):
+            b = order[i]
+            S = self.buckets[b][2]
+            dst = bufs[i % buffers][:self.K * S]
+            if self._stage_io.host:
+                self.gather_bucket(b, dst)
+                works[i] = None
+            else:
+                works[i] = gather_bucket_params(self.param_shards, dst, self.buckets, b, self.K, self.intra,
+                                                async_op=True)
+
+        for i in range(min(buffers - 1, len(order))):
+            issue(i)
+        for i, b in enumerate(order):
+            if i + buffers - 1 < len(order):
+                issue(i + buffers - 1)
+            wk = works.pop(i)
+            if wk is not None:
+                wk.wait()
+            yield b, bufs[i % buffers][:self.buckets[b][1]]
 
     def _gather_sums(self):
         import torch.distributed as dist
