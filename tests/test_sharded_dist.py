@@ -250,3 +250,57 @@ def _hybrid_rank(rank, M, case):
 @pytest.mark.parametrize("case", ["two_buckets_ragged", "many_buckets"])
 def test_sharded_exchange_hybrid_four_ranks(case):
     _spawn(4, case, _hybrid_rank)
+
+
+def _leaving_rank(rank, world, port, q):
+    """Rank 1 leaves between steps (after one exchange, with nothing in flight); rank 0's next
+    exchange must end with an error, within the process group's short timeout, not hang."""
+    import time
+
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        import datetime
+
+        import torch
+        import torch.distributed as dist
+
+        import oracle as O
+        import zero_gradient_reduce_scatter_gb300 as zg
+        from zero_gradient_reduce_scatter_gb300.sharded import exchange_gradients
+
+        dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+        numel, bucket_bytes = CASES["two_buckets_ragged"]
+        p = O.plan(numel, world, bucket_bytes)
+        _, buckets = zg.layout(numel, world, 1, bucket_bytes)
+        g = torch.from_numpy(_grads(p, world, 5)[rank].view(np.int16).copy()).view(torch.bfloat16)
+        recv = torch.zeros(p.npad, dtype=torch.int16).view(torch.bfloat16)
+        exchange_gradients(g, recv, buckets, world)  # step 1: both ranks
+        if rank == 1:
+            q.put((rank, "left"))
+            q.close()
+            q.join_thread()  # the message is out before the process ends
+            os._exit(0)  # leaves between steps, without a word to the others
+        time.sleep(1.0)
+        t0 = time.time()
+        try:
+            exchange_gradients(g, recv, buckets, world)  # step 2: the peer is gone
+            q.put((rank, "completed"))
+        except Exception as e:  # detected on the host
+            q.put((rank, f"error {type(e).__name__} after {time.time() - t0:.1f}s"))
+    except BaseException:
+        q.put((rank, traceback.format_exc()))
+
+
+def test_rank_leaving_between_steps_is_detected():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_leaving_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert got[1] == "left"
+    assert got[0].startswith("error"), got[0]
+    assert float(got[0].split(" after ")[1][:-1]) < 60.0
