@@ -311,7 +311,8 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * The gather field has no effect: the owner always writes param_shards.
  * Calls of the emulated mode that would touch other ranks' data (zero_step, zero_step_host*,
  * the per-bucket and scheduled forms, zero_gather*) return INVALID_ARG on such a context.
- * zero_get_state copies this rank's shard (rank must be cfg->rank, or k with groups);
+ * zero_get_state copies this rank's shard (its `rank` argument must name the shard this
+ * context owns: cfg->rank, or cfg->rank % K with hybrid sharding);
  * zero_save_state writes this rank's real lanes of the unpadded vectors and leaves the other
  * lanes untouched (the ranks' outputs are disjoint; summing zero-filled outputs across
  * ranks, or across one group, gives the whole state); zero_load_state reads the whole

@@ -247,3 +247,43 @@ def test_sharded_per_bucket_steps_in_any_order():
     assert lib.zero_rank_step_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), stage, ctypes.byref(h), s) == -1
     for rc in ranks:
         rc.close()
+
+
+def test_sharded_nonfinite_on_one_rank_skips_every_rank():
+    """A NaN in one rank's gradient reaches every rank through the gathered sums of squares:
+    every rank skips the update (state unchanged, status NONFINITE), and the next finite step
+    runs on every rank as the oracle's does."""
+    dev = torch.device("cuda")
+    numel, M, stage = RAGGED, 4, 1
+    p = O.plan(numel, M, 6000)
+    w = W.small_variant(W.workload("tiny"), tuple(numel), steps=3)
+    mi = W.master_init(w, dev)
+    ranks = [RankCtx(numel, M, r, stage, mi, 6000) for r in range(M)]
+    st = O.init_state(p, stage, f32(mi))
+    h = zg.Hyper(clip=True, max_grad_norm=0.05)
+    oh = O.hyper(clip=True, max_grad_norm=0.05)
+    for k in range(3):
+        grads = _grads(p, M, k, dev)
+        if k == 1:
+            grads[2][int(p.t_off[3]) + 5] = float("nan")  # one lane of rank 2
+        before = [f32(rc.master).copy() for rc in ranks]
+        run_step(ranks, grads, h)
+        _, norm, _, rc_o = O.zero_step(p, st, [u16(g) for g in grads], oh)
+        torch.cuda.synchronize()
+        for i, rc in enumerate(ranks):
+            if k == 1:
+                assert rc_o == 1 and rc.status() == zg.ZERO_ERR_NONFINITE
+                assert np.array_equal(f32(rc.master).view(np.uint32), before[i].view(np.uint32))
+            else:
+                assert rc_o == 0 and rc.status() == 0
+            assert_state_close(f32(rc.master), st.master[rc.rank][:p.shard_len], f"step {k} rank {rc.rank}")
+            assert_state_close(f32(rc.v), st.var[rc.rank][:p.shard_len], f"step {k} rank {rc.rank} v")
+    for rc in ranks:
+        rc.close()
+
+
+def test_sharded_largest_rank_count():
+    # 64 ranks: the generic (runtime M) kernels; most ranks own a few real lanes per bucket
+    # (the average over 64 ranks is small: a lower threshold keeps the clip scale in play)
+    for rc in _run((3001, 1000, 37, 4099), 64, 3, True, bucket_bytes=6000, steps=2, max_norm=0.01)[0]:
+        rc.close()
