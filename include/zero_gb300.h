@@ -352,9 +352,23 @@ int zero_rank_step_bucket(zero_ctx* ctx, int64_t bucket, const void* src, int st
  * the fp64 sum of squares over its real lanes to *sumsq (device, 8-byte aligned). Under
  * ZERO_GHAT_MATERIALIZE (or AUTO choosing it) the fp32 average also goes to the ghat buffer,
  * and zero_rank_step reads it instead of src. hyper->clip must be 1.
- * Errors: BAD_CONTEXT, INVALID_ARG, MISALIGNED, SIZE_MISMATCH, CUDA. */
+ * src NULL (flat mode, after zero_rank_reduce_bucket of every bucket): *sumsq = the sum of the
+ * buckets' sums, and zero_rank_step then updates from the ghat buffer (materialized form).
+ * Errors: BAD_CONTEXT, INVALID_ARG (also: src NULL before every bucket was reduced, or src
+ * given while some were), MISALIGNED, SIZE_MISMATCH, CUDA. */
 int zero_rank_sumsq(zero_ctx* ctx, const void* src, const zero_hyper* hyper, double* sumsq,
                     void* stream);
+
+/* Clipped ZeRO-2 streaming (flat mode): reduces bucket `bucket`'s slice of this rank's shard
+ * from src (the exchange buffer; only the bucket's region is read) as soon as its all-to-all
+ * has landed: the average into the ghat buffer (required) and the bucket's sum of squares
+ * kept by the context. Once every bucket is reduced, zero_rank_sumsq(src = NULL) gives the
+ * rank's sum for the all-gather of sums, and zero_rank_step(src = NULL, sums) updates the
+ * shard from the ghat buffer ("CS336 2026 Lecture 8" Slide 23; "并行训练优化、MoE扩展与系统
+ * 瓶颈" 2.2.4: each bucket is reduce-scattered as its gradients appear; clipping needs every
+ * bucket's norm before the update). A bucket reduced twice keeps its last reduction.
+ * Errors: BAD_CONTEXT, INVALID_ARG, SIZE_MISMATCH (no ghat buffer), MISALIGNED, CUDA. */
+int zero_rank_reduce_bucket(zero_ctx* ctx, int64_t bucket, const void* src, void* stream);
 
 /* Hybrid mode only: the group partial of this rank's shard, part[j] = the K exchanged bf16
  * slices of local lane j summed in fp32 in order from +0 (no scaling; padding lanes 0), from

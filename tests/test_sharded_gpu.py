@@ -287,3 +287,54 @@ def test_sharded_largest_rank_count():
     # (the average over 64 ranks is small: a lower threshold keeps the clip scale in play)
     for rc in _run((3001, 1000, 37, 4099), 64, 3, True, bucket_bytes=6000, steps=2, max_norm=0.01)[0]:
         rc.close()
+
+
+def test_sharded_clipped_streaming_reduce_then_apply():
+    """zero_rank_reduce_bucket per bucket (reverse order, each right after its exchange), then
+    the rank's sum from the buckets' sums, the gathered sums and the update from the average:
+    the average bit-exact and the state as the oracle's clipped step."""
+    dev = torch.device("cuda")
+    numel, M, stage = RAGGED, 4, 2
+    p = O.plan(numel, M, 4096)
+    assert p.nb > 3
+    w = W.small_variant(W.workload("tiny"), tuple(numel), steps=3)
+    mi = W.master_init(w, dev)
+    ranks = [RankCtx(numel, M, r, stage, mi, 4096) for r in range(M)]
+    st = O.init_state(p, stage, f32(mi))
+    h = zg.Hyper(clip=True, max_grad_norm=0.05)
+    lib, s = zg._lib(), zg._stream_handle(None)
+    from rank_util import loopback_exchange, loopback_gather, loopback_sums
+    for k in range(3):
+        grads = _grads(p, M, k, dev)
+        loopback_exchange(ranks, grads)
+        for b in reversed(range(p.nb)):
+            for rc in ranks:
+                assert lib.zero_rank_reduce_bucket(rc.ctx, b, rc.recv.data_ptr(), s) == 0
+            if b == 1:  # not every bucket reduced yet: no sum, no whole-step call
+                rc = ranks[0]
+                assert lib.zero_rank_sumsq(rc.ctx, None, ctypes.byref(h), rc.sumsq.data_ptr(), s) == -1
+                assert lib.zero_rank_sumsq(rc.ctx, rc.recv.data_ptr(), ctypes.byref(h), rc.sumsq.data_ptr(), s) == -1
+                assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr(), None, stage, ctypes.byref(zg.Hyper()), s) == -1
+        for rc in ranks:
+            assert lib.zero_rank_sumsq(rc.ctx, None, ctypes.byref(h), rc.sumsq.data_ptr(), s) == 0
+        loopback_sums(ranks)
+        for rc in ranks:
+            assert lib.zero_rank_step(rc.ctx, None, rc.sums.data_ptr(), stage, ctypes.byref(h), s) == 0
+        loopback_gather(ranks)
+        full, norm, scale, _ = O.zero_step(p, st, [u16(g) for g in grads], O.hyper(clip=True, max_grad_norm=0.05))
+        assert scale < 1.0
+        torch.cuda.synchronize()
+        for rc in ranks:
+            assert np.array_equal(f32(rc.ghat).view(np.uint32), st.ghat[rc.rank][:p.shard_len].view(np.uint32))
+            gn, gs = rc.last_norm()
+            assert abs(gn - norm) <= 1e-7 * norm
+            assert_state_close(f32(rc.master), st.master[rc.rank][:p.shard_len], f"step {k} master")
+            assert_state_close(f32(rc.m), st.mom[rc.rank][:p.shard_len], f"step {k} m")
+            assert_state_close(f32(rc.v), st.var[rc.rank][:p.shard_len], f"step {k} v")
+            assert bf16_ulp_diff(padded_to_unpadded(p, u16(rc.full)), full) <= 1
+    rc = ranks[0]
+    nog = RankCtx(numel, M, 0, stage, mi, 4096, ghat=False)
+    assert lib.zero_rank_reduce_bucket(nog.ctx, 0, nog.recv.data_ptr(), s) == -3  # needs a ghat buffer
+    assert lib.zero_rank_reduce_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), s) == -1
+    for rc in ranks + [nog]:
+        rc.close()

@@ -4,9 +4,10 @@ NCCL does not run two ranks on one device, so the ranks exchange through gloo wi
 device buffers staged through host memory (ShardedZeroOptimizer(transport="host")). Each
 process runs the library's kernels on its own shard only. Three clipped steps on a ragged
 multi-bucket layout, at ZeRO-1 (full parameters kept) and ZeRO-3 (per-bucket gathers into a
-transient buffer), both forms of the clipped step, and three unclipped ZeRO-2 steps streamed
-bucket by bucket in backward order (step_streamed); every rank checks itself against the
-oracle's two-rank step: its shard of master / m / v (1e-6 relative; bit-identical expected),
+transient buffer), both forms of the clipped step, and three ZeRO-2 steps streamed bucket by
+bucket in backward order (step_streamed), unclipped and clipped; every rank checks itself
+against the oracle's two-rank step: its shard of master / m / v (1e-6 relative;
+bit-identical expected),
 the averaged gradient bit-exact when materialized, the norm within 1e-7 and equal on both
 ranks, the gathered bf16 parameters within 1 ulp; then the assembled checkpoint state equals
 the oracle's bit for bit.
@@ -75,7 +76,7 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
         assert opt.M == world and opt.rank == rank and len(opt.buckets) >= 2
         p = O.plan(NUMEL, world, BUCKET_BYTES)
         st = O.init_state(p, stage, f32(mi))
-        clip = not streamed  # the streamed form does not clip
+        clip = streamed in (False, "clipped")  # streamed=True: the unclipped streamed form
         h = zg.Hyper(clip=clip, max_grad_norm=0.05, ghat_mode=ghat_mode)
         oh = O.hyper(clip=clip, max_grad_norm=0.05)
         scratch = torch.empty(world * max(b[2] for b in opt.buckets), dtype=torch.bfloat16, device=dev)
@@ -87,7 +88,7 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
             else:
                 opt.step(mine, h)
             full, norm, scale, rc = O.zero_step(p, st, G, oh)
-            assert rc == 0 and (scale < 1.0 or streamed)
+            assert rc == 0 and (scale < 1.0 or not clip)
             assert opt.sync_status() == 0
             if clip:
                 gn, gs = opt.last_norm()
@@ -132,7 +133,8 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
 
 
 @pytest.mark.parametrize("stage,ghat_mode,streamed", [(1, "materialize", False), (3, "recompute", False),
-                                                      (3, "materialize", False), (2, "auto", True)])
+                                                      (3, "materialize", False), (2, "auto", True),
+                                                      (2, "materialize", "clipped")])
 def test_two_processes_on_one_gpu(stage, ghat_mode, streamed):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()

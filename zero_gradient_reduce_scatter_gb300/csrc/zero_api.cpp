@@ -979,6 +979,12 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
     if (e != cudaSuccess) return cuda_fail(e);
     c->t = t;
     c->rank_reduced = false;
+    if (c->cfg.sharded) {  // a loaded state starts a fresh step
+        std::fill(c->reduced.begin(), c->reduced.end(), 0);
+        c->n_reduced = 0;
+        std::fill(c->bucket_done.begin(), c->bucket_done.end(), 0);
+        c->n_bucket_done = 0;
+    }
     return ZERO_OK;
 }
 
@@ -1053,24 +1059,6 @@ static zg::StepArgs rank_args(zero_ctx* c) {
     return a;
 }
 
-// One bucket's sources for the fused kernel (zero_rank_step_bucket): the slice that source q
-// (of `count`) sent for this shard starts at lane off_b + q * S_b of recv; each pointer is
-// shifted back by the slice's local start base_b, since the fused kernel addresses its
-// sources by local lane (address arithmetic only: it reads lanes [base_b, base_b + S_b)).
-static void slice_sources(const zero_ctx* c, zg::StepArgs& a, const void* recv, int64_t b, int count) {
-    const zg::Bucket& G = c->buckets[(size_t)b];
-    const zg::Bucket& L = c->local[(size_t)b];
-    const int64_t S = L.end - L.off;
-    for (int q = 0; q < count; ++q)
-        a.grads[q] = (const uint16_t*)((uintptr_t)recv + 2 * (uintptr_t)(G.off + (int64_t)q * S) - 2 * (uintptr_t)L.off);
-    a.M = count;
-    a.vbeg = L.off / 8;
-    a.vend = L.end / 8;
-    a.b_first = b;
-    a.b_end = b + 1;
-    a.gext = L.end;
-}
-
 // The exchange buffer as the sources of one launch over the whole shard: `count` sources,
 // bucket b's slice of source q at lanes [count * base_b + q * S_b, +S_b) (the kernels find it
 // from the rank's own table).
@@ -1078,6 +1066,15 @@ static void exchange_sources(const zero_ctx* c, zg::StepArgs& a, const void* rec
     a.grads[0] = (const uint16_t*)recv;
     a.M = count;
     a.gext = c->npad;  // lanes of the exchange buffer
+}
+
+// Restricts a launch over the shard to bucket b's slice: local lanes [base_b, base_b + S_b).
+static void one_bucket(const zero_ctx* c, zg::StepArgs& a, int64_t b) {
+    const zg::Bucket& L = c->local[(size_t)b];
+    a.vbeg = L.off / 8;
+    a.vend = L.end / 8;
+    a.b_first = b;
+    a.b_end = b + 1;
 }
 
 // Hybrid mode: the G gathered fp32 group partials of this shard, group grp at [grp * shard_len].
@@ -1123,8 +1120,29 @@ int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* s
     if (rc) return rc;
     if (c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if ((rc = check_hyper(h))) return rc;
-    if (!h->clip || !src || !sumsq) return ZERO_ERR_INVALID_ARG;
-    if (!aligned16(src) || (reinterpret_cast<uintptr_t>(sumsq) & 7u)) return ZERO_ERR_MISALIGNED;
+    if (!h->clip || !sumsq) return ZERO_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(sumsq) & 7u) return ZERO_ERR_MISALIGNED;
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (!src) {  // every bucket reduced by zero_rank_reduce_bucket: the sum of their sums
+        if (c->n_reduced != nb) return ZERO_ERR_INVALID_ARG;
+        DeviceGuard guard(c->device);
+        if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e;
+        {
+            Timed tm(c, ZERO_K_NORM_FINAL, s);
+            e = zg::launch_sum_partials(c->bucket_sums, (int)nb, sumsq, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+        std::fill(c->reduced.begin(), c->reduced.end(), 0);
+        c->n_reduced = 0;
+        c->rank_reduced = true;
+        c->rank_mode = ZERO_GHAT_MATERIALIZE;
+        c->last_stream = s;
+        return ZERO_OK;
+    }
+    if (c->n_reduced) return ZERO_ERR_INVALID_ARG;  // a per-bucket reduction is in progress
+    if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
     int mode;
     if ((rc = resolve_ghat_mode(c, h, &mode))) return rc;
     DeviceGuard guard(c->device);
@@ -1159,7 +1177,7 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
                    void* stream) {
     int rc = check_rank_ctx(c);
     if (rc) return rc;
-    if (c->n_bucket_done) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
+    if (c->n_bucket_done || c->n_reduced) return ZERO_ERR_INVALID_ARG;  // a per-bucket step is in progress
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     if ((rc = check_hyper(h))) return rc;
     const int clip = h->clip;
@@ -1206,6 +1224,38 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
     return ZERO_OK;
 }
 
+int zero_rank_reduce_bucket(zero_ctx* c, int64_t bucket, const void* src, void* stream) {
+    int rc = check_rank_ctx(c);
+    if (rc) return rc;
+    const int64_t nb = (int64_t)c->buckets.size();
+    if (hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
+    if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
+    if (c->n_bucket_done || c->rank_reduced) return ZERO_ERR_INVALID_ARG;
+    if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t s = (cudaStream_t)stream;
+    // the bucket's average into the ghat shard, its sum of squares into its slot
+    zg::StepArgs a = rank_args(c);
+    exchange_sources(c, a, src, c->cfg.M);
+    one_bucket(c, a, bucket);
+    const int g1 = grid_for(c, zg::kVarRsNormWriteX, a.vend - a.vbeg);
+    cudaError_t e;
+    {
+        Timed tm(c, ZERO_K_RS_NORM, s);
+        e = zg::launch_rs_norm_exchange(a, true, g1, s);
+    }
+    if (e == cudaSuccess) {
+        Timed tm(c, ZERO_K_NORM_FINAL, s);
+        e = zg::launch_sum_partials(c->partials, g1, c->bucket_sums + bucket, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!c->reduced[(size_t)bucket]) c->n_reduced += 1;
+    c->reduced[(size_t)bucket] = 1;
+    c->last_stream = s;
+    return ZERO_OK;
+}
+
 int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stage, const zero_hyper* h,
                           void* stream) {
     int rc = check_rank_ctx(c);
@@ -1214,19 +1264,20 @@ int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stag
     if ((rc = check_hyper(h))) return rc;
     const int64_t nb = (int64_t)c->buckets.size();
     if (h->clip || hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
-    if (c->rank_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
+    if (c->rank_reduced || c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     zg::StepArgs a = rank_args(c);
-    slice_sources(c, a, src, bucket, c->cfg.M);
+    exchange_sources(c, a, src, c->cfg.M);
+    one_bucket(c, a, bucket);
     a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
-    const int g4 = grid_for(c, zg::kVarRsAdamwPlain, a.vend - a.vbeg);
+    const int g4 = grid_for(c, zg::kVarRsAdamwPlainX, a.vend - a.vbeg);
     cudaError_t e;
     {
         Timed tm(c, ZERO_K_RS_ADAMW, s);
-        e = zg::launch_rs_adamw(a, false, false, g4, s);
+        e = zg::launch_rs_adamw_exchange(a, false, g4, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     c->bucket_done[(size_t)bucket] = 1;

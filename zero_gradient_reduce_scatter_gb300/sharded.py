@@ -303,25 +303,38 @@ class ShardedZeroOptimizer:
         return None
 
     def step_streamed(self, grad: torch.Tensor, hyper: Hyper, order=None, gather: bool = True):
-        """One step without clipping, bucket by bucket (ZeRO-2 streaming, "CS336 2026 Lecture 8"
-        Slide 23; "并行训练优化、MoE扩展与系统瓶颈" 2.2.4): every bucket's exchange is issued at once
-        (asynchronous over NCCL), each bucket is updated as soon as its own exchange has
-        landed while later ones are still in flight, and its all-gather follows its update.
-        order: the buckets' order (default: layout order; backward passes produce them in
-        reverse). Results equal step()'s bit for bit."""
-        if hyper.clip:
-            raise ValueError("step_streamed does not clip: the norm needs every bucket first (use step)")
+        """One step, bucket by bucket (ZeRO-2 streaming, "CS336 2026 Lecture 8" Slide 23;
+        "并行训练优化、MoE扩展与系统瓶颈" 2.2.4): every bucket's exchange is issued at once
+        (asynchronous over NCCL) and each bucket is handled as soon as its own exchange has
+        landed while later ones are still in flight. Without clipping each bucket is updated
+        then, and its all-gather follows; with clipping each bucket is reduced into the ghat
+        buffer (required) with its sum of squares, then the sums are gathered and the shard is
+        updated from the average. order: the buckets' order (default: layout order; backward
+        passes produce them in reverse). Results equal step()'s."""
         if self.groups > 1:
             raise ValueError("step_streamed is the flat mode's form")
+        if hyper.clip and self.ghat is None:
+            raise ValueError("the clipped streamed step keeps the average in a ghat buffer (ghat_buffer=True)")
+        lib, ctx, s = _lib(), self._ctx, _stream_handle(None)
         order = list(range(len(self.buckets))) if order is None else list(order)
         works = [self.exchange_bucket(b, grad, async_op=True) for b in order]
         gathers = []
         for b, wk in zip(order, works):
             if wk is not None:
                 wk.wait()
+            if hyper.clip:
+                _check(lib.zero_rank_reduce_bucket(ctx, b, self.recv.data_ptr(), s), "zero_rank_reduce_bucket")
+                continue
             self.step_bucket(b, hyper)
             if gather and self.param_full is not None:
                 gathers.append(self.gather_bucket_into_full(b, async_op=True))
+        if hyper.clip:
+            _check(lib.zero_rank_sumsq(ctx, None, ctypes.byref(hyper), self.sumsq.data_ptr(), s), "zero_rank_sumsq")
+            self._gather_sums()
+            _check(lib.zero_rank_step(ctx, None, self.sumsq_all.data_ptr(), self.stage, ctypes.byref(hyper), s),
+                   "zero_rank_step")
+            if gather and self.param_full is not None:
+                self.gather_all()
         for wk in gathers:
             if wk is not None:
                 wk.wait()
