@@ -138,6 +138,8 @@ class ShardedZeroOptimizer:
                  all-gathers, each as one group of collectives (one NCCL group call)
     full_params  keep the full parameters (default: stages 1 and 2; ZeRO-3 gathers per
                  bucket with gather_bucket, or into the full buffer with gather_all)
+    stream       the stream the initialisation runs on (later calls run on the current
+                 stream, which the collectives also follow)
     """
 
     def __init__(self, numel, stage: int, master_init: torch.Tensor, group=None, bucket_bytes: int = 0,
@@ -311,6 +313,7 @@ class ShardedZeroOptimizer:
         buffer (required) with its sum of squares, then the sums are gathered and the shard is
         updated from the average. order: the buckets' order (default: layout order; backward
         passes produce them in reverse). Results equal step()'s."""
+        self._check_grad(grad)
         if self.groups > 1:
             raise ValueError("step_streamed is the flat mode's form")
         if hyper.clip and self.ghat is None:
@@ -391,12 +394,15 @@ class ShardedZeroOptimizer:
                          [self.parts])
 
     # -- the step ------------------------------------------------------------------------------
-    def step(self, grad: torch.Tensor, hyper: Hyper, gather: bool = True):
-        """One ZeRO step of this rank (every rank calls it with its own gradient, bf16 [npad]
-        in the padded layout). gather: all-gather the parameters into the full buffer."""
+    def _check_grad(self, grad: torch.Tensor):
         npad = self.sizes["npad"]
         if not (grad.is_cuda and grad.dtype == torch.bfloat16 and grad.is_contiguous() and grad.numel() == npad):
             raise ValueError(f"grad must be a contiguous CUDA bf16 tensor of npad={npad}")
+
+    def step(self, grad: torch.Tensor, hyper: Hyper, gather: bool = True):
+        """One ZeRO step of this rank (every rank calls it with its own gradient, bf16 [npad]
+        in the padded layout). gather: all-gather the parameters into the full buffer."""
+        self._check_grad(grad)
         lib, ctx, s = _lib(), self._ctx, _stream_handle(None)
         self.exchange(grad)
         src = self.recv
