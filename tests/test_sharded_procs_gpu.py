@@ -10,7 +10,8 @@ against the oracle's two-rank step: its shard of master / m / v (1e-6 relative;
 bit-identical expected),
 the averaged gradient bit-exact when materialized, the norm within 1e-7 and equal on both
 ranks, the gathered bf16 parameters within 1 ulp; then the assembled checkpoint state equals
-the oracle's bit for bit.
+the oracle's bit for bit, and both ranks resume from it in another bucket layout and take one
+more step as the oracle does.
 
 The ranks wait for each other only on the host (gloo), never inside a kernel.
 """
@@ -125,7 +126,21 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
             want[u[real]] = flat[real]
             assert np.array_equal(f32(state[name]).view(np.uint32), want.view(np.uint32)), name
         assert state["t"] == 3
+        # resume from the checkpoint in another layout (one bucket) and take one more step
+        sd = opt.state_dict()
         opt.close()
+        opt2 = zg.ShardedZeroOptimizer(NUMEL, stage, mi, bucket_bytes=0, transport="host", ghat_buffer=True)
+        opt2.load_state_dict(sd)
+        assert opt2.t == 3
+        p2 = O.plan(NUMEL, world, 0)
+        st2 = O.init_state(p2, stage, sd["master"].numpy(), sd["m"].numpy(), sd["v"].numpy(), t=3)
+        G = _grads_all(p2, world, 9)
+        mine = torch.from_numpy(G[rank].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        opt2.step(mine, h)
+        O.zero_step(p2, st2, G, oh)
+        assert_state_close(f32(opt2.get_state("master")), st2.master[rank][:p2.shard_len], "resumed master")
+        assert_state_close(f32(opt2.get_state("v")), st2.var[rank][:p2.shard_len], "resumed v")
+        opt2.close()
         dist.destroy_process_group()
         q.put((rank, "ok"))
     except BaseException:

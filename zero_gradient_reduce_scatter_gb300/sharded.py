@@ -480,6 +480,20 @@ class ShardedZeroOptimizer:
                                       _stream_handle(None)), "zero_load_state")
         torch.cuda.current_stream().synchronize()
 
+    def state_dict(self) -> dict:
+        """Host copy of the whole state for a checkpoint file (the same on every rank; one
+        rank writes it), with the tensor sizes."""
+        st = self.save_state()
+        torch.cuda.current_stream().synchronize()
+        return {"numel": list(self.numel), "t": st["t"], **{k: st[k].cpu() for k in ("master", "m", "v")}}
+
+    def load_state_dict(self, sd: dict):
+        """Loads a state_dict written by any job over the same tensors (any rank count, stage
+        or bucket size, emulated or process-per-rank)."""
+        if list(sd["numel"]) != list(self.numel):
+            raise ValueError("checkpoint was written for different tensors")
+        self.load_state(sd)
+
     @property
     def t(self) -> int:
         t = ctypes.c_int64()
