@@ -98,7 +98,7 @@ def _run(numel, M, stage, clip, ghat_mode="auto", bucket_bytes=0, groups=1, step
     return ranks, p, st
 
 
-@pytest.mark.parametrize("M", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 16])
 def test_sharded_flat_clipped_zero1(M):
     for rc in _run(RAGGED, M, 1, True, bucket_bytes=8192)[0]:
         rc.close()

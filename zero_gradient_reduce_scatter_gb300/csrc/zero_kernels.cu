@@ -653,6 +653,17 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
         const int64_t o = vi * 8;
         c.seek(o);
         float sum[8], gh[8], p[8], m[8], v[8];
+        if constexpr (MT == 1) {
+            // one source: too few loads in flight per thread to cover the memory latency at one
+            // CTA per SM, so the next iteration's state lines are prefetched into L2 (the state
+            // arrays hold every lane below vend * 8, so the addresses are in range)
+            const int64_t on = o + stride * 8;
+            if (on < a.vend * 8) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.master + on));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.m + on));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.v + on));
+            }
+        }
         if (!ZG_OK(a.status, o + 8 <= a.npad && src_in_range<SRC>(a, c.e, o), kSiteStepLanes, o)) continue;
         // state loads first: neutral for the plain kernel, +10% for the grouped one (measured)
         load_state<kStateLoadRsAdamw>(a, o, p, m, v);
