@@ -1044,8 +1044,12 @@ def run_shard_emulated(args):
     if args.ranks:
         w = W.small_variant(w, w.numel, name=w.name + f" (as {args.ranks} ranks)", M=args.ranks)
     M, lib, sh = w.M, zg._lib(), zg._stream_handle(None)
-    _, buckets = zg.layout(w.numel, M, w.stage, w.bucket_bytes)
-    sz = zg.plan(w.numel, M, w.stage, w.bucket_bytes, rank=0)
+    G = max(1, args.groups)
+    if M % G:
+        raise SystemExit(f"{M} ranks do not split into {G} groups")
+    K = M // G  # owners of one copy of the state (the layout is planned for them)
+    _, buckets = zg.layout(w.numel, M, w.stage, w.bucket_bytes, groups=G)
+    sz = zg.plan(w.numel, M, w.stage, w.bucket_bytes, groups=G, rank=0)
     L, npad = sz["shard_len"], sz["npad"]
     clip = w.clip is not None
     h = zg.Hyper(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, clip=clip,
@@ -1061,18 +1065,22 @@ def run_shard_emulated(args):
         b["scratch"] = torch.empty(sz["bytes_scratch"], dtype=torch.uint8, device=device)
         b["recv"] = torch.empty(npad, dtype=torch.bfloat16, device=device)
         b["sumsq"] = torch.zeros(1, dtype=torch.float64, device=device)
-        b["sums"] = torch.zeros(M, dtype=torch.float64, device=device)
+        b["sums"] = torch.zeros(K, dtype=torch.float64, device=device)
+        if G > 1:
+            b["part"] = torch.empty(L, dtype=torch.float32, device=device)
+            b["parts"] = torch.empty(G * L, dtype=torch.float32, device=device)
+        b["grp"], b["k"] = divmod(r, K)
         bufs = zg.Buffers(b["master"].data_ptr(), b["m"].data_ptr(), b["v"].data_ptr(),
                           b["ghat"].data_ptr() if ghat else None, b["full"].data_ptr(), b["shards"].data_ptr(),
                           b["scratch"].data_ptr())
         ctx = ctypes.c_void_p()
-        cfg = zg.Config(M, w.stage, w.bucket_bytes, 0, 0, 1, r)
+        cfg = zg.Config(M, w.stage, w.bucket_bytes, 0, G if G > 1 else 0, 1, r)
         zg._check(lib.zero_init(ctypes.byref(ctx), ctypes.byref(cfg), ctypes.cast(zg._i64_array(w.numel), ctypes.c_void_p),
                                 len(w.numel), ctypes.byref(bufs), mi.data_ptr(), sh), "zero_init")
         b["ctx"] = ctx
         ranks.append(b)
     del mi
-    toff, _ = zg.layout(w.numel, M, w.stage, w.bucket_bytes)
+    toff, _ = zg.layout(w.numel, M, w.stage, w.bucket_bytes, groups=G)
     grads = [torch.zeros(npad, dtype=torch.bfloat16, device=device) for _ in range(M)]
     sig = W.sigmas(w)
     for r in range(M):
@@ -1081,29 +1089,61 @@ def run_shard_emulated(args):
     for bk in buckets:
         bases.append(bases[-1] + bk[2])
 
+    # the collectives, as device copies (the exchange and the all-gather inside each group,
+    # the group partials of a shard across the groups, the sums inside the group)
     def exchange():
-        for r, b in enumerate(ranks):
+        for b in ranks:
             for off, _n, S, _ in buckets:
-                for q in range(M):
-                    b["recv"][off + q * S: off + (q + 1) * S].copy_(grads[q][off + r * S: off + (r + 1) * S])
+                for q in range(K):
+                    src = grads[b["grp"] * K + q]
+                    b["recv"][off + q * S: off + (q + 1) * S].copy_(src[off + b["k"] * S: off + (b["k"] + 1) * S])
 
     def gather():
         for b in ranks:
             for i, (off, _n, S, _) in enumerate(buckets):
-                for q in range(M):
-                    b["full"][off + q * S: off + (q + 1) * S].copy_(ranks[q]["shards"][bases[i]:bases[i] + S])
+                for q in range(K):
+                    sh_q = ranks[b["grp"] * K + q]["shards"]
+                    b["full"][off + q * S: off + (q + 1) * S].copy_(sh_q[bases[i]:bases[i] + S])
 
-    def kernels():
-        if clip:
-            for b in ranks:
-                zg._check(lib.zero_rank_sumsq(b["ctx"], b["recv"].data_ptr(), ctypes.byref(h), b["sumsq"].data_ptr(), sh),
-                          "zero_rank_sumsq")
-            allsums = torch.cat([b["sumsq"] for b in ranks])
-            for b in ranks:
-                b["sums"].copy_(allsums)
+    def xfer_parts():
         for b in ranks:
-            zg._check(lib.zero_rank_step(b["ctx"], b["recv"].data_ptr(), b["sums"].data_ptr() if clip else None,
+            for g in range(G):
+                b["parts"][g * L:(g + 1) * L].copy_(ranks[g * K + b["k"]]["part"])
+
+    def xfer_sums():
+        for b in ranks:
+            for q in range(K):
+                b["sums"][q:q + 1].copy_(ranks[b["grp"] * K + q]["sumsq"])
+
+    def src(b):
+        return b["parts"] if G > 1 else b["recv"]
+
+    # the library's calls, phase by phase
+    def lib_partial():
+        for b in ranks:
+            zg._check(lib.zero_rank_partial(b["ctx"], b["recv"].data_ptr(), b["part"].data_ptr(), sh),
+                      "zero_rank_partial")
+
+    def lib_sumsq():
+        for b in ranks:
+            zg._check(lib.zero_rank_sumsq(b["ctx"], src(b).data_ptr(), ctypes.byref(h), b["sumsq"].data_ptr(), sh),
+                      "zero_rank_sumsq")
+
+    def lib_step():
+        for b in ranks:
+            zg._check(lib.zero_rank_step(b["ctx"], src(b).data_ptr(), b["sums"].data_ptr() if clip else None,
                                          w.stage, ctypes.byref(h), sh), "zero_rank_step")
+
+    phases = [("copy", exchange)]
+    if G > 1:
+        phases += [("lib", lib_partial), ("copy", xfer_parts)]
+    if clip:
+        phases += [("lib", lib_sumsq), ("copy", xfer_sums)]
+    phases += [("lib", lib_step), ("copy", gather)]
+
+    def kernels():  # the library's calls alone (for per-kernel timing), with the copies between
+        for kind, fn in phases[1:-1]:
+            fn()
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -1115,20 +1155,26 @@ def run_shard_emulated(args):
         if lib.zero_sync_status(b["ctx"]) != 0:
             raise SystemExit("warm-up step saw a non-finite gradient norm")
     # every step: the exchange copies, the ranks' kernels (events around them), the all-gather
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    nlib = sum(1 for kind, _ in phases if kind == "lib")
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nlib)]
+          for _ in range(args.steps)]
     clocks = ClockSampler(local)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        exchange()
-        ev[i][0].record(stream)
-        kernels()
-        ev[i][1].record(stream)
-        gather()
+        j = 0
+        for kind, fn in phases:
+            if kind == "lib":
+                ev[i][j][0].record(stream)
+                fn()
+                ev[i][j][1].record(stream)
+                j += 1
+            else:
+                fn()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    kms = [a.elapsed_time(b) for a, b in ev]
+    kms = [sum(a.elapsed_time(b) for a, b in step) for step in ev]
     k_ms = sum(kms) / args.steps
     total_ms = t0.elapsed_time(t1) / args.steps
     # per-kernel times in a second pass (each launch bracketed by events)
@@ -1151,9 +1197,21 @@ def run_shard_emulated(args):
     ghat_mode = args.ghat_mode
     if ghat_mode == "auto":
         ghat_mode = ("materialize" if ghat else "recompute") if clip else "none"
-    dom = max((k for k in tot if tot[k][1] > 0), key=lambda k: tot[k][0])
-    dom_bytes = kernel_alg_bytes_per_lane(dom, M, ghat_mode == "materialize") * L  # per rank launch
-    dom_ms = tot[dom][0] / tot[dom][1]
+    mat = ghat_mode == "materialize"
+    # algorithmic bytes per lane of the rank's shard, per kernel kind and step: flat, the
+    # emulated kernels' bytes with M bf16 sources; hybrid, the group partial (K bf16 sources
+    # in, one fp32 out) and the passes over the G fp32 partials
+    if G > 1:
+        per_lane = {"rs_norm": (2 * K + 4) + ((4 * G + (4 if mat else 0)) if clip else 0),
+                    "rs_adamw": 4 * G + 26, "adamw": 30, "norm_final": 0}
+    else:
+        per_lane = {"rs_norm": (2 * M + (4 if mat else 0)) if clip else 0, "rs_adamw": 2 * M + 26, "adamw": 30,
+                    "norm_final": 0}
+    ran = {k: v for k, v in tot.items() if v[1] > 0}
+    step_bytes = sum(per_lane.get(k, 0) for k in ran) * L * M
+    dom = max(ran, key=lambda k: ran[k][0])
+    dom_ms = ran[dom][0] / ran[dom][1]
+    dom_bytes = per_lane.get(dom, 0) * L * M * args.steps / ran[dom][1]  # per launch
     peak, peak_kind = hbm_peak()
     n = w.N
     line = {
@@ -1161,15 +1219,19 @@ def run_shard_emulated(args):
         "warmup": args.warmup, "ms_per_step": k_ms, "ms_per_step_median": round(statistics.median(kms), 4),
         "ms_per_step_min": round(min(kms), 4), "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name + f"; process-per-rank kernels of all {M} ranks, one process",
-                   "params": n, "M": M, "stage": w.stage, "clip": w.clip, "bucket_bytes": w.bucket_bytes,
+        "config": {"workload": w.name + f"; process-per-rank kernels of all {M} ranks, one process"
+                               + (f", hybrid sharding: {G} groups of {K}" if G > 1 else ""),
+                   "params": n, "M": M, "groups": G, "stage": w.stage, "clip": w.clip, "bucket_bytes": w.bucket_bytes,
                    "ghat_mode": ghat_mode, "shard_lanes": L, "padded_lanes": npad,
                    "l2": l2_note(2 * npad * M),
                    "parallelism": f"zero-dp{M} emulated: {M} rank contexts on one GPU, collectives as device copies"},
         "value_counts": "the ranks' kernels only (the step's library calls, all ranks one after another)",
         "ms_per_step_with_copies": round(total_ms, 4),
-        "frac_of_peak_alg": round(alg_bytes_per_param(M) * n / (k_ms / 1e3) / 1e9 / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": dom + " (exchange-layout sources)", "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
+        "kernel_alg_bytes_per_step": step_bytes,
+        "frac_of_peak_kernels": round(step_bytes / (k_ms / 1e3) / 1e9 / peak, 4),
+        "frac_of_peak_alg": round(alg_bytes_per_param(M) * n / (k_ms / 1e3) / 1e9 / peak, 4) if G == 1 else None,
+        "roofline": {"bound": "hbm", "kernel": dom + (" (exchange-layout sources)" if G == 1 else " (hybrid rank kernels)"),
+                     "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4),
                      "traffic": None, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
