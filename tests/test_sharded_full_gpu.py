@@ -23,7 +23,6 @@ import torch
 
 import oracle as O
 import workloads as W
-import zero_gradient_reduce_scatter_gb300 as zg
 from parity_util import REL_NORM, bf16_ulp_diff, f32, make_hyper, state_errors, u16
 from rank_util import RankCtx, run_step
 from test_parity_full_gpu import CHUNK, sample_lanes, streamed_norm, unpadded_of
