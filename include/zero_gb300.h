@@ -318,14 +318,15 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * ranks, or across one group, gives the whole state); zero_load_state reads the whole
  * unpadded vectors. */
 
-/* Without clipping, the whole update of this rank's shard in one fused pass (one launch over
- * every bucket of the shard):
- * reduce-scatter from the exchanged slices (rank-ordered fp32 sum x (float)(1/M)), AdamW,
- * the bf16 shard into param_shards. With clipping: zero_rank_sumsq first, then the gathered
- * sums, then this call. Increments t.
+/* Without clipping, the whole update of this rank's shard in one fused pass, one launch over
+ * every bucket of the shard: reduce-scatter from the exchanged slices (rank-ordered fp32 sum
+ * x (float)(1/M)), AdamW, the bf16 shard into param_shards. With clipping: zero_rank_sumsq
+ * first, then the gathered sums, then this call. Increments t.
  *  src        flat mode: bf16 recv [npad] in the exchange layout (read-only, borrowed until
  *             the stream passes the call); hybrid mode: fp32 parts [G * shard_len], the
- *             gathered group partials of this shard, group grp at [grp * shard_len]
+ *             gathered group partials of this shard, group grp at [grp * shard_len]. May be
+ *             NULL when the clipped form is the materialized one (the update then reads the
+ *             average from the ghat buffer)
  *  sumsq_all  clipping only (else NULL): device fp64 [P], P = M (flat) or K (hybrid), entry i
  *             = the value zero_rank_sumsq wrote on rank i (of this group); the same on every
  *             rank, so every rank computes the same norm and clip scale
