@@ -76,7 +76,7 @@ extern "C" {
                                       none, or a step past the schedule's last entry        */
 
 #define ZERO_ALIGN       64  /* shard length granule in lanes: 128 B of bf16, 256 B of fp32 */
-#define ZERO_MAX_RANKS   64  /* largest emulated rank count M                             */
+#define ZERO_MAX_RANKS   64  /* largest rank count M (emulated ranks, or processes)       */
 #define ZERO_NOALLOC_MAX_BUCKETS 2048  /* bucket-table rows zero_grad_norm_noalloc can hold  */
 #define ZERO_MAX_SCHEDULE 1024  /* entries of one step schedule (zero_set_schedule), kept in
                                    the scratch buffer (40 bytes each)                       */
@@ -116,7 +116,8 @@ typedef struct zero_ctx zero_ctx; /* opaque, library-owned */
 
 /* Layout and persistence choices, fixed for the life of a context. */
 typedef struct {
-    int32_t M;            /* emulated data-parallel ranks, 1..ZERO_MAX_RANKS            */
+    int32_t M;            /* data-parallel ranks, 1..ZERO_MAX_RANKS: emulated on this
+                             device, or the job's processes when sharded = 1                */
     int32_t stage;        /* ZeRO stage: 1, 2 or 3                                        */
     int64_t bucket_bytes; /* bf16 gradient bytes per bucket; 0 = one bucket              */
     int32_t gather;       /* ZERO_GATHER_FUSED or ZERO_GATHER_SHARDS (stage 3 only)       */
