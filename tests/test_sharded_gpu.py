@@ -338,3 +338,12 @@ def test_sharded_clipped_streaming_reduce_then_apply():
     assert lib.zero_rank_reduce_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), s) == -1
     for rc in ranks + [nog]:
         rc.close()
+
+
+@pytest.mark.parametrize("ghat_mode", ["materialize", "recompute"])
+def test_sharded_zero_size_tensors_and_many_buckets(ghat_mode):
+    # zero-size tensors between real ones, 64-byte buckets (about one tensor each: ~60 local
+    # buckets walked by one launch), 3 ranks (inexact 1/M, generic source count)
+    numel = tuple([0, 5, 0, 1, 33, 0] + [17 + 29 * i for i in range(50)] + [0, 1000, 3])
+    for rc in _run(numel, 3, 3, True, ghat_mode=ghat_mode, bucket_bytes=64, max_norm=0.01)[0]:
+        rc.close()
