@@ -304,3 +304,49 @@ def test_rank_leaving_between_steps_is_detected():
     assert got[1] == "left"
     assert got[0].startswith("error"), got[0]
     assert float(got[0].split(" after ")[1][:-1]) < 60.0
+
+
+def _random_layouts_rank(rank, M, case):
+    """Five seeded random layouts (sizes 0..5000, some zero, bucket caps from one tensor to
+    everything) over M = 3 ranks: the exchange delivers the oracle's operands for this owner
+    and the all-gather rebuilds the oracle's parameters."""
+    import torch
+
+    import oracle as O
+    import zero_gradient_reduce_scatter_gb300 as zg
+    from zero_gradient_reduce_scatter_gb300.sharded import exchange_gradients, gather_params
+
+    rng = np.random.default_rng(77)
+    for trial in range(5):
+        T = int(rng.integers(1, 12))
+        numel = tuple(int(x) if rng.random() > 0.15 else 0 for x in rng.integers(1, 5000, T))
+        if sum(numel) == 0:
+            numel = numel + (7,)
+        bucket_bytes = int(rng.choice([0, 64, 2048, 10000]))
+        p = O.plan(numel, M, bucket_bytes)
+        toff, buckets = zg.layout(numel, M, 1, bucket_bytes)
+        assert [int(x) for x in p.t_off] == toff
+        G = _grads(p, M, seed=500 + trial)
+        mine = torch.from_numpy(G[rank].view(np.int16).copy()).view(torch.bfloat16)
+        recv = torch.zeros(p.npad, dtype=torch.int16).view(torch.bfloat16)
+        exchange_gradients(mine, recv, buckets, M)
+        got = recv.view(torch.int16).numpy().view(np.uint16)
+        virt = [np.full(p.npad, BF16_NAN, dtype=np.uint16) for _ in range(M)]
+        for b in range(p.nb):
+            off, S = int(p.b_off[b]), int(p.b_S[b])
+            for src in range(M):
+                virt[src][off + rank * S: off + (rank + 1) * S] = got[off + src * S: off + (src + 1) * S]
+        want = O.reduce_scatter(p, G)[rank]
+        assert np.array_equal(O.reduce_scatter(p, virt)[rank].view(np.uint32), want.view(np.uint32)), trial
+        st = O.init_state(p, 3, np.zeros(p.N, np.float32))
+        full_want, _, _, _ = O.zero_step(p, st, G, O.hyper())
+        shard = torch.from_numpy(st.param[rank][:p.shard_len].view(np.int16).copy()).view(torch.bfloat16)
+        full = torch.zeros(p.npad, dtype=torch.int16).view(torch.bfloat16)
+        gather_params(shard, full, buckets, M)
+        u = p.unpadded_index()
+        full_u = full.view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(full_u[u >= 0][np.argsort(u[u >= 0])], full_want), trial
+
+
+def test_sharded_exchange_random_layouts_three_ranks():
+    _spawn(3, None, _random_layouts_rank)

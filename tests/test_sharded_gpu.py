@@ -347,3 +347,23 @@ def test_sharded_zero_size_tensors_and_many_buckets(ghat_mode):
     numel = tuple([0, 5, 0, 1, 33, 0] + [17 + 29 * i for i in range(50)] + [0, 1000, 3])
     for rc in _run(numel, 3, 3, True, ghat_mode=ghat_mode, bucket_bytes=64, max_norm=0.01)[0]:
         rc.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_sharded_random_configurations(seed):
+    """Seeded random configurations: tensor sizes (some zero), rank count, groups, stage,
+    bucket cap and clipping form, two steps each, every rank against the oracle."""
+    rng = np.random.default_rng(9000 + seed)
+    T = int(rng.integers(1, 9))
+    numel = tuple(int(x) if rng.random() > 0.15 else 0 for x in rng.integers(1, 6000, T))
+    if sum(numel) == 0:
+        numel = numel + (11,)
+    groups = int(rng.choice([1, 1, 2]))
+    M = groups * int(rng.choice([1, 2, 3, 4])) if groups > 1 else int(rng.integers(1, 10))
+    stage = int(rng.integers(1, 4))
+    clip = bool(rng.random() < 0.6)
+    ghat_mode = str(rng.choice(["auto", "materialize", "recompute"]))
+    bucket_bytes = int(rng.choice([0, 128, 3000]))
+    for rc in _run(numel, M, stage, clip, ghat_mode=ghat_mode, bucket_bytes=bucket_bytes, groups=groups, steps=2,
+                   max_norm=1e-4)[0]:
+        rc.close()
