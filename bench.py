@@ -996,9 +996,12 @@ def run_shard(args):
                        "stage": w.stage, "clip": w.clip, "bucket_bytes": w.bucket_bytes, "ghat_mode": ghat_mode,
                        "padded_lanes": opt.sizes["npad"], "shard_lanes": L,
                        "l2": l2_note(opt.sizes["bytes_grad_each"] * 2 + 12 * L),
-                       "parallelism": f"zero-dp{world}: one process per GPU, state sharded over {world} ranks "
-                                      f"(NCCL all-to-all of bf16 bucket slices, rank-ordered fp32 sum at the owner, "
-                                      f"bf16 all-gather)"},
+                       "parallelism": (f"zero-dp{world}: one process per GPU, state sharded over {world} ranks "
+                                       f"(NCCL all-to-all of bf16 bucket slices, rank-ordered fp32 sum at the owner, "
+                                       f"bf16 all-gather)") if world > 1 else
+                                      ("zero-dp1: one process, the whole state on one GPU (the exchange and the "
+                                       "all-gather of one rank are identities: the kernels read the gradient in "
+                                       "place, the full parameters are the bf16 shard)")},
             "kernel_ms_per_step": round(kernel_ms, 4),
             "collective_ms_per_step": round(ms_per_step - kernel_ms, 4),
             "kernel_timing": "a second pass of the same steps, each kernel launch bracketed by events",

@@ -4,14 +4,13 @@ NCCL does not run two ranks on one device, so the ranks exchange through gloo wi
 device buffers staged through host memory (ShardedZeroOptimizer(transport="host")). Each
 process runs the library's kernels on its own shard only. Three clipped steps on a ragged
 multi-bucket layout, at ZeRO-1 (full parameters kept) and ZeRO-3 (per-bucket gathers into a
-transient buffer), both forms of the clipped step, and three ZeRO-2 steps streamed bucket by
-bucket in backward order (step_streamed), unclipped and clipped; every rank checks itself
-against the oracle's two-rank step: its shard of master / m / v (1e-6 relative;
-bit-identical expected),
-the averaged gradient bit-exact when materialized, the norm within 1e-7 and equal on both
-ranks, the gathered bf16 parameters within 1 ulp; then the assembled checkpoint state equals
-the oracle's bit for bit, and both ranks resume from it in another bucket layout and take one
-more step as the oracle does.
+transient buffer), both forms of the clipped step, flat and hybrid with one rank per group;
+and three ZeRO-2 steps streamed bucket by bucket in backward order (step_streamed), unclipped
+and clipped. Every rank checks itself against the oracle's two-rank step: its shard of
+master / m / v (1e-6 relative; bit-identical expected), the averaged gradient bit-exact when
+materialized, the norm within 1e-7 and equal on both ranks, the gathered bf16 parameters within
+1 ulp. Then the assembled checkpoint state equals the oracle's bit for bit, and both ranks
+resume from it in another bucket layout and take one more step as the oracle does.
 
 The ranks wait for each other only on the host (gloo), never inside a kernel.
 """
@@ -55,7 +54,7 @@ def _grads_all(p, M, k):
     return out
 
 
-def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
+def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False, groups=1):
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
         import torch
@@ -73,10 +72,14 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
         w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
         mi = W.master_init(w, dev)
         opt = zg.ShardedZeroOptimizer(NUMEL, stage, mi, bucket_bytes=BUCKET_BYTES, transport="host",
-                                      ghat_buffer=True)
+                                      ghat_buffer=True, groups=groups)
         assert opt.M == world and opt.rank == rank and len(opt.buckets) >= 2
-        p = O.plan(NUMEL, world, BUCKET_BYTES)
-        st = O.init_state(p, stage, f32(mi))
+        K = world // groups  # owners per group: the oracle plans for K
+        assert opt.identity == (K == 1)
+        if opt.identity:  # nothing to exchange, and the full parameters are the shard itself
+            assert opt.recv is None and (stage == 3 or opt.params() is opt.param_shards)
+        p = O.plan(NUMEL, K, BUCKET_BYTES)
+        st = O.init_state(p, stage, f32(mi), groups=groups)
         clip = streamed in (False, "clipped")  # streamed=True: the unclipped streamed form
         h = zg.Hyper(clip=clip, max_grad_norm=0.05, ghat_mode=ghat_mode)
         oh = O.hyper(clip=clip, max_grad_norm=0.05)
@@ -129,11 +132,12 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
         # resume from the checkpoint in another layout (one bucket) and take one more step
         sd = opt.state_dict()
         opt.close()
-        opt2 = zg.ShardedZeroOptimizer(NUMEL, stage, mi, bucket_bytes=0, transport="host", ghat_buffer=True)
+        opt2 = zg.ShardedZeroOptimizer(NUMEL, stage, mi, bucket_bytes=0, transport="host", ghat_buffer=True,
+                                       groups=groups)
         opt2.load_state_dict(sd)
         assert opt2.t == 3
-        p2 = O.plan(NUMEL, world, 0)
-        st2 = O.init_state(p2, stage, sd["master"].numpy(), sd["m"].numpy(), sd["v"].numpy(), t=3)
+        p2 = O.plan(NUMEL, K, 0)
+        st2 = O.init_state(p2, stage, sd["master"].numpy(), sd["m"].numpy(), sd["v"].numpy(), t=3, groups=groups)
         G = _grads_all(p2, world, 9)
         mine = torch.from_numpy(G[rank].view(np.int16).copy()).to(dev).view(torch.bfloat16)
         opt2.step(mine, h)
@@ -147,14 +151,18 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False):
         q.put((rank, traceback.format_exc()))
 
 
-@pytest.mark.parametrize("stage,ghat_mode,streamed", [(1, "materialize", False), (3, "recompute", False),
-                                                      (3, "materialize", False), (2, "auto", True),
-                                                      (2, "materialize", "clipped")])
-def test_two_processes_on_one_gpu(stage, ghat_mode, streamed):
+@pytest.mark.parametrize("stage,ghat_mode,streamed,groups", [(1, "materialize", False, 1), (3, "recompute", False, 1),
+                                                             (3, "materialize", False, 1), (2, "auto", True, 1),
+                                                             (2, "materialize", "clipped", 1),
+                                                             (1, "materialize", False, 2), (3, "recompute", False, 2)])
+def test_two_processes_on_one_gpu(stage, ghat_mode, streamed, groups):
+    """groups=2: hybrid sharding with one rank per group (a replicated state whose exchange and
+    all-gather are identities; the group partials still cross the process boundary)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, stage, ghat_mode, q, streamed)) for r in range(2)]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, stage, ghat_mode, q, streamed, groups))
+             for r in range(2)]
     for p in procs:
         p.start()
     got = dict(q.get(timeout=600) for _ in procs)

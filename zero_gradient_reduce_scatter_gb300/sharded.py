@@ -140,6 +140,10 @@ class ShardedZeroOptimizer:
                  bucket with gather_bucket, or into the full buffer with gather_all)
     stream       the stream the initialisation runs on (later calls run on the current
                  stream, which the collectives also follow)
+
+    With one rank per group (M = 1, or G = M) the exchange and the all-gather inside the group
+    are identities and are skipped: the kernels read the gradient where it lies, and the full
+    parameter buffer is the bf16 shard itself.
     """
 
     def __init__(self, numel, stage: int, master_init: torch.Tensor, group=None, bucket_bytes: int = 0,
@@ -194,9 +198,18 @@ class ShardedZeroOptimizer:
         self.param_shards = torch.empty(L, dtype=torch.bfloat16, device=dev)
         if full_params is None:
             full_params = stage < 3
-        self.param_full = torch.empty(npad, dtype=torch.bfloat16, device=dev) if full_params else None
+        # One rank per group (K == 1): the shard is the whole padded layout, lane for lane, so
+        # the group's all-gather is the identity and the full parameters are the shard itself;
+        # and the exchange layout is the gradient's own, so the kernels read the gradient in
+        # place (self._src) and no exchange buffer is kept.
+        self.identity = self.K == 1
+        if self.identity and full_params:
+            self.param_full = self.param_shards
+        else:
+            self.param_full = torch.empty(npad, dtype=torch.bfloat16, device=dev) if full_params else None
         self.scratch = torch.empty(s["bytes_scratch"], dtype=torch.uint8, device=dev)
-        self.recv = torch.empty(npad, dtype=torch.bfloat16, device=dev)
+        self.recv = None if self.identity else torch.empty(npad, dtype=torch.bfloat16, device=dev)
+        self._src = self.recv  # where the kernels read this step's exchanged slices
         P = self.K if self.groups > 1 else self.M
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.sumsq_all = torch.zeros(P, dtype=torch.float64, device=dev)
@@ -248,9 +261,15 @@ class ShardedZeroOptimizer:
             return fn()
 
     def exchange(self, grad: torch.Tensor):
-        """Step 1's collective: this rank's gradient out, its shard's slices in (self.recv)."""
+        """Step 1's collective: this rank's gradient out, its shard's slices in (self.recv).
+        With one rank per group there is nothing to exchange: the step reads grad itself, which
+        must then stay unchanged until the step's kernels have run (stream order)."""
+        if self.identity:
+            self._src = grad
+            return
         self._grouped(lambda: self._collective(
             "exchange", lambda g, r: exchange_gradients(g, r, self.buckets, self.K, self.intra), [grad], [self.recv]))
+        self._src = self.recv
 
     def gather_all(self, dst: torch.Tensor | None = None):
         """The all-gather of every bucket into dst (bf16 [npad], padded; default the full
@@ -258,6 +277,8 @@ class ShardedZeroOptimizer:
         dst = self.param_full if dst is None else dst
         if dst is None:
             raise ValueError("no full parameter buffer: pass dst")
+        if self.identity and dst.data_ptr() == self.param_shards.data_ptr():
+            return  # the full buffer is the shard
         self._grouped(lambda: self._collective(
             "gather", lambda s, f: gather_params(s, f, self.buckets, self.K, self.intra), [self.param_shards], [dst]))
 
@@ -277,6 +298,10 @@ class ShardedZeroOptimizer:
         """Bucket `bucket`'s exchange (as soon as its gradients exist). With the direct
         transport and async_op, returns the collective's work handle: wait() on it makes the
         current stream wait for the exchange."""
+        if self.identity:  # the bucket's slice of grad is already in the exchange layout
+            self._src = grad
+            return None
+        self._src = self.recv
         if async_op and not self._stage_io.host:
             return exchange_gradients(grad, self.recv, self.buckets, self.K, self.intra, [bucket], True)[0]
         off, _n, S, _ = self.buckets[bucket]
@@ -289,11 +314,13 @@ class ShardedZeroOptimizer:
     def step_bucket(self, bucket: int, hyper: Hyper):
         """Bucket `bucket`'s update from its exchanged slices (no clipping): zero_rank_step_bucket.
         The step completes once every bucket has been stepped."""
-        _check(_lib().zero_rank_step_bucket(self._ctx, bucket, self.recv.data_ptr(), self.stage, ctypes.byref(hyper),
+        _check(_lib().zero_rank_step_bucket(self._ctx, bucket, self._src.data_ptr(), self.stage, ctypes.byref(hyper),
                                             _stream_handle(None)), "zero_rank_step_bucket")
 
     def gather_bucket_into_full(self, bucket: int, async_op: bool = False):
         """Bucket `bucket`'s all-gather into the full parameter buffer."""
+        if self.identity and self.param_full is self.param_shards:
+            return None  # the full buffer is the shard
         if async_op and not self._stage_io.host:
             return gather_params(self.param_shards, self.param_full, self.buckets, self.K, self.intra, [bucket],
                                  True)[0]
@@ -326,7 +353,7 @@ class ShardedZeroOptimizer:
             if wk is not None:
                 wk.wait()
             if hyper.clip:
-                _check(lib.zero_rank_reduce_bucket(ctx, b, self.recv.data_ptr(), s), "zero_rank_reduce_bucket")
+                _check(lib.zero_rank_reduce_bucket(ctx, b, self._src.data_ptr(), s), "zero_rank_reduce_bucket")
                 continue
             self.step_bucket(b, hyper)
             if gather and self.param_full is not None:
@@ -405,9 +432,9 @@ class ShardedZeroOptimizer:
         self._check_grad(grad)
         lib, ctx, s = _lib(), self._ctx, _stream_handle(None)
         self.exchange(grad)
-        src = self.recv
+        src = self._src
         if self.groups > 1:  # the group partial, then the G partials of this shard
-            _check(lib.zero_rank_partial(ctx, self.recv.data_ptr(), self.part.data_ptr(), s), "zero_rank_partial")
+            _check(lib.zero_rank_partial(ctx, src.data_ptr(), self.part.data_ptr(), s), "zero_rank_partial")
             self._gather_partials()
             src = self.parts
         sums = None
