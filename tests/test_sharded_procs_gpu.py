@@ -174,10 +174,11 @@ def test_two_processes_on_one_gpu(stage, ghat_mode, streamed, groups):
 
 
 def _nccl_one_rank(q, coalesce):
-    """A job of one rank over NCCL (the only NCCL job one GPU can hold): the collectives run
-    through NCCL, grouped per step or one call per bucket; three clipped steps and three
-    streamed ones, and prefetched per-bucket gathers after each, against the oracle's
-    one-rank step."""
+    """A job of one rank over NCCL (the only NCCL job one GPU can hold), grouped per step or
+    one call per bucket: clipped steps, unclipped streamed ones and clipped streamed ones in
+    turn, and a prefetched per-bucket sweep after each, against the oracle's one-rank step.
+    With one rank the exchange and the all-gather are identities: the kernels read the
+    gradient in place and the parameters are the shard itself."""
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(free_port()))
         import torch
@@ -194,23 +195,33 @@ def _nccl_one_rank(q, coalesce):
         dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
         w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
         mi = W.master_init(w, dev)
-        opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce, full_params=True)
+        opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce, full_params=True,
+                                      ghat_buffer=True)
         assert opt.M == 1 and len(opt.buckets) >= 2
+        assert opt.identity and opt.recv is None and opt.params() is opt.param_shards
         p = O.plan(NUMEL, 1, BUCKET_BYTES)
         st = O.init_state(p, 2, f32(mi))
-        for k in range(6):
-            clip = k < 3
+        for k in range(9):
+            form = k % 3  # 0: clipped step, 1: unclipped streamed, 2: clipped streamed
+            clip = form != 1
             G = _grads_all(p, 1, k)
             mine = torch.from_numpy(G[0].view(np.int16).copy()).to(dev).view(torch.bfloat16)
             h = zg.Hyper(clip=clip, max_grad_norm=0.05)
-            if clip:
+            if form == 0:
                 opt.step(mine, h)
             else:
                 opt.step_streamed(mine, h, order=reversed(range(len(opt.buckets))))
             full, norm, scale, rc = O.zero_step(p, st, G, O.hyper(clip=clip, max_grad_norm=0.05))
-            assert rc == 0
+            assert rc == 0 and (scale < 1.0 or not clip)
+            if clip:
+                gn, _gs = opt.last_norm()
+                assert abs(gn - norm) <= 1e-7 * norm
             assert_state_close(f32(opt.get_state("master")), st.master[0][:p.shard_len], f"step {k} master")
+            assert_state_close(f32(opt.get_state("m")), st.mom[0][:p.shard_len], f"step {k} m")
             assert_state_close(f32(opt.get_state("v")), st.var[0][:p.shard_len], f"step {k} v")
+            if form == 2:  # the clipped streamed step keeps the average: bit-exact
+                assert np.array_equal(f32(opt.get_state("ghat")).view(np.uint32),
+                                      st.ghat[0][:p.shard_len].view(np.uint32))
             assert bf16_ulp_diff(padded_to_unpadded(p, u16(opt.params())), full) <= 1
             uoffs = np.cumsum([0] + [b[1] for b in opt.buckets])
             for b, got in opt.prefetched_buckets(reversed(range(len(opt.buckets))), buffers=3):

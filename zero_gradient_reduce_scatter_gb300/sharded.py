@@ -379,12 +379,20 @@ class ShardedZeroOptimizer:
         transport), each into one of `buffers` transient buffers used in turn. A buffer is
         reused only by a gather issued after the consumer's work on the previous bucket in it
         was queued, and the collective waits for the work queued on the current stream before
-        it starts, so no gather overwrites a buffer still being read."""
+        it starts, so no gather overwrites a buffer still being read.
+
+        With one rank per group there is nothing to gather: each yielded tensor is a view of
+        the bf16 shard itself (read it, do not write it)."""
         order = list(order)
         if not order:
             return
         if buffers < 2:
             raise ValueError("buffers must be at least 2")
+        if self.identity:
+            for b in order:
+                off, n, _S, _ = self.buckets[b]
+                yield b, self.param_shards[off:off + n]
+            return
         cap = self.K * max(self.buckets[b][2] for b in order)
         bufs = [torch.empty(cap, dtype=torch.bfloat16, device=self.device) for _ in range(buffers)]
         works = {}
