@@ -368,8 +368,9 @@ class ShardedZeroOptimizer:
         for wk in gathers:
             if wk is not None:
                 wk.wait()
+        self._src = self.recv  # hold no reference to the caller's gradient
 
-    def prefetched_buckets(self, order, buffers: int = 2):
+    def prefetched_buckets(self, order, buffers: int = 4):
         """ZeRO-3 just-in-time parameters ("CS336 2026 Lecture 8" Slides 24-26; "CS231n Lecture
         11" 4.3: the next block's weights are gathered while the current one computes).
 
@@ -452,6 +453,7 @@ class ShardedZeroOptimizer:
             self._gather_sums()
             sums = self.sumsq_all.data_ptr()
         _check(lib.zero_rank_step(ctx, src.data_ptr(), sums, self.stage, ctypes.byref(hyper), s), "zero_rank_step")
+        self._src = self.recv  # hold no reference to the caller's gradient
         if gather and self.param_full is not None:
             self.gather_all()
 
@@ -494,6 +496,8 @@ class ShardedZeroOptimizer:
         _check(_lib().zero_save_state(self._ctx, out["master"].data_ptr(), out["m"].data_ptr(), out["v"].data_ptr(),
                                       _stream_handle(None)), "zero_save_state")
         for k in ("master", "m", "v"):
+            if self.identity:  # one owner per group: its lanes are the whole state
+                break
             self._collective("state", lambda x: dist.all_reduce(x, group=self.intra), [], [out[k].view(torch.int32)])
         out["t"] = self.t
         return out
