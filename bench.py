@@ -1007,7 +1007,9 @@ def run_shard(args):
             "kernel_timing": "a second pass of the same steps, each kernel launch bracketed by events",
             "frac_of_peak_alg_kernels": round(alg_bytes_per_param(w.M) * L / (kernel_ms / 1e3) / 1e9 / peak, 4),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(dom, f"{args.workload or '4b'}-shard-m{world}")
+                         if not args.max_params else None,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                          "alg_bytes_per_launch": dom_step_bytes / max(dom_launches, 1),
                          "avg_launch_ms": round(dom_ms / max(dom_launches, 1), 4),
@@ -1236,7 +1238,9 @@ def run_shard_emulated(args):
         "roofline": {"bound": "hbm", "kernel": dom + (" (exchange-layout sources)" if G == 1 else " (hybrid rank kernels)"),
                      "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4),
-                     "traffic": None, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": ncu_traffic(dom, f"{args.workload or '4b'}-ranks-m{M}")
+                     if G == 1 and not args.max_params else None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "alg_bytes_per_launch": dom_bytes, "avg_launch_ms": round(dom_ms, 4),
                      "kernel_share": {k: round(v[0] / max(sum(x[0] for x in tot.values()), 1e-9), 4)
                                       for k, v in tot.items() if v[1]}},
