@@ -968,21 +968,32 @@ def run_shard(args):
     kernel_ms = sum(v[0] for v in kt.values()) / args.steps
 
     e2e = None
-    if not args.no_e2e:  # the rank's gradient from pinned host memory in, the parameters out
+    if not args.no_e2e:
+        # the rank's gradient from pinned host memory in (on a copy stream, into two device
+        # buffers in turn, so the next step's copy overlaps this step), the parameters out
         host_g = torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
         host_g.copy_(grad)
         host_p = torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
+        bufs = [grad, opt.new_grad_buffer()]
+        copy_stream = torch.cuda.Stream(device=device)
+        turn = [0]
 
         def e2e_step():
-            grad.copy_(host_g, non_blocking=True)
-            opt.step(grad, h)
-            host_p.copy_(opt.params(), non_blocking=True)
+            opt.step_host_overlapped(host_g, bufs[turn[0] % 2], host_p, h, copy_stream)
+            turn[0] += 1
 
-        e2e_step()
+        for _ in range(2):
+            e2e_step()
         e_ms, _, e_stats = _timed_region(e2e_step, args.e2e_steps, stream, dist, device)
+        gbytes = 2 * opt.sizes["npad"]
+        h2d_gbs = copy_rate([(bufs[0], host_g)], copy_stream)
+        d2h_gbs = copy_rate([(host_p, opt.params())], copy_stream)
         e2e = {"value": n / (e_ms / args.e2e_steps / 1e3), "unit": "params/s", "ms_per_step": e_ms / args.e2e_steps,
-               "ms_per_step_median": e_stats["median"], "call": "ShardedZeroOptimizer.step",
-               "h2d_bytes_per_step": 2 * opt.sizes["npad"] * world, "d2h_bytes_per_step": 2 * opt.sizes["npad"] * world}
+               "ms_per_step_median": e_stats["median"], "call": "ShardedZeroOptimizer.step_host_overlapped",
+               "h2d_bytes_per_step": gbytes * world, "d2h_bytes_per_step": gbytes * world,
+               "h2d_copy_gbs_after": round(h2d_gbs, 1), "d2h_copy_gbs_after": round(d2h_gbs, 1),
+               "copy_floor_ms_after": round(gbytes / min(h2d_gbs, d2h_gbs) / 1e6, 2)}
+        del bufs
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_procs)

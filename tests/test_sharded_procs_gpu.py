@@ -10,7 +10,8 @@ and clipped. Every rank checks itself against the oracle's two-rank step: its sh
 master / m / v (1e-6 relative; bit-identical expected), the averaged gradient bit-exact when
 materialized, the norm within 1e-7 and equal on both ranks, the gathered bf16 parameters within
 1 ulp. Then the assembled checkpoint state equals the oracle's bit for bit, and both ranks
-resume from it in another bucket layout and take one more step as the oracle does.
+resume from it in another bucket layout and take one more step as the oracle does, then three
+steps fed from pinned host memory (step_host_overlapped).
 
 The ranks wait for each other only on the host (gloo), never inside a kernel.
 """
@@ -144,11 +145,42 @@ def _rank_main(rank, world, port, stage, ghat_mode, q, streamed=False, groups=1)
         O.zero_step(p2, st2, G, oh)
         assert_state_close(f32(opt2.get_state("master")), st2.master[rank][:p2.shard_len], "resumed master")
         assert_state_close(f32(opt2.get_state("v")), st2.var[rank][:p2.shard_len], "resumed v")
+        _host_fed_steps(opt2, p2, st2, world, rank, h, oh, dev, range(10, 13))
         opt2.close()
         dist.destroy_process_group()
         q.put((rank, "ok"))
     except BaseException:
         q.put((rank, traceback.format_exc()))
+
+
+def _host_fed_steps(opt, p, st, world, rank, h, oh, dev, steps):
+    """Steps from pinned host gradients (step_host_overlapped, two device buffers in turn, a
+    copy stream), issued with no synchronisation in between, then checked against the oracle:
+    the state, and the parameters copied back to host memory after the last step."""
+    import torch
+
+    import oracle as O
+    from parity_util import assert_state_close, bf16_ulp_diff, f32, u16
+    from rank_util import padded_to_unpadded
+
+    bufs = [opt.new_grad_buffer(), opt.new_grad_buffer()]
+    cs = torch.cuda.Stream(device=dev)
+    keep = opt.param_full is not None
+    host_p = torch.empty(p.npad, dtype=torch.bfloat16).pin_memory() if keep else None
+    hgs = []
+    for i, k in enumerate(steps):
+        G = _grads_all(p, world, k)
+        hgs.append(torch.from_numpy(G[rank].view(np.int16).copy()).view(torch.bfloat16).pin_memory())
+        opt.step_host_overlapped(hgs[-1], bufs[i % 2], host_p, h, cs)
+        full, _norm, _scale, rc = O.zero_step(p, st, G, oh)
+        assert rc == 0
+    torch.cuda.synchronize()
+    assert opt.sync_status() == 0
+    assert_state_close(f32(opt.get_state("master")), st.master[rank][:p.shard_len], "host-fed master")
+    assert_state_close(f32(opt.get_state("m")), st.mom[rank][:p.shard_len], "host-fed m")
+    assert_state_close(f32(opt.get_state("v")), st.var[rank][:p.shard_len], "host-fed v")
+    if keep:
+        assert bf16_ulp_diff(padded_to_unpadded(p, u16(host_p)), full) <= 1
 
 
 @pytest.mark.parametrize("stage,ghat_mode,streamed,groups", [(1, "materialize", False, 1), (3, "recompute", False, 1),
@@ -226,6 +258,8 @@ def _nccl_one_rank(q, coalesce):
             uoffs = np.cumsum([0] + [b[1] for b in opt.buckets])
             for b, got in opt.prefetched_buckets(reversed(range(len(opt.buckets))), buffers=3):
                 assert bf16_ulp_diff(u16(got), full[uoffs[b]:uoffs[b] + opt.buckets[b][1]]) <= 1
+        _host_fed_steps(opt, p, st, 1, 0, zg.Hyper(clip=True, max_grad_norm=0.05),
+                        O.hyper(clip=True, max_grad_norm=0.05), dev, range(20, 23))
         opt.close()
         dist.destroy_process_group()
         q.put("ok")

@@ -210,6 +210,7 @@ class ShardedZeroOptimizer:
         self.scratch = torch.empty(s["bytes_scratch"], dtype=torch.uint8, device=dev)
         self.recv = None if self.identity else torch.empty(npad, dtype=torch.bfloat16, device=dev)
         self._src = self.recv  # where the kernels read this step's exchanged slices
+        self._consumed = {}  # device gradient buffer -> event after the last step that read it
         P = self.K if self.groups > 1 else self.M
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.sumsq_all = torch.zeros(P, dtype=torch.float64, device=dev)
@@ -456,6 +457,47 @@ class ShardedZeroOptimizer:
         self._src = self.recv  # hold no reference to the caller's gradient
         if gather and self.param_full is not None:
             self.gather_all()
+
+    def step_host_overlapped(self, host_grad: torch.Tensor, dev_grad: torch.Tensor, host_params, hyper: Hyper,
+                             copy_stream, gather: bool = True):
+        """One step from this rank's gradient in (pinned) host memory, bf16 [npad] in the padded
+        layout, with the full parameters copied back into host_params (bf16 [npad], padded
+        layout; None: no copy) after it.
+
+        The host-to-device copy runs on `copy_stream` into dev_grad, and the step waits for it.
+        With two device buffers used in turn, the next step's copy overlaps this step's
+        collectives, kernels and parameter copy. A buffer is overwritten only after the last
+        step that read it has run (an event recorded after that step). The parameter copy runs
+        on the current stream, before any later step can rewrite the parameters."""
+        npad = self.sizes["npad"]
+        if host_grad.is_cuda or host_grad.dtype != torch.bfloat16 or host_grad.numel() != npad:
+            raise ValueError(f"host_grad must be a host bf16 tensor of npad={npad}")
+        if host_params is not None:
+            if host_params.is_cuda or host_params.dtype != torch.bfloat16 or host_params.numel() != npad:
+                raise ValueError(f"host_params must be a host bf16 tensor of npad={npad}")
+            if self.param_full is None or not gather:
+                raise ValueError("the parameters are copied back from the full buffer: keep it and gather")
+        self._check_grad(dev_grad)
+        cur = torch.cuda.current_stream(self.device)
+        if copy_stream == cur:
+            raise ValueError("copy_stream must differ from the current stream")
+        key = dev_grad.data_ptr()
+        if key not in self._consumed and len(self._consumed) >= 8:
+            raise ValueError("at most 8 device gradient buffers in turn")
+        last = self._consumed.get(key)
+        if last is not None:
+            copy_stream.wait_event(last)
+        with torch.cuda.stream(copy_stream):
+            dev_grad.copy_(host_grad.reshape(-1), non_blocking=True)
+        landed = torch.cuda.Event()
+        landed.record(copy_stream)
+        cur.wait_event(landed)
+        self.step(dev_grad, hyper, gather=gather)
+        done = torch.cuda.Event()
+        done.record(cur)
+        self._consumed[key] = done
+        if host_params is not None:
+            host_params.reshape(-1).copy_(self.param_full, non_blocking=True)
 
     # -- results and state -------------------------------------------------------------------
     def params(self) -> torch.Tensor:
