@@ -174,13 +174,14 @@ def _host_fed_steps(opt, p, st, world, rank, h, oh, dev, steps):
         opt.step_host_overlapped(hgs[-1], bufs[i % 2], host_p, h, cs)
         full, _norm, _scale, rc = O.zero_step(p, st, G, oh)
         assert rc == 0
+    if keep:  # the parameters reach the host on a stream of their own
+        opt.params_copied.synchronize()
+        assert bf16_ulp_diff(padded_to_unpadded(p, u16(host_p)), full) <= 1
     torch.cuda.synchronize()
     assert opt.sync_status() == 0
     assert_state_close(f32(opt.get_state("master")), st.master[rank][:p.shard_len], "host-fed master")
     assert_state_close(f32(opt.get_state("m")), st.mom[rank][:p.shard_len], "host-fed m")
     assert_state_close(f32(opt.get_state("v")), st.var[rank][:p.shard_len], "host-fed v")
-    if keep:
-        assert bf16_ulp_diff(padded_to_unpadded(p, u16(host_p)), full) <= 1
 
 
 @pytest.mark.parametrize("stage,ghat_mode,streamed,groups", [(1, "materialize", False, 1), (3, "recompute", False, 1),

@@ -211,6 +211,9 @@ class ShardedZeroOptimizer:
         self.recv = None if self.identity else torch.empty(npad, dtype=torch.bfloat16, device=dev)
         self._src = self.recv  # where the kernels read this step's exchanged slices
         self._consumed = {}  # device gradient buffer -> event after the last step that read it
+        self._d2h_stream = None  # parameter copies to host (step_host_overlapped)
+        self._params_out = None  # event after the last of them
+        self._snap = None  # one rank per group: the parameters as of the last host-fed step
         P = self.K if self.groups > 1 else self.M
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.sumsq_all = torch.zeros(P, dtype=torch.float64, device=dev)
@@ -465,10 +468,14 @@ class ShardedZeroOptimizer:
         layout; None: no copy) after it.
 
         The host-to-device copy runs on `copy_stream` into dev_grad, and the step waits for it.
-        With two device buffers used in turn, the next step's copy overlaps this step's
-        collectives, kernels and parameter copy. A buffer is overwritten only after the last
-        step that read it has run (an event recorded after that step). The parameter copy runs
-        on the current stream, before any later step can rewrite the parameters."""
+        With two device buffers used in turn, the next step's copy overlaps this step. A buffer
+        is overwritten only after the last step that read it has run (an event recorded after
+        that step). The parameter copy runs on a stream of its own, beside the next step's
+        collectives and kernels: the next all-gather into the full buffer waits for it. With
+        one rank per group the kernels write the parameters themselves, so they are first
+        copied to a device snapshot (4 B per parameter of HBM traffic), and the copy to host
+        reads that. host_params is valid once `params_copied` has completed (synchronize() on
+        it, or make a stream wait on it)."""
         npad = self.sizes["npad"]
         if host_grad.is_cuda or host_grad.dtype != torch.bfloat16 or host_grad.numel() != npad:
             raise ValueError(f"host_grad must be a host bf16 tensor of npad={npad}")
@@ -492,12 +499,40 @@ class ShardedZeroOptimizer:
         landed = torch.cuda.Event()
         landed.record(copy_stream)
         cur.wait_event(landed)
-        self.step(dev_grad, hyper, gather=gather)
+        prev = self._params_out  # the previous step's copy to host still reads its source
+        if host_params is not None and self.param_full is self.param_shards:
+            self.step(dev_grad, hyper, gather=gather)  # the kernels write the full parameters
+            if self._snap is None:
+                self._snap = torch.empty_like(self.param_shards)
+            if prev is not None:
+                cur.wait_event(prev)
+            self._snap.copy_(self.param_shards)
+            src = self._snap
+        else:
+            self.step(dev_grad, hyper, gather=False)
+            if gather and self.param_full is not None:
+                if prev is not None:
+                    cur.wait_event(prev)  # the all-gather rewrites what that copy reads
+                self.gather_all()
+            src = self.param_full
         done = torch.cuda.Event()
         done.record(cur)
         self._consumed[key] = done
         if host_params is not None:
-            host_params.reshape(-1).copy_(self.param_full, non_blocking=True)
+            if self._d2h_stream is None:
+                self._d2h_stream = torch.cuda.Stream(device=self.device)
+            self._d2h_stream.wait_event(done)
+            with torch.cuda.stream(self._d2h_stream):
+                host_params.reshape(-1).copy_(src, non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(self._d2h_stream)
+            self._params_out = out
+
+    @property
+    def params_copied(self):
+        """The event after the last parameter copy to host of step_host_overlapped (None before
+        the first)."""
+        return self._params_out
 
     # -- results and state -------------------------------------------------------------------
     def params(self) -> torch.Tensor:
