@@ -280,7 +280,11 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  *       would not be). Per bucket, an all-to-all of the bucket's M slices:
  *         recv[off_b + q*S_b + j] = grad_q[off_b + r*S_b + j],   0 <= q < M, 0 <= j < S_b,
  *       i.e. all_to_all_single(recv[off_b : off_b + M*S_b], grad[off_b : off_b + M*S_b])
- *       with equal splits. recv is bf16 [npad] ("the exchange layout").
+ *       with equal splits. recv is bf16 [npad] ("the exchange layout"). With one rank per
+ *       group (M = 1, or K = 1 with hybrid sharding) the rank's own gradient is already in
+ *       the exchange layout and may be passed wherever recv is asked for; the shard is then
+ *       the whole padded layout, lane for lane, so param_full may be the param_shards
+ *       buffer itself and (3) is the identity.
  *   (2) with clipping, one fp64 per rank: each rank's sum of squares of its averaged shard
  *       (zero_rank_sumsq), gathered in rank order into a device array of M doubles on every
  *       rank (all_gather). Every rank then forms the same norm in the same order.

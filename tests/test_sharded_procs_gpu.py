@@ -261,6 +261,25 @@ def _nccl_one_rank(q, coalesce):
                 assert bf16_ulp_diff(u16(got), full[uoffs[b]:uoffs[b] + opt.buckets[b][1]]) <= 1
         _host_fed_steps(opt, p, st, 1, 0, zg.Hyper(clip=True, max_grad_norm=0.05),
                         O.hyper(clip=True, max_grad_norm=0.05), dev, range(20, 23))
+        # argument errors of the host-fed step, each refused before anything is enqueued
+        hg = torch.zeros(p.npad, dtype=torch.bfloat16).pin_memory()
+        hp = torch.zeros(p.npad, dtype=torch.bfloat16).pin_memory()
+        dg = opt.new_grad_buffer()
+        cs = torch.cuda.Stream()
+        bad = [(hg.to(dev), dg, hp, cs),                                   # gradient not on the host
+               (hg[:-1], dg, hp, cs),                                      # wrong length
+               (hg.float(), dg, hp, cs),                                   # wrong type
+               (hg, dg, hp[:-1], cs),                                      # parameters of the wrong length
+               (hg, dg.float(), hp, cs),                                   # device buffer of the wrong type
+               (hg, dg, hp, torch.cuda.current_stream())]                  # copy stream = current stream
+        t0 = opt.t
+        for args in bad:
+            try:
+                opt.step_host_overlapped(*args, zg.Hyper())
+            except ValueError:
+                continue
+            raise AssertionError("accepted a bad argument")
+        assert opt.t == t0
         opt.close()
         dist.destroy_process_group()
         q.put("ok")
