@@ -275,7 +275,7 @@ def _nccl_one_rank(q, coalesce):
         t0 = opt.t
         for args in bad:
             try:
-                opt.step_host_overlapped(*args, zg.Hyper())
+                opt.step_host_overlapped(args[0], args[1], args[2], zg.Hyper(), args[3])
             except ValueError:
                 continue
             raise AssertionError("accepted a bad argument")

@@ -490,7 +490,10 @@ class ShardedZeroOptimizer:
             raise ValueError("copy_stream must differ from the current stream")
         key = dev_grad.data_ptr()
         if key not in self._consumed and len(self._consumed) >= 8:
-            raise ValueError("at most 8 device gradient buffers in turn")
+            # forget buffers whose last reader has finished (nothing to wait for there)
+            self._consumed = {k: e for k, e in self._consumed.items() if not e.query()}
+            if len(self._consumed) >= 8:
+                raise ValueError("at most 8 device gradient buffers in turn")
         last = self._consumed.get(key)
         if last is not None:
             copy_stream.wait_event(last)
