@@ -252,8 +252,9 @@ int zero_step_host(zero_ctx* ctx, const void* const* host_grads, void* const* de
  * copy_stream (a second stream of the caller), the step's kernels and the copy of the
  * parameters back to host_params on `stream`. The library orders them with its own CUDA
  * events: the kernels wait for this call's copies, and a copy into a set of device gradient
- * buffers (identified by dev_grads[0]; at most 8 distinct sets) waits until the previous step
- * that read that set is done. A caller alternating two device sets lets the copies of step
+ * buffers (identified by dev_grads[0]; at most 8 distinct sets whose last step is still
+ * pending: a set whose step has finished is forgotten when a new one needs the room) waits
+ * until the previous step that read that set is done. A caller alternating two device sets lets the copies of step
  * k+1 run while step k computes and returns its parameters; with one set, only the
  * parameter copy overlaps. The host buffers must stay valid, and host_params unread, until
  * `stream` has passed the call. Errors as zero_step_host; INVALID_ARG also when the two

@@ -269,6 +269,31 @@ def test_overlapped_host_steps_equal_device_steps():
     assert torch.equal(a.master, b.master)
 
 
+def test_overlapped_host_steps_forget_finished_sets():
+    """Ten distinct device gradient sets, one per step, all kept alive (distinct addresses):
+    a set whose step has finished is forgotten when a new set needs the room, so the ninth
+    and tenth are accepted, and every step's parameters equal the device path's."""
+    w = W.small_variant(W.workload("4b"), (5000, 77, 130), steps=10)
+    dev = torch.device("cuda")
+    a = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    b = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, dev))
+    h, _ = make_hyper(w)
+    sig = W.sigmas(w)
+    sets = [a.new_grad_buffers() for _ in range(w.steps)]
+    copy_stream = torch.cuda.Stream()
+    out = torch.empty(a.sizes["n"], dtype=torch.bfloat16).pin_memory()
+    for k in range(w.steps):
+        grads = b.new_grad_buffers()
+        for r in range(w.M):
+            W.fill_grads(w, r, k, grads[r], b.tensor_offsets, sig)
+        b.step(grads, h)
+        host = [g.cpu().pin_memory() for g in grads]
+        a.step_host_overlapped(host, sets[k], out, h, copy_stream)
+        torch.cuda.synchronize()
+        assert torch.equal(out, b.params().cpu()), k
+    assert torch.equal(a.master, b.master)
+
+
 def test_step_counter_and_resume():
     """K steps == K1 steps, save (state + t), restore into a fresh context, K2 steps."""
     w = W.small_variant(W.workload("1p3b"), (30000, 5000), steps=4)

@@ -1011,6 +1011,15 @@ int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* 
     zero_ctx::GradSet* set = nullptr;
     for (auto& g : c->grad_sets)
         if (g.key == dev_grads[0]) set = &g;
+    if (!set && c->grad_sets.size() >= 8) {
+        // forget sets whose last reading step has finished: nothing to wait for there
+        std::vector<zero_ctx::GradSet> keep;
+        for (auto& g : c->grad_sets) {
+            if (g.recorded && cudaEventQuery(g.consumed) == cudaSuccess) cudaEventDestroy(g.consumed);
+            else keep.push_back(g);
+        }
+        c->grad_sets.swap(keep);
+    }
     if (!set) {
         if (c->grad_sets.size() >= 8) return ZERO_ERR_INVALID_ARG;  // a handful of buffer sets at most
         zero_ctx::GradSet g{dev_grads[0], nullptr, false};
