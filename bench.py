@@ -968,7 +968,13 @@ def run_shard(args):
     kernel_ms = sum(v[0] for v in kt.values()) / args.steps
 
     e2e = None
-    if not args.no_e2e:
+    # every rank on the node pins its gradient and its parameters (2 B per padded lane each)
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    e2e_fits = local_world * 4 * opt.sizes["npad"] <= 0.6 * host_mem_available()
+    if not args.no_e2e and not e2e_fits:
+        e2e = {"skipped": f"{local_world} ranks x {4 * opt.sizes['npad'] / 1e9:.1f} GB of pinned host memory "
+                          f"would exceed 60% of the host's available memory"}
+    if not args.no_e2e and e2e_fits:
         # the rank's gradient from pinned host memory in (on a copy stream, into two device
         # buffers in turn, so the next step's copy overlaps this step), the parameters out
         host_g = torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
