@@ -501,7 +501,13 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with host buffers (pinned) -----------------------
     e2e = None
-    if not args.no_e2e:
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    one_fits = local_world * (2 * opt.sizes["npad"] + 2 * n) <= 0.6 * host_mem_available()
+    one_fits = max_over_ranks(dist, 0.0 if one_fits else 1.0, device) == 0.0  # all ranks agree
+    if not args.no_e2e and not one_fits:
+        e2e = {"skipped": f"{local_world} ranks x {(2 * opt.sizes['npad'] + 2 * n) / 1e9:.1f} GB of pinned host "
+                          f"memory would exceed 60% of the host's available memory"}
+    if not args.no_e2e and one_fits:
         # Through the public host-buffer call: every step copies the M pinned host gradients in
         # (on a copy stream, into one of two device sets in turn, so step k+1's copies run
         # while step k computes) and copies the bf16 parameters back to pinned host memory.
@@ -509,9 +515,9 @@ def run_ours(args):
         # synchronisations.
         # Host memory: every rank on the node pins its M replicas. When they would not fit,
         # one pinned replica is the source of all M copies (the same bytes move every step).
-        local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
         rep_bytes = 2 * opt.sizes["npad"]
         distinct = local_world * (w.M * rep_bytes + 2 * n) <= 0.6 * host_mem_available()
+        distinct = max_over_ranks(dist, 0.0 if distinct else 1.0, device) == 0.0
         srcs = [torch.empty(opt.sizes["npad"], dtype=torch.bfloat16, pin_memory=True)
                 for _ in range(w.M if distinct else 1)]
         for i, hs in enumerate(srcs):
@@ -971,6 +977,7 @@ def run_shard(args):
     # every rank on the node pins its gradient and its parameters (2 B per padded lane each)
     local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
     e2e_fits = local_world * 4 * opt.sizes["npad"] <= 0.6 * host_mem_available()
+    e2e_fits = max_over_ranks(dist, 0.0 if e2e_fits else 1.0, device) == 0.0  # all ranks agree
     if not args.no_e2e and not e2e_fits:
         e2e = {"skipped": f"{local_world} ranks x {4 * opt.sizes['npad'] / 1e9:.1f} GB of pinned host memory "
                           f"would exceed 60% of the host's available memory"}
