@@ -7,9 +7,13 @@ parameter set (4,092,982,400 params, M = 4, ZeRO-3, clip 1.0).
 
 Prints ONE JSON line (rank 0). Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload tiny|gpt2s|1p3b|ragged|4b] [--impl ours|reference]
-Multi-GPU: launched by torchrun, one process per GPU; every rank runs its own emulated job
-(weak scaling, no data-path collective); the barrier and the max-over-ranks timing use
-torch.distributed.
+Multi-GPU: launched by torchrun, one process per GPU. By default every rank runs its own
+emulated job (weak scaling, no data-path collective); the barrier and the max-over-ranks
+timing use torch.distributed. With --shard the N processes form one job of M = N ranks,
+each holding only its shard, with NCCL collectives between them (strong scaling); with
+--shard --emulate-ranks one process runs every rank's kernels of such a job on one GPU.
+Other modes: --mode stream (ZeRO-2 per-bucket streaming), --mode gather (ZeRO-3 per-bucket
+gathers with prefetch), --graph (captured steps), --impl reference (the CPU oracle).
 """
 from __future__ import annotations
 
@@ -57,8 +61,9 @@ def parse():
                     help="oracle processes for the CPU baseline and the reference arm (0 = one per host core)")
     ap.add_argument("--ghat-mode", default="auto", choices=["auto", "materialize", "recompute"])
     ap.add_argument("--mode", choices=["step", "stream", "gather"], default="step",
-                    help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket reduce-scatter "
-                         "then one update; gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
+                    help="step: the fused ZeRO step (default); stream: ZeRO-2 per-bucket streaming (one fused "
+                         "pass per bucket, or every bucket's reduce-scatter then one update: --stream-form); "
+                         "gather: ZeRO-3 per-bucket parameter all-gather with prefetch")
     ap.add_argument("--emulate-ranks", action="store_true",
                     help="with --shard on one GPU: the workload's M ranks as M rank contexts in this one process, "
                          "each holding only its shard, with device copies in place of the collectives (timed "
