@@ -206,12 +206,13 @@ def test_two_processes_on_one_gpu(stage, ghat_mode, streamed, groups):
     assert all(p.exitcode == 0 for p in procs)
 
 
-def _nccl_one_rank(q, coalesce):
-    """A job of one rank over NCCL (the only NCCL job one GPU can hold), grouped per step or
-    one call per bucket: clipped steps, unclipped streamed ones and clipped streamed ones in
-    turn, and a prefetched per-bucket sweep after each, against the oracle's one-rank step.
-    With one rank the exchange and the all-gather are identities: the kernels read the
-    gradient in place and the parameters are the shard itself."""
+def _nccl_one_rank(q, coalesce, identity):
+    """A job of one rank over NCCL (the only NCCL job one GPU can hold): clipped steps,
+    unclipped streamed ones and clipped streamed ones in turn, and a prefetched per-bucket
+    sweep after each, against the oracle's one-rank step. identity: the exchange and the
+    all-gather of one rank are skipped (the kernels read the gradient in place, the parameters
+    are the shard itself); otherwise they run as NCCL collectives, grouped per step or one
+    call per bucket (coalesce)."""
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(free_port()))
         import torch
@@ -229,9 +230,10 @@ def _nccl_one_rank(q, coalesce):
         w = W.small_variant(W.workload("tiny"), NUMEL, steps=3)
         mi = W.master_init(w, dev)
         opt = zg.ShardedZeroOptimizer(NUMEL, 2, mi, bucket_bytes=BUCKET_BYTES, coalesce=coalesce, full_params=True,
-                                      ghat_buffer=True)
+                                      ghat_buffer=True, skip_identity=identity)
         assert opt.M == 1 and len(opt.buckets) >= 2
-        assert opt.identity and opt.recv is None and opt.params() is opt.param_shards
+        assert opt.identity == identity
+        assert (opt.recv is None and opt.params() is opt.param_shards) == identity
         p = O.plan(NUMEL, 1, BUCKET_BYTES)
         st = O.init_state(p, 2, f32(mi))
         for k in range(9):
@@ -287,11 +289,11 @@ def _nccl_one_rank(q, coalesce):
         q.put(traceback.format_exc())
 
 
-@pytest.mark.parametrize("coalesce", [True, False])
-def test_nccl_one_rank_job(coalesce):
+@pytest.mark.parametrize("coalesce,identity", [(True, True), (True, False), (False, False)])
+def test_nccl_one_rank_job(coalesce, identity):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    proc = ctx.Process(target=_nccl_one_rank, args=(q, coalesce))
+    proc = ctx.Process(target=_nccl_one_rank, args=(q, coalesce, identity))
     proc.start()
     got = q.get(timeout=600)
     proc.join(timeout=120)

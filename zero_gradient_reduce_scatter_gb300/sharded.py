@@ -140,15 +140,17 @@ class ShardedZeroOptimizer:
                  bucket with gather_bucket, or into the full buffer with gather_all)
     stream       the stream the initialisation runs on (later calls run on the current
                  stream, which the collectives also follow)
-
-    With one rank per group (M = 1, or G = M) the exchange and the all-gather inside the group
-    are identities and are skipped: the kernels read the gradient where it lies, and the full
-    parameter buffer is the bf16 shard itself.
+    skip_identity  with one rank per group (M = 1, or G = M) the exchange and the all-gather
+                 inside the group are identities and are skipped (default): the kernels read
+                 the gradient where it lies, and the full parameter buffer is the bf16 shard
+                 itself. False runs them as collectives all the same (the one-GPU test of the
+                 collective path).
     """
 
     def __init__(self, numel, stage: int, master_init: torch.Tensor, group=None, bucket_bytes: int = 0,
                  groups: int = 1, ghat_buffer: bool | None = None, transport: str = "direct",
-                 full_params: bool | None = None, stream=None, coalesce: bool = True):
+                 full_params: bool | None = None, stream=None, coalesce: bool = True,
+                 skip_identity: bool = True):
         import torch.distributed as dist
         if not (isinstance(master_init, torch.Tensor) and master_init.is_cuda and master_init.dtype == torch.float32):
             raise TypeError("master_init must be a CUDA float32 tensor of the unpadded parameters")
@@ -202,7 +204,7 @@ class ShardedZeroOptimizer:
         # the group's all-gather is the identity and the full parameters are the shard itself;
         # and the exchange layout is the gradient's own, so the kernels read the gradient in
         # place (self._src) and no exchange buffer is kept.
-        self.identity = self.K == 1
+        self.identity = self.K == 1 and bool(skip_identity)
         if self.identity and full_params:
             self.param_full = self.param_shards
         else:
