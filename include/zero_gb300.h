@@ -496,7 +496,8 @@ int zero_set_step(zero_ctx* ctx, int64_t t);
 int zero_set_timing(zero_ctx* ctx, int on);
 int zero_kernel_times(zero_ctx* ctx, double* ms, int64_t* launches);
 
-/* Launch configuration of the streaming kernels: CTAs in the grid and threads per CTA. */
+/* Launch configuration of the fused step kernel: CTAs in the grid and threads per CTA as
+ * launched (fewer threads with one source, M = 1). */
 int zero_launch_shape(zero_ctx* ctx, int* ctas, int* threads);
 
 /* Caps the grid of every streaming kernel at `ctas` CTAs (0 = no cap, the default: as many

@@ -1507,7 +1507,7 @@ int zero_set_max_ctas(zero_ctx* c, int ctas) {
 int zero_launch_shape(zero_ctx* c, int* ctas, int* threads) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (ctas) *ctas = grid_for(c, zg::kVarRsAdamwPlain, c->npad / 8);
-    if (threads) *threads = zg::variant_threads(zg::kVarRsAdamwPlain);
+    if (threads) *threads = zg::rs_adamw_threads(c->cfg.M);  // as launched
     return ZERO_OK;
 }
 

@@ -106,6 +106,11 @@ enum LoadPath : int {
 constexpr int kThreadsRsNormOnly = 1024;   // norm pass, averaged gradient kept in registers
 constexpr int kThreadsRsNormWrite = 256;  // norm pass that also writes the averaged gradient
 constexpr int kThreadsRsAdamw = 512;
+// The one-source fused kernel (M = 1) launches fewer threads into the same one CTA per SM:
+// 14 warps per SM ran it at 96-98% of the copy peak against 92-94% with 16, and 12, 10 and
+// 24 warps were slower again (A/B runs on one box each); with more sources 14 warps lost.
+constexpr int kThreadsRsAdamwOne = 448;
+constexpr int rs_adamw_threads(int M) { return M == 1 ? kThreadsRsAdamwOne : kThreadsRsAdamw; }
 constexpr int kThreadsAdamw = 512;
 constexpr int kThreadsGather = 256;
 constexpr int kThreadsInit = 256;

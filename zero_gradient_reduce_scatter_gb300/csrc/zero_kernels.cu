@@ -644,8 +644,11 @@ __global__ void __launch_bounds__(kThreadsRsAdamw) k_rs_adamw(const StepArgs a) 
     // (with plain state accesses the clipped M = 4 kernel ran 1.7% faster this way than when
     // it read them where they are used)
     const AdamConsts k = SCHED ? a.status->cur : a.k;
-    const int64_t stride = (int64_t)gridDim.x * kThreadsRsAdamw;
-    int64_t vi = a.vbeg + (int64_t)blockIdx.x * kThreadsRsAdamw + threadIdx.x;
+    // the launched block size, rs_adamw_threads(M): only the one-source instance (MT = 1) is
+    // launched for M = 1 (ByM), and it takes fewer threads
+    constexpr int kT = MT == 1 ? kThreadsRsAdamwOne : kThreadsRsAdamw;
+    const int64_t stride = (int64_t)gridDim.x * kT;
+    int64_t vi = a.vbeg + (int64_t)blockIdx.x * kT + threadIdx.x;
     if (vi >= a.vend) return;
     Cursor c;
     c.init(a.buckets, a.nb, vi * 8, a.b_first, a.b_end);
@@ -1040,8 +1043,9 @@ cudaError_t launch_rs_norm_exchange(const StepArgs& a, bool write_ghat, int grid
 }
 
 cudaError_t launch_rs_adamw_exchange(const StepArgs& a, bool apply_scale, int grid, cudaStream_t s) {
-    if (apply_scale) ByM<RsAdamwScaledX>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
-    else ByM<RsAdamwPlainX>::get(a.M)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+    const int threads = rs_adamw_threads(a.M);
+    if (apply_scale) ByM<RsAdamwScaledX>::get(a.M)<<<grid, threads, 0, s>>>(a);
+    else ByM<RsAdamwPlainX>::get(a.M)<<<grid, threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -1074,15 +1078,16 @@ cudaError_t launch_adamw(const StepArgs& a, bool sched, int grid, cudaStream_t s
 }
 
 cudaError_t launch_rs_adamw(const StepArgs& a, bool apply_scale, bool sched, int grid, cudaStream_t s) {
+    const int threads = rs_adamw_threads(a.M);
     if (sched) {
-        if (apply_scale) ByM<RsAdamwScaledSched>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
-        else ByM<RsAdamwPlainSched>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+        if (apply_scale) ByM<RsAdamwScaledSched>::get(a.M, a.groups)<<<grid, threads, 0, s>>>(a);
+        else ByM<RsAdamwPlainSched>::get(a.M, a.groups)<<<grid, threads, 0, s>>>(a);
     } else if (apply_scale) {
-        ByM<RsAdamwScaled>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+        ByM<RsAdamwScaled>::get(a.M, a.groups)<<<grid, threads, 0, s>>>(a);
     } else if (a.pdl != kPdlNone) {
-        return launch_pdl(ByM<RsAdamwPlainPdl>::get(a.M, a.groups), grid, kThreadsRsAdamw, s, a);
+        return launch_pdl(ByM<RsAdamwPlainPdl>::get(a.M, a.groups), grid, threads, s, a);
     } else {
-        ByM<RsAdamwPlain>::get(a.M, a.groups)<<<grid, kThreadsRsAdamw, 0, s>>>(a);
+        ByM<RsAdamwPlain>::get(a.M, a.groups)<<<grid, threads, 0, s>>>(a);
     }
     return cudaGetLastError();
 }
