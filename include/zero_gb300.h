@@ -57,7 +57,10 @@ extern "C" {
 
 /* ---- status codes ------------------------------------------------------------------- */
 #define ZERO_OK                 0
-#define ZERO_ERR_INVALID_ARG   -1  /* null pointer, out-of-range value, bad enum        */
+#define ZERO_ERR_INVALID_ARG   -1  /* null pointer, out-of-range value, bad enum; a
+                                      pointer that the kernels would use which is not
+                                      device memory of the context's GPU (or managed
+                                      memory): host memory is refused, never dereferenced */
 #define ZERO_ERR_MISALIGNED    -2  /* a device pointer is not 16-byte aligned           */
 #define ZERO_ERR_SIZE_MISMATCH -3  /* a required buffer is missing for this config       */
 #define ZERO_ERR_STAGE         -4  /* stage not 1/2/3, or not the context's stage        */

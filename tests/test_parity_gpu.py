@@ -194,6 +194,36 @@ def test_invalid_step_arguments_rejected_on_host():
     assert lib.zero_destroy(raw) == -7
 
 
+def test_host_memory_pointers_refused():
+    """Host memory, pinned or pageable, where a call wants this GPU's memory (a gradient, a
+    state output or input) is refused with INVALID_ARG before anything is enqueued, and the
+    context keeps working."""
+    import ctypes
+    w = W.small_variant(W.workload("tiny"), (4096,), steps=1)
+    opt = zg.ZeroOptimizer(w.numel, w.M, w.stage, W.master_init(w, torch.device("cuda")))
+    grads = opt.new_grad_buffers()
+    h, _ = make_hyper(w)
+    t0 = opt.t
+    lib, s = zg._lib(), zg._stream_handle(None)
+    for host in (torch.zeros(opt.sizes["npad"], dtype=torch.bfloat16).pin_memory(),
+                 torch.zeros(opt.sizes["npad"], dtype=torch.bfloat16)):
+        with pytest.raises(ValueError):  # the binding refuses it first
+            opt.step([grads[0], host], h)
+        ptrs = (ctypes.c_void_p * w.M)(grads[0].data_ptr(), host.data_ptr())
+        assert lib.zero_step(opt._ctx, ctypes.cast(ptrs, ctypes.c_void_p), w.stage, ctypes.byref(h), s) == -1
+    out = torch.zeros(opt.sizes["n"], dtype=torch.float32).pin_memory()
+    assert lib.zero_save_state(opt._ctx, out.data_ptr(), None, None, s) == -1
+    assert lib.zero_load_state(opt._ctx, out.data_ptr(), None, None, 0, s) == -1
+    assert lib.zero_get_state(opt._ctx, 0, 0, out.data_ptr(), s) == -1
+    bufs = (ctypes.c_void_p * w.M)(grads[0].data_ptr(), out.data_ptr())
+    assert lib.zero_step_host(opt._ctx, ctypes.cast(bufs, ctypes.c_void_p), ctypes.cast(bufs, ctypes.c_void_p),
+                              w.stage, ctypes.byref(h), out.data_ptr(), s) == -1
+    opt.step(grads, h)
+    torch.cuda.synchronize()
+    assert opt.t == t0 + 1 and opt.sync_status() == 0
+    opt.close()
+
+
 # ------------------------------------------------------------------------------------------
 # Other entry points: per-rank state, per-bucket gather, host-buffer step, step counter
 # ------------------------------------------------------------------------------------------

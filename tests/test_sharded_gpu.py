@@ -190,6 +190,12 @@ def test_sharded_argument_errors():
     assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr(), None, 2, ctypes.byref(zg.Hyper()), s) == -4  # stage
     assert lib.zero_rank_partial(rc.ctx, rc.recv.data_ptr(), rc.master.data_ptr(), s) == -1  # not hybrid
     assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr() + 2, None, 1, ctypes.byref(zg.Hyper()), s) == -2
+    # host memory where the kernels would read or write: refused before any launch
+    host = torch.zeros(rc.recv.numel(), dtype=torch.bfloat16).pin_memory()
+    assert lib.zero_rank_step(rc.ctx, host.data_ptr(), None, 1, ctypes.byref(zg.Hyper()), s) == -1
+    assert lib.zero_rank_step_bucket(rc.ctx, 0, host.data_ptr(), 1, ctypes.byref(zg.Hyper()), s) == -1
+    hsum = torch.zeros(2, dtype=torch.float64).pin_memory()
+    assert lib.zero_rank_sumsq(rc.ctx, rc.recv.data_ptr(), ctypes.byref(h), hsum.data_ptr(), s) == -1
     # the emulated mode's calls refuse a rank context, and the rank calls an emulated one
     ptrs = (ctypes.c_void_p * 2)(rc.recv.data_ptr(), rc.recv.data_ptr())
     assert lib.zero_step(rc.ctx, ctypes.cast(ptrs, ctypes.c_void_p), 1, ctypes.byref(zg.Hyper()), s) == -1

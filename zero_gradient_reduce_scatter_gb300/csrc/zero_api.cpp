@@ -31,6 +31,8 @@ struct zero_ctx {
     int64_t npad, n, shard_len;
     // borrowed device buffers
     zero_buffers bufs;
+    // pointers passed to later calls that were found to be this GPU's memory (dev_ptr_ok)
+    mutable std::unordered_set<uintptr_t> dev_ok;
     zg::Status* status;
     double* partials;
     zg::Bucket* dev_buckets;
@@ -571,11 +573,32 @@ static int resolve_ghat_mode(const zero_ctx* c, const zero_hyper* h, int* mode) 
     return ZERO_OK;
 }
 
+// A pointer that a call hands to the context's kernels: device memory of the context's GPU,
+// or managed memory. Checked with cudaPointerGetAttributes once per pointer value, then
+// remembered, so that steps over the same buffers pay a set lookup. A host pointer, or one
+// of another GPU, is refused (INVALID_ARG) instead of faulting in a kernel.
+static bool dev_ptr_ok(const zero_ctx* c, const void* p) {
+    const uintptr_t key = (uintptr_t)p;
+    if (c->dev_ok.count(key)) return true;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();  // the non-sticky error of an unknown pointer
+        return false;
+    }
+    const bool ok = attr.type == cudaMemoryTypeManaged ||
+                    (attr.type == cudaMemoryTypeDevice && attr.device == c->device);
+    if (!ok) return false;
+    if (c->dev_ok.size() >= 4096) c->dev_ok.clear();
+    c->dev_ok.insert(key);
+    return true;
+}
+
 static int check_grads(const zero_ctx* c, const void* const* grads) {
     if (!grads) return ZERO_ERR_INVALID_ARG;
     for (int r = 0; r < c->cfg.M; ++r) {
         if (!grads[r]) return ZERO_ERR_INVALID_ARG;
         if (!aligned16(grads[r])) return ZERO_ERR_MISALIGNED;
+        if (!dev_ptr_ok(c, grads[r])) return ZERO_ERR_INVALID_ARG;
     }
     return ZERO_OK;
 }
@@ -678,6 +701,7 @@ int zero_reduce_bucket(zero_ctx* c, int64_t bucket, const void* const* grads_b, 
     for (int r = 0; r < c->cfg.M; ++r) {
         if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
         if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
+        if (!dev_ptr_ok(c, grads_b[r])) return ZERO_ERR_INVALID_ARG;
     }
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
@@ -775,6 +799,7 @@ static int check_step_bucket(const zero_ctx* c, int64_t bucket, const void* cons
     for (int r = 0; r < c->cfg.M; ++r) {
         if (!grads_b[r]) return ZERO_ERR_INVALID_ARG;
         if (!aligned16(grads_b[r])) return ZERO_ERR_MISALIGNED;
+        if (!dev_ptr_ok(c, grads_b[r])) return ZERO_ERR_INVALID_ARG;
     }
     return ZERO_OK;
 }
@@ -936,6 +961,7 @@ int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     int rc = check_hyper(h);
     if (rc) return rc;
+    if ((rc = check_grads(c, (const void* const*)dev_grads))) return rc;  // before any copy
     DeviceGuard guard(c->device);
     ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
@@ -954,6 +980,8 @@ int zero_step_host(zero_ctx* c, const void* const* host_grads, void* const* dev_
 int zero_save_state(zero_ctx* c, void* master, void* m, void* v, void* stream) {
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (!master && !m && !v) return ZERO_ERR_INVALID_ARG;
+    for (const void* p : {(const void*)master, (const void*)m, (const void*)v})
+        if (p && !dev_ptr_ok(c, p)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
@@ -972,6 +1000,8 @@ int zero_load_state(zero_ctx* c, const void* master, const void* m, const void* 
     if (!live(c)) return ZERO_ERR_BAD_CONTEXT;
     if (c->sched_active) return ZERO_ERR_SCHEDULE;
     if (!master || t < 0) return ZERO_ERR_INVALID_ARG;
+    for (const void* p : {master, m, v})
+        if (p && !dev_ptr_ok(c, p)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
@@ -999,6 +1029,7 @@ int zero_step_host_overlapped(zero_ctx* c, const void* const* host_grads, void* 
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     int rc = check_hyper(h);
     if (rc) return rc;
+    if ((rc = check_grads(c, (const void* const*)dev_grads))) return rc;  // before any copy
     DeviceGuard guard(c->device);
     ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
@@ -1104,6 +1135,7 @@ int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
     if (rc) return rc;
     if (!hybrid(c) || !recv || !part) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(recv) || !aligned16(part)) return ZERO_ERR_MISALIGNED;
+    if (!dev_ptr_ok(c, recv) || !dev_ptr_ok(c, part)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
@@ -1131,6 +1163,7 @@ int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* s
     if ((rc = check_hyper(h))) return rc;
     if (!h->clip || !sumsq) return ZERO_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(sumsq) & 7u) return ZERO_ERR_MISALIGNED;
+    if (!dev_ptr_ok(c, sumsq)) return ZERO_ERR_INVALID_ARG;
     const int64_t nb = (int64_t)c->buckets.size();
     if (!src) {  // every bucket reduced by zero_rank_reduce_bucket: the sum of their sums
         if (c->n_reduced != nb) return ZERO_ERR_INVALID_ARG;
@@ -1196,6 +1229,7 @@ int zero_rank_step(zero_ctx* c, const void* src, const double* sumsq_all, int st
     if (!from_ghat && !src) return ZERO_ERR_INVALID_ARG;
     if (src && !aligned16(src)) return ZERO_ERR_MISALIGNED;
     if (clip && (reinterpret_cast<uintptr_t>(sumsq_all) & 7u)) return ZERO_ERR_MISALIGNED;
+    if ((src && !dev_ptr_ok(c, src)) || (clip && !dev_ptr_ok(c, sumsq_all))) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
@@ -1241,6 +1275,7 @@ int zero_rank_reduce_bucket(zero_ctx* c, int64_t bucket, const void* src, void* 
     if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
     if (c->n_bucket_done || c->rank_reduced) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
+    if (!dev_ptr_ok(c, src)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
@@ -1275,6 +1310,7 @@ int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stag
     if (h->clip || hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
     if (c->rank_reduced || c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
+    if (!dev_ptr_ok(c, src)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
@@ -1315,6 +1351,7 @@ int zero_gather(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     const int64_t nb = (int64_t)c->buckets.size();
     if (bucket < -1 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
     if (dst && !aligned16(dst)) return ZERO_ERR_MISALIGNED;
+    if (dst && !dev_ptr_ok(c, dst)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     uint16_t* out = (uint16_t*)(dst ? dst : c->bufs.param_full);
@@ -1333,6 +1370,7 @@ int zero_gather_bucket(zero_ctx* c, int64_t bucket, void* dst, void* stream) {
     if (c->cfg.gather != ZERO_GATHER_SHARDS || !dst) return ZERO_ERR_INVALID_ARG;
     if (bucket < 0 || bucket >= (int64_t)c->buckets.size()) return ZERO_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(dst) & 1u) return ZERO_ERR_MISALIGNED;
+    if (!dev_ptr_ok(c, dst)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     const zg::Bucket& e = c->buckets[(size_t)bucket];
@@ -1359,6 +1397,7 @@ int zero_get_state(zero_ctx* c, int which, int rank, void* dst, void* stream) {
         default: return ZERO_ERR_INVALID_ARG;
     }
     if (!src) return ZERO_ERR_SIZE_MISMATCH;
+    if (!dev_ptr_ok(c, dst)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
     ++c->seq;  // enqueues stream work: no later per-bucket launch overlaps what came before
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
