@@ -345,16 +345,18 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
 int zero_rank_step(zero_ctx* ctx, const void* src, const double* sumsq_all, int stage,
                    const zero_hyper* hyper, void* stream);
 
-/* Per-bucket form of zero_rank_step without clipping (flat mode): the update of bucket
- * `bucket`'s slice of this rank's shard, from src (the exchange buffer; only the bucket's
- * region, lanes [off_b, off_b + M*S_b), is read, so the call may follow that bucket's
- * all-to-all while later buckets are still in flight: the ZeRO-2 pattern of reducing each
- * bucket as soon as its gradients exist, "CS336 2026 Lecture 8" Slide 23, "并行训练优化、
- * MoE扩展与系统瓶颈" 2.2.4). Every bucket takes step t + 1; the step is complete, and t
- * advances, once every bucket has been stepped, in any order. Until then zero_rank_step,
- * zero_rank_sumsq and a second call for the same bucket return INVALID_ARG.
- * Errors: BAD_CONTEXT, INVALID_ARG (not a flat sharded context, clipping, bad bucket),
- * STAGE, MISALIGNED, CUDA. */
+/* Per-bucket form of zero_rank_step without clipping: the update of bucket `bucket`'s slice
+ * of this rank's shard, from src, of which only the bucket's region is read. Flat mode: src
+ * is the exchange buffer (the region is lanes [off_b, off_b + M*S_b)). Hybrid mode: src is
+ * the gathered group partials, fp32 [G * shard_len] as for zero_rank_step (the region is
+ * lanes [grp * shard_len + base_b, +S_b) of each group grp). So the call may follow that
+ * bucket's collectives while later buckets are still in flight: the ZeRO-2 pattern of
+ * reducing each bucket as soon as its gradients exist ("CS336 2026 Lecture 8" Slide 23;
+ * "并行训练优化、MoE扩展与系统瓶颈" 2.2.4). Every bucket takes step t + 1; the step is
+ * complete, and t advances, once every bucket has been stepped, in any order. Until then
+ * zero_rank_step, zero_rank_sumsq and a second call for the same bucket return INVALID_ARG.
+ * Errors: BAD_CONTEXT, INVALID_ARG (not a sharded context, clipping, bad bucket), STAGE,
+ * MISALIGNED, CUDA. */
 int zero_rank_step_bucket(zero_ctx* ctx, int64_t bucket, const void* src, int stage,
                           const zero_hyper* hyper, void* stream);
 
@@ -362,17 +364,18 @@ int zero_rank_step_bucket(zero_ctx* ctx, int64_t bucket, const void* src, int st
  * the fp64 sum of squares over its real lanes to *sumsq (device, 8-byte aligned). Under
  * ZERO_GHAT_MATERIALIZE (or AUTO choosing it) the fp32 average also goes to the ghat buffer,
  * and zero_rank_step reads it instead of src. hyper->clip must be 1.
- * src NULL (flat mode, after zero_rank_reduce_bucket of every bucket): *sumsq = the sum of the
- * buckets' sums, and zero_rank_step then updates from the ghat buffer (materialized form).
+ * src NULL (after zero_rank_reduce_bucket of every bucket): *sumsq = the sum of the buckets'
+ * sums, and zero_rank_step then updates from the ghat buffer (materialized form).
  * Errors: BAD_CONTEXT, INVALID_ARG (also: src NULL before every bucket was reduced, or src
  * given while some were), MISALIGNED, SIZE_MISMATCH, CUDA. */
 int zero_rank_sumsq(zero_ctx* ctx, const void* src, const zero_hyper* hyper, double* sumsq,
                     void* stream);
 
-/* Clipped ZeRO-2 streaming (flat mode): reduces bucket `bucket`'s slice of this rank's shard
- * from src (the exchange buffer; only the bucket's region is read) as soon as its all-to-all
- * has landed: the average into the ghat buffer (required) and the bucket's sum of squares
- * kept by the context. Once every bucket is reduced, zero_rank_sumsq(src = NULL) gives the
+/* Clipped ZeRO-2 streaming: reduces bucket `bucket`'s slice of this rank's shard from src
+ * (as for zero_rank_step_bucket: the exchange buffer, or in hybrid mode the gathered group
+ * partials; only the bucket's region is read) as soon as its collectives have landed: the
+ * average into the ghat buffer (required) and the bucket's sum of squares kept by the
+ * context. Once every bucket is reduced, zero_rank_sumsq(src = NULL) gives the
  * rank's sum for the all-gather of sums, and zero_rank_step(src = NULL, sums) updates the
  * shard from the ghat buffer ("CS336 2026 Lecture 8" Slide 23; "并行训练优化、MoE扩展与系统
  * 瓶颈" 2.2.4: each bucket is reduce-scattered as its gradients appear; clipping needs every
@@ -385,6 +388,12 @@ int zero_rank_reduce_bucket(zero_ctx* ctx, int64_t bucket, const void* src, void
  * recv (bf16 [npad], the exchange layout of this rank's group) into part (fp32 [shard_len]).
  * Errors: BAD_CONTEXT, INVALID_ARG (not a hybrid sharded context), MISALIGNED, CUDA. */
 int zero_rank_partial(zero_ctx* ctx, const void* recv, void* part, void* stream);
+
+/* Hybrid mode, per bucket: the group partial of bucket `bucket`'s slice only (local lanes
+ * [base_b, base_b + S_b) of part, from the bucket's region of recv), so that a bucket's
+ * partial can cross the groups while later buckets are still being exchanged. Arguments and
+ * errors as zero_rank_partial; INVALID_ARG also for a bucket outside [0, n_buckets). */
+int zero_rank_partial_bucket(zero_ctx* ctx, int64_t bucket, const void* recv, void* part, void* stream);
 
 /* Steps whose scalars live on the device, for capture in a CUDA graph. The pages define no
  * interface for this. It serves training loops that capture whole steps as CUDA graphs and

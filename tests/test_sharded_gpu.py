@@ -189,6 +189,7 @@ def test_sharded_argument_errors():
     assert lib.zero_rank_sumsq(rc.ctx, rc.recv.data_ptr(), ctypes.byref(zg.Hyper()), rc.sumsq.data_ptr(), s) == -1
     assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr(), None, 2, ctypes.byref(zg.Hyper()), s) == -4  # stage
     assert lib.zero_rank_partial(rc.ctx, rc.recv.data_ptr(), rc.master.data_ptr(), s) == -1  # not hybrid
+    assert lib.zero_rank_partial_bucket(rc.ctx, 0, rc.recv.data_ptr(), rc.master.data_ptr(), s) == -1
     assert lib.zero_rank_step(rc.ctx, rc.recv.data_ptr() + 2, None, 1, ctypes.byref(zg.Hyper()), s) == -2
     # host memory where the kernels would read or write: refused before any launch
     host = torch.zeros(rc.recv.numel(), dtype=torch.bfloat16).pin_memory()
@@ -292,6 +293,77 @@ def test_sharded_largest_rank_count():
     # 64 ranks: the generic (runtime M) kernels; most ranks own a few real lanes per bucket
     # (the average over 64 ranks is small: a lower threshold keeps the clip scale in play)
     for rc in _run((3001, 1000, 37, 4099), 64, 3, True, bucket_bytes=6000, steps=2, max_norm=0.01)[0]:
+        rc.close()
+
+
+@pytest.mark.parametrize("groups,M,stage,clip", [(2, 4, 2, False), (4, 8, 1, False), (4, 4, 2, False),
+                                                  (2, 8, 3, True), (2, 4, 1, True)])
+def test_sharded_hybrid_streamed_per_bucket(groups, M, stage, clip):
+    """Hybrid sharding streamed bucket by bucket, buckets in reverse order. Per bucket: the
+    group partial of that bucket only (zero_rank_partial_bucket), the cross-group gather of
+    that bucket's region only, then the bucket's update (unclipped, zero_rank_step_bucket) or
+    its reduction into ghat (clipped, zero_rank_reduce_bucket; then the rank's sum from the
+    buckets' sums, the gathered sums and one update from the average). Against the oracle's
+    hybrid step: the state within 1e-6 (bit-identical expected unclipped), the average
+    bit-exact, the norm within 1e-7 and equal on every rank, the parameters within 1 ulp.
+    G = M (one rank per group) included."""
+    dev = torch.device("cuda")
+    K = M // groups
+    p = O.plan(RAGGED, K, 4096)
+    assert p.nb > 3
+    w = W.small_variant(W.workload("tiny"), tuple(RAGGED), steps=2)
+    mi = W.master_init(w, dev)
+    ranks = [RankCtx(RAGGED, M, r, stage, mi, 4096, groups) for r in range(M)]
+    st = O.init_state(p, stage, f32(mi), groups=groups)
+    h = zg.Hyper(clip=clip, max_grad_norm=0.05)
+    oh = O.hyper(clip=clip, max_grad_norm=0.05)
+    lib, s = zg._lib(), zg._stream_handle(None)
+    from rank_util import loopback_exchange, loopback_gather, loopback_sums
+    L = p.shard_len
+    bases = np.concatenate([[0], np.cumsum(p.b_S)[:-1]])
+    for k in range(2):
+        grads = _grads(p, M, k, dev)
+        loopback_exchange(ranks, grads)
+        for b in reversed(range(p.nb)):
+            base, S = int(bases[b]), int(p.b_S[b])
+            for rc in ranks:
+                assert lib.zero_rank_partial_bucket(rc.ctx, b, rc.recv.data_ptr(), rc.part.data_ptr(), s) == 0
+            for rc in ranks:  # this bucket's region of every group's partial of this rank's shard
+                for g in range(groups):
+                    rc.parts[g * L + base:g * L + base + S].copy_(ranks[g * K + rc.owner].part[base:base + S])
+            for rc in ranks:
+                if clip:
+                    assert lib.zero_rank_reduce_bucket(rc.ctx, b, rc.parts.data_ptr(), s) == 0
+                else:
+                    assert lib.zero_rank_step_bucket(rc.ctx, b, rc.parts.data_ptr(), stage, ctypes.byref(h), s) == 0
+        if clip:
+            for rc in ranks:
+                assert lib.zero_rank_sumsq(rc.ctx, None, ctypes.byref(h), rc.sumsq.data_ptr(), s) == 0
+            loopback_sums(ranks)
+            for rc in ranks:
+                assert lib.zero_rank_step(rc.ctx, None, rc.sums.data_ptr(), stage, ctypes.byref(h), s) == 0
+        loopback_gather(ranks)
+        full, norm, scale, rc_o = O.zero_step(p, st, [u16(g) for g in grads], oh)
+        assert rc_o == 0 and (scale < 1.0 or not clip)
+        torch.cuda.synchronize()
+        norms = set()
+        for rc in ranks:
+            q = rc.grp * K + rc.owner
+            assert rc.status() == 0
+            assert_state_close(f32(rc.master), st.master[q][:L], f"step {k} rank {rc.rank} master")
+            assert_state_close(f32(rc.m), st.mom[q][:L], f"step {k} rank {rc.rank} m")
+            assert_state_close(f32(rc.v), st.var[q][:L], f"step {k} rank {rc.rank} v")
+            if clip:
+                assert np.array_equal(f32(rc.ghat).view(np.uint32), st.ghat[q][:L].view(np.uint32))
+                gn, gs = rc.last_norm()
+                assert abs(gn - norm) <= 1e-7 * norm
+                norms.add((gn, gs))
+            assert bf16_ulp_diff(padded_to_unpadded(p, u16(rc.full)), full) <= 1
+        assert len(norms) <= 1
+    rc = ranks[0]
+    assert lib.zero_rank_partial_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), rc.part.data_ptr(), s) == -1
+    assert lib.zero_rank_partial_bucket(rc.ctx, -1, rc.recv.data_ptr(), rc.part.data_ptr(), s) == -1
+    for rc in ranks:
         rc.close()
 
 

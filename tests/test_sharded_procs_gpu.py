@@ -6,7 +6,7 @@ process runs the library's kernels on its own shard only. Three clipped steps on
 multi-bucket layout, at ZeRO-1 (full parameters kept) and ZeRO-3 (per-bucket gathers into a
 transient buffer), both forms of the clipped step, flat and hybrid with one rank per group;
 and three ZeRO-2 steps streamed bucket by bucket in backward order (step_streamed), unclipped
-and clipped. Every rank checks itself against the oracle's two-rank step: its shard of
+and clipped, flat and hybrid. Every rank checks itself against the oracle's two-rank step: its shard of
 master / m / v (1e-6 relative; bit-identical expected), the averaged gradient bit-exact when
 materialized, the norm within 1e-7 and equal on both ranks, the gathered bf16 parameters within
 1 ulp. Then the assembled checkpoint state equals the oracle's bit for bit, and both ranks
@@ -187,7 +187,8 @@ def _host_fed_steps(opt, p, st, world, rank, h, oh, dev, steps):
 @pytest.mark.parametrize("stage,ghat_mode,streamed,groups", [(1, "materialize", False, 1), (3, "recompute", False, 1),
                                                              (3, "materialize", False, 1), (2, "auto", True, 1),
                                                              (2, "materialize", "clipped", 1),
-                                                             (1, "materialize", False, 2), (3, "recompute", False, 2)])
+                                                             (1, "materialize", False, 2), (3, "recompute", False, 2),
+                                                             (2, "auto", True, 2), (2, "materialize", "clipped", 2)])
 def test_two_processes_on_one_gpu(stage, ghat_mode, streamed, groups):
     """groups=2: hybrid sharding with one rank per group (a replicated state whose exchange and
     all-gather are identities; the group partials still cross the process boundary)."""

@@ -134,6 +134,7 @@ SIGNATURES = {
     "zero_rank_step": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_rank_sumsq": (ctypes.c_int, [_P, _P, ctypes.POINTER(Hyper), _P, _P]),
     "zero_rank_partial": (ctypes.c_int, [_P, _P, _P, _P]),
+    "zero_rank_partial_bucket": (ctypes.c_int, [_P, ctypes.c_int64, _P, _P, _P]),
     "zero_rank_step_bucket": (ctypes.c_int, [_P, _I64, _P, ctypes.c_int, ctypes.POINTER(Hyper), _P]),
     "zero_rank_reduce_bucket": (ctypes.c_int, [_P, _I64, _P, _P]),
 }

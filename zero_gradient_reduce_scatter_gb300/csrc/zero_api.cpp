@@ -1130,10 +1130,11 @@ static int check_rank_ctx(const zero_ctx* c) {
     return ZERO_OK;
 }
 
-int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
+// The group partial of the whole shard (bucket < 0) or of one bucket's slice.
+static int rank_partial(zero_ctx* c, int64_t bucket, const void* recv, void* part, void* stream) {
     int rc = check_rank_ctx(c);
     if (rc) return rc;
-    if (!hybrid(c) || !recv || !part) return ZERO_ERR_INVALID_ARG;
+    if (!hybrid(c) || !recv || !part || bucket >= (int64_t)c->buckets.size()) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(recv) || !aligned16(part)) return ZERO_ERR_MISALIGNED;
     if (!dev_ptr_ok(c, recv) || !dev_ptr_ok(c, part)) return ZERO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);
@@ -1143,9 +1144,10 @@ int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
     // pass's partial sums of squares are not used
     zg::StepArgs a = rank_args(c);
     exchange_sources(c, a, recv, shard_count(&c->cfg));
+    if (bucket >= 0) one_bucket(c, a, bucket);
     a.inv_M = 1.0f;
     a.ghat = (float*)part;
-    const int g1 = grid_for(c, zg::kVarRsNormWriteX, a.nvec);
+    const int g1 = grid_for(c, zg::kVarRsNormWriteX, a.vend - a.vbeg);
     cudaError_t e;
     {
         Timed tm(c, ZERO_K_RS_NORM, s);
@@ -1154,6 +1156,15 @@ int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     c->last_stream = s;
     return ZERO_OK;
+}
+
+int zero_rank_partial(zero_ctx* c, const void* recv, void* part, void* stream) {
+    return rank_partial(c, -1, recv, part, stream);
+}
+
+int zero_rank_partial_bucket(zero_ctx* c, int64_t bucket, const void* recv, void* part, void* stream) {
+    if (bucket < 0) return ZERO_ERR_INVALID_ARG;
+    return rank_partial(c, bucket, recv, part, stream);
 }
 
 int zero_rank_sumsq(zero_ctx* c, const void* src, const zero_hyper* h, double* sumsq, void* stream) {
@@ -1271,7 +1282,7 @@ int zero_rank_reduce_bucket(zero_ctx* c, int64_t bucket, const void* src, void* 
     int rc = check_rank_ctx(c);
     if (rc) return rc;
     const int64_t nb = (int64_t)c->buckets.size();
-    if (hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
+    if (!src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
     if (!c->bufs.ghat) return ZERO_ERR_SIZE_MISMATCH;
     if (c->n_bucket_done || c->rank_reduced) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
@@ -1279,15 +1290,17 @@ int zero_rank_reduce_bucket(zero_ctx* c, int64_t bucket, const void* src, void* 
     DeviceGuard guard(c->device);
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
-    // the bucket's average into the ghat shard, its sum of squares into its slot
+    // the bucket's average into the ghat shard, its sum of squares into its slot: from the
+    // exchange buffer (flat) or the gathered group partials (hybrid)
     zg::StepArgs a = rank_args(c);
-    exchange_sources(c, a, src, c->cfg.M);
+    if (hybrid(c)) part_sources(c, a, src);
+    else exchange_sources(c, a, src, c->cfg.M);
     one_bucket(c, a, bucket);
-    const int g1 = grid_for(c, zg::kVarRsNormWriteX, a.vend - a.vbeg);
+    const int g1 = grid_for(c, hybrid(c) ? zg::kVarRsNormWriteF : zg::kVarRsNormWriteX, a.vend - a.vbeg);
     cudaError_t e;
     {
         Timed tm(c, ZERO_K_RS_NORM, s);
-        e = zg::launch_rs_norm_exchange(a, true, g1, s);
+        e = hybrid(c) ? zg::launch_rs_norm_f32src(a, true, g1, s) : zg::launch_rs_norm_exchange(a, true, g1, s);
     }
     if (e == cudaSuccess) {
         Timed tm(c, ZERO_K_NORM_FINAL, s);
@@ -1307,7 +1320,7 @@ int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stag
     if (stage != c->cfg.stage) return ZERO_ERR_STAGE;
     if ((rc = check_hyper(h))) return rc;
     const int64_t nb = (int64_t)c->buckets.size();
-    if (h->clip || hybrid(c) || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
+    if (h->clip || !src || bucket < 0 || bucket >= nb) return ZERO_ERR_INVALID_ARG;
     if (c->rank_reduced || c->n_reduced || c->bucket_done[(size_t)bucket]) return ZERO_ERR_INVALID_ARG;
     if (!aligned16(src)) return ZERO_ERR_MISALIGNED;
     if (!dev_ptr_ok(c, src)) return ZERO_ERR_INVALID_ARG;
@@ -1315,14 +1328,15 @@ int zero_rank_step_bucket(zero_ctx* c, int64_t bucket, const void* src, int stag
     if (!guard.ok) return cuda_fail(cudaErrorInvalidDevice);
     cudaStream_t s = (cudaStream_t)stream;
     zg::StepArgs a = rank_args(c);
-    exchange_sources(c, a, src, c->cfg.M);
+    if (hybrid(c)) part_sources(c, a, src);
+    else exchange_sources(c, a, src, c->cfg.M);
     one_bucket(c, a, bucket);
     a.k = adam_consts(h, c->t + 1);  // every bucket of the step takes step t + 1
-    const int g4 = grid_for(c, zg::kVarRsAdamwPlainX, a.vend - a.vbeg);
+    const int g4 = grid_for(c, hybrid(c) ? zg::kVarRsAdamwPlainF : zg::kVarRsAdamwPlainX, a.vend - a.vbeg);
     cudaError_t e;
     {
         Timed tm(c, ZERO_K_RS_ADAMW, s);
-        e = zg::launch_rs_adamw_exchange(a, false, g4, s);
+        e = hybrid(c) ? zg::launch_rs_adamw_f32src(a, false, g4, s) : zg::launch_rs_adamw_exchange(a, false, g4, s);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     c->bucket_done[(size_t)bucket] = 1;

@@ -212,6 +212,9 @@ class ShardedZeroOptimizer:
         self.scratch = torch.empty(s["bytes_scratch"], dtype=torch.uint8, device=dev)
         self.recv = None if self.identity else torch.empty(npad, dtype=torch.bfloat16, device=dev)
         self._src = self.recv  # where the kernels read this step's exchanged slices
+        self._bases = [0]  # each bucket's first lane in the shard
+        for b in self.buckets[:-1]:
+            self._bases.append(self._bases[-1] + b[2])
         self._consumed = {}  # device gradient buffer -> event after the last step that read it
         self._d2h_stream = None  # parameter copies to host (step_host_overlapped)
         self._params_out = None  # event after the last of them
@@ -317,10 +320,32 @@ class ShardedZeroOptimizer:
                          [grad[off:off + lanes]], [self.recv[off:off + lanes]])
         return None
 
+    def _bucket_source(self, bucket: int) -> torch.Tensor:
+        """What the per-bucket kernels read once bucket `bucket`'s exchange has landed: the
+        exchanged slices (flat), or, with hybrid sharding, the gathered group partials after
+        this bucket's partial has crossed the groups (its region only)."""
+        if self.groups == 1:
+            return self._src
+        _check(_lib().zero_rank_partial_bucket(self._ctx, bucket, self._src.data_ptr(), self.part.data_ptr(),
+                                               _stream_handle(None)), "zero_rank_partial_bucket")
+        self._gather_partials_bucket(bucket)
+        return self.parts
+
+    def _gather_partials_bucket(self, bucket: int):
+        """The cross-group all-gather of bucket `bucket`'s group partial: every group's slice
+        of it into that group's block of the partials (the bucket's region only)."""
+        import torch.distributed as dist
+        base, S, L = self._bases[bucket], self.buckets[bucket][2], self.sizes["shard_len"]
+        outs = [self.parts[g * L + base:g * L + base + S] for g in range(self.groups)]
+        self._collective(f"partials{bucket}", lambda x, *o: dist.all_gather(list(o), x, group=self.cross),
+                         [self.part[base:base + S]], outs)
+
     def step_bucket(self, bucket: int, hyper: Hyper):
-        """Bucket `bucket`'s update from its exchanged slices (no clipping): zero_rank_step_bucket.
-        The step completes once every bucket has been stepped."""
-        _check(_lib().zero_rank_step_bucket(self._ctx, bucket, self._src.data_ptr(), self.stage, ctypes.byref(hyper),
+        """Bucket `bucket`'s update once its exchange has landed (no clipping):
+        zero_rank_step_bucket, with hybrid sharding after the bucket's group partial has
+        crossed the groups. The step completes once every bucket has been stepped."""
+        src = self._bucket_source(bucket)
+        _check(_lib().zero_rank_step_bucket(self._ctx, bucket, src.data_ptr(), self.stage, ctypes.byref(hyper),
                                             _stream_handle(None)), "zero_rank_step_bucket")
 
     def gather_bucket_into_full(self, bucket: int, async_op: bool = False):
@@ -331,7 +356,7 @@ class ShardedZeroOptimizer:
             return gather_params(self.param_shards, self.param_full, self.buckets, self.K, self.intra, [bucket],
                                  True)[0]
         off, _n, S, _ = self.buckets[bucket]
-        base = sum(b[2] for b in self.buckets[:bucket])
+        base = self._bases[bucket]
         self._collective(f"gather{bucket}",
                          lambda sh, f: gather_params(sh, f, [(0, 0, S, 0)], self.K, self.intra),
                          [self.param_shards[base:base + S]], [self.param_full[off:off + self.K * S]])
@@ -344,11 +369,10 @@ class ShardedZeroOptimizer:
         landed while later ones are still in flight. Without clipping each bucket is updated
         then, and its all-gather follows; with clipping each bucket is reduced into the ghat
         buffer (required) with its sum of squares, then the sums are gathered and the shard is
-        updated from the average. order: the buckets' order (default: layout order; backward
-        passes produce them in reverse). Results equal step()'s."""
+        updated from the average. With hybrid sharding each bucket's group partial crosses the
+        groups before the bucket is handled. order: the buckets' order (default: layout order;
+        backward passes produce them in reverse). Results equal step()'s."""
         self._check_grad(grad)
-        if self.groups > 1:
-            raise ValueError("step_streamed is the flat mode's form")
         if hyper.clip and self.ghat is None:
             raise ValueError("the clipped streamed step keeps the average in a ghat buffer (ghat_buffer=True)")
         lib, ctx, s = _lib(), self._ctx, _stream_handle(None)
@@ -359,7 +383,8 @@ class ShardedZeroOptimizer:
             if wk is not None:
                 wk.wait()
             if hyper.clip:
-                _check(lib.zero_rank_reduce_bucket(ctx, b, self._src.data_ptr(), s), "zero_rank_reduce_bucket")
+                src = self._bucket_source(b)
+                _check(lib.zero_rank_reduce_bucket(ctx, b, src.data_ptr(), s), "zero_rank_reduce_bucket")
                 continue
             self.step_bucket(b, hyper)
             if gather and self.param_full is not None:
