@@ -209,6 +209,14 @@ def main():
             assert zg._lib().zero_check_report(rc_.ctx, ctypes.byref(site), ctypes.byref(idx)) == 0
             assert site.value == 0, f"rank {rc_.rank} {kw}: bounds check {site.value} failed at {idx.value}"
             rc_.close()
+    # hybrid sharding streamed bucket by bucket (per-bucket partials, bucket-restricted
+    # fp32-source passes), unclipped and clipped
+    for args in ((2, 4, 2, False), (2, 8, 3, True)):
+        for rc_ in TS._run_hybrid_streamed(*args):
+            site, idx = ctypes.c_int64(), ctypes.c_int64()
+            assert zg._lib().zero_check_report(rc_.ctx, ctypes.byref(site), ctypes.byref(idx)) == 0
+            assert site.value == 0, f"rank {rc_.rank} {args}: bounds check {site.value} failed at {idx.value}"
+            rc_.close()
     print("checked build: all scenarios clean")
 
 

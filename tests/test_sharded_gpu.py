@@ -299,6 +299,11 @@ def test_sharded_largest_rank_count():
 @pytest.mark.parametrize("groups,M,stage,clip", [(2, 4, 2, False), (4, 8, 1, False), (4, 4, 2, False),
                                                   (2, 8, 3, True), (2, 4, 1, True)])
 def test_sharded_hybrid_streamed_per_bucket(groups, M, stage, clip):
+    for rc in _run_hybrid_streamed(groups, M, stage, clip):
+        rc.close()
+
+
+def _run_hybrid_streamed(groups, M, stage, clip):
     """Hybrid sharding streamed bucket by bucket, buckets in reverse order. Per bucket: the
     group partial of that bucket only (zero_rank_partial_bucket), the cross-group gather of
     that bucket's region only, then the bucket's update (unclipped, zero_rank_step_bucket) or
@@ -363,8 +368,7 @@ def test_sharded_hybrid_streamed_per_bucket(groups, M, stage, clip):
     rc = ranks[0]
     assert lib.zero_rank_partial_bucket(rc.ctx, p.nb, rc.recv.data_ptr(), rc.part.data_ptr(), s) == -1
     assert lib.zero_rank_partial_bucket(rc.ctx, -1, rc.recv.data_ptr(), rc.part.data_ptr(), s) == -1
-    for rc in ranks:
-        rc.close()
+    return ranks
 
 
 def test_sharded_clipped_streaming_reduce_then_apply():
