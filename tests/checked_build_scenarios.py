@@ -61,9 +61,9 @@ def main():
         pass
     clean(opt, "per-bucket gathers")
 
-    for M in (3, 64):
+    for M in (1, 3, 64):  # the one-source kernel (its own block size), the generic one
         exact(run_elementwise(W.small_variant(W.workload("ragged"), (3001, 17, 1), M=M, steps=2), gather="shards"),
-              f"generic M={M}")
+              f"M={M}")
     exact(run_elementwise(W.small_variant(W.workload("ragged"), (3,), steps=2), gather="shards"), "3 lanes, 16 ranks")
 
     wg = W.small_variant(W.workload("ragged"), W.ragged_numel(30, 200, 5000, 23), M=8, stage=3, steps=2)
@@ -202,7 +202,8 @@ def main():
                {"M": 3, "stage": 1, "clip": True, "ghat_mode": "recompute"},
                {"M": 4, "stage": 2, "clip": False},
                {"M": 4, "stage": 1, "clip": True, "groups": 2},
-               {"M": 8, "stage": 3, "clip": False, "groups": 2}):
+               {"M": 8, "stage": 3, "clip": False, "groups": 2},
+               {"M": 1, "stage": 2, "clip": True}):
         ranks, _, _ = TS._run(TS.RAGGED, bucket_bytes=6000, steps=2, **kw)
         for rc_ in ranks:
             site, idx = ctypes.c_int64(), ctypes.c_int64()
