@@ -1,6 +1,6 @@
 """The bounds-checked build (-DZERO_CHECKED) over every kernel path.
 
-compute-sanitizer is closed on this machine; instead the checked library tests each global
+compute-sanitizer is not used; instead the checked library tests each global
 index against its buffer before the access and records the first failure (site, index) in
 the status word without trapping. tests/checked_build_scenarios.py drives every kernel path
 (misaligned fused all-gather stores, shards and per-bucket gathers, generic rank counts,

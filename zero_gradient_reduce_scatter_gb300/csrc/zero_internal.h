@@ -108,7 +108,7 @@ constexpr int kThreadsRsNormWrite = 256;  // norm pass that also writes the aver
 constexpr int kThreadsRsAdamw = 512;
 // The one-source fused kernel (M = 1) launches fewer threads into the same one CTA per SM:
 // 14 warps per SM ran it at 96-98% of the copy peak against 92-94% with 16, and 12, 10 and
-// 24 warps were slower again (A/B runs on one box each); with more sources 14 warps lost.
+// 24 warps were slower again (A/B runs, each on one GPU); with more sources 14 warps lost.
 constexpr int kThreadsRsAdamwOne = 448;
 constexpr int rs_adamw_threads(int M) { return M == 1 ? kThreadsRsAdamwOne : kThreadsRsAdamw; }
 constexpr int kThreadsAdamw = 512;
@@ -128,7 +128,7 @@ enum CachePolicy : int {
     kCacheGlobal = 3,     // ld/st.global.cg: L2 only
 };
 // Chosen by a sweep of all load x store combinations on GB300 (full 4B, 1.3B, ragged and
-// GPT-2-small workloads, two runs each on one box). The fused kernel: plain loads and stores
+// GPT-2-small workloads, two runs each on one GPU). The fused kernel: plain loads and stores
 // 25.23 ms per 4B step against 25.53 with evict-first ones (ld.ca + st.cg within noise);
 // evict-first loads with plain stores lost 10%. AdamW from the average: ld.ca loads and plain
 // stores 9.55 ms per 1.3B step against 9.73; the same pair cost the fused kernel 5%, so each
