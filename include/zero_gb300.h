@@ -22,7 +22,9 @@
  *    zero_strerror() gives the text. No call aborts or throws.
  *  - Memory: the library allocates no device memory. The caller allocates every device
  *    buffer in the sizes zero_plan() reports and keeps it alive while a context uses it;
- *    the context only borrows the pointers. The context owns host tables, CUDA events for
+ *    the context only borrows the pointers. A pointer that a call passes to the kernels must be device
+ *    memory of the context's GPU (or managed memory); anything else is refused with
+ *    ZERO_ERR_INVALID_ARG before work is enqueued. The context owns host tables, CUDA events for
  *    optional kernel timing, and nothing else.
  *  - Streams: work is enqueued on the caller's stream (a cudaStream_t passed as void*; NULL
  *    is the legacy default stream). Calls return once the work is enqueued; only zero_init,
@@ -303,6 +305,9 @@ int zero_step_host_overlapped(zero_ctx* ctx, const void* const* host_grads, void
  * all-gathered across the G groups in group order (among ranks k, K + k, ...) into
  * parts[G * shard_len]; the step sums them in group order and multiplies by (float)(1/M)
  * -- the all-reduce across groups, in a fixed order. (2) gathers the K sums of one group.
+ * Streamed bucket by bucket, each bucket goes through the same steps on its own region:
+ * zero_rank_partial_bucket, the cross-group all-gather of that bucket's partials, then
+ * zero_rank_step_bucket or zero_rank_reduce_bucket.
  *
  * Buffers in this mode (zero_plan reports these sizes when cfg->sharded = 1):
  *   master, m, v  fp32 [shard_len]: this rank's shard of the state (required)
