@@ -22,10 +22,10 @@
  *    zero_strerror() gives the text. No call aborts or throws.
  *  - Memory: the library allocates no device memory. The caller allocates every device
  *    buffer in the sizes zero_plan() reports and keeps it alive while a context uses it;
- *    the context only borrows the pointers. A pointer that a call passes to the kernels must be device
- *    memory of the context's GPU (or managed memory); anything else is refused with
- *    ZERO_ERR_INVALID_ARG before work is enqueued. The context owns host tables, CUDA events for
- *    optional kernel timing, and nothing else.
+ *    the context only borrows the pointers. A pointer that a call passes to the kernels
+ *    must be device memory of the context's GPU (or managed memory); anything else is
+ *    refused with ZERO_ERR_INVALID_ARG before work is enqueued. The context owns host
+ *    tables, CUDA events for optional kernel timing, and nothing else.
  *  - Streams: work is enqueued on the caller's stream (a cudaStream_t passed as void*; NULL
  *    is the legacy default stream). Calls return once the work is enqueued; only zero_init,
  *    zero_last_norm(), zero_sync_status(), zero_check_report() and zero_kernel_times() wait
